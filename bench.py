@@ -1,0 +1,417 @@
+"""Benchmark of the POET-X transformed linear on B300: one JSON line.
+
+A step is one pass of the whole hot path on one batch: the Cayley-Neumann
+blocks of both sides, the forward y = R (W0 (P x)) and the backward to dX and
+the packed skew gradients, on the square 2048-wide layer (d_in = d_out = 2048,
+8 + 8 blocks of b = 256, n = 3, 8192 bf16 tokens).  ``value`` is tokens/s with
+the inputs resident in HBM; ``e2e`` is the same step through the C ABI with
+host buffers (pinned host -> device copies of x and dy, device -> host copies
+of y, dX and both skew gradients inside the timed region).
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl poetx|reference]
+For N > 1 launch one rank per GPU with torch.distributed.run; each rank runs
+its own batch (weak scaling) and the packed skew gradients are all-reduced,
+the data-parallel exchange of the method.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from orthogonal_equivalence_neumann_b300 import TransformedLinear, _lib, inputs  # noqa: E402
+
+METRIC = "transformed-linear tokens/s (fwd+bwd) and Cayley-Neumann blocks/s; % of roofline"
+CASE = inputs.SQUARE_2048
+ROTATE = 4            # input sets cycled over the steps: 4 x (x + dy) = 268 MB > 126 MB L2
+CPU_SAMPLE_TOKENS = 2048
+REF_SAMPLE_TOKENS = 512
+
+# Peak of the fp32 FFMA pipes: 148 SMs x 128 lanes x 2 flop x 2.032 GHz.
+ALU_FP32_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+def kernel_work(case):
+    """Algorithmic work per launch of each kernel for one step of `case`:
+    name -> (bound, flops per launch, bytes per launch)."""
+    T, di, do, bi, bo, n = case.T, case.d_in, case.d_out, case.b_in, case.b_out, case.n
+    es = 2 if case.dtype == "bf16" else 4
+    nbi, nbo = di // bi, do // bo
+    gemm_flops = 2.0 * T * di * do
+    gemm_bytes = es * (T * di + di * do + T * do)
+    blk_flops = (2.0 * T * di * bi + 2.0 * T * do * bo) / 2      # mean over the P and R sides
+    blk_bytes = es * (2 * T * di + 2 * T * do) / 2
+    dq_flops = (2.0 * T * di * bi + 2.0 * T * do * bo) / 2
+    dq_bytes = es * (2 * T * di + 2 * T * do) / 2 + 4 * (di * bi + do * bo) / 2
+    cnp_f = (2.0 * n * bi ** 3 * nbi + 2.0 * n * bo ** 3 * nbo) / 2
+    cnp_fb = 4 * (nbi * bi * (bi - 1) / 2 + nbo * bo * (bo - 1) / 2) / 2 + es * (nbi * bi * bi + nbo * bo * bo) / 2
+    cnpb_f = 3 * cnp_f
+    cnpb_b = 4 * (nbi * bi * bi + nbo * bo * bo) / 2 + 8 * (nbi * bi * (bi - 1) / 2 + nbo * bo * (bo - 1) / 2) / 2
+    return {
+        "gemm_simt": ("alu", gemm_flops, gemm_bytes),
+        "block_apply_simt": ("alu", blk_flops, blk_bytes),
+        "dq_simt": ("alu", dq_flops, dq_bytes),
+        "cnp_fwd_simt": ("alu", cnp_f, cnp_fb),
+        "cnp_bwd_simt": ("alu", cnpb_f, cnpb_b),
+    }
+
+
+def step_flops(case):
+    T, di, do, bi, bo, n = case.T, case.d_in, case.d_out, case.b_in, case.b_out, case.n
+    fwd = 2.0 * T * di * do + 2.0 * T * di * bi + 2.0 * T * do * bo
+    bwd = fwd + 2.0 * T * di * bi + 2.0 * T * do * bo
+    return fwd + bwd
+
+
+def read_traffic(kernel):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if the
+    kernel's source is unchanged since the capture (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    for line in open(p):
+        parts = line.split("#", 1)[0].split()
+        if len(parts) == 4 and parts[0] == kernel:
+            src, sha, nbytes = parts[1], parts[2], parts[3]
+            path = os.path.join(ROOT, src)
+            if os.path.exists(path) and hashlib.sha1(open(path, "rb").read()).hexdigest()[:12] == sha:
+                return float(nbytes)
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def allreduce_grads(layer, world):
+    """The data-parallel exchange: sum the packed skew gradients over ranks."""
+    if world == 1:
+        return
+    import torch.distributed as dist
+    dist.all_reduce(layer.dtheta_P)
+    dist.all_reduce(layer.dtheta_R)
+
+
+def oracle_step_seconds(case, T_sample, inp):
+    """Time the CPU oracle (as it stands) on the first T_sample tokens: Cayley-
+    Neumann of both sides, forward, backward to dX and dtheta."""
+    import oracle
+    x = inp["x"][:T_sample].float().double().numpy()
+    dy = inp["dy"][:T_sample].float().double().numpy()
+    W0 = inp["W0"].float().double().numpy()
+    t0 = time.perf_counter()
+    oracle.layer(x, W0, inp["theta_P"].double().numpy(), inp["theta_R"].double().numpy(), case.n,
+                 inp["perm_in"].numpy(), inp["perm_out"].numpy(), case.b_in, case.b_out, dy=dy)
+    return time.perf_counter() - t0
+
+
+def host_cores():
+    return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle on a bounded token sample per step."""
+    if rank != 0:
+        return
+    inp = inputs.make_linear_inputs(CASE)
+    for _ in range(args.warmup):
+        oracle_step_seconds(CASE, REF_SAMPLE_TOKENS, inp)
+    ts = [oracle_step_seconds(CASE, REF_SAMPLE_TOKENS, inp) for _ in range(args.steps)]
+    total = sum(ts)
+    value = REF_SAMPLE_TOKENS * args.steps / total
+    sample = "first %d of %d tokens of the square 2048 layer per step" % (REF_SAMPLE_TOKENS, CASE.T)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(world),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": host_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(world):
+    return {"workload": "square_d2048_b256_n3_T8192 (POET-X transformed linear fwd+bwd)",
+            "d_in": CASE.d_in, "d_out": CASE.d_out, "b": CASE.b_in, "n": CASE.n,
+            "tokens_per_gpu": CASE.T, "global_batch_tokens": CASE.T * world,
+            "parallelism": "dp%d" % world,
+            "l2": "inputs rotate over %d sets of x and dy (%d MB > 126 MB L2)" % (
+                ROTATE, ROTATE * 2 * CASE.T * CASE.d_in * 2 // 2 ** 20)}
+
+
+def cnp_points(dev):
+    """Cayley-Neumann generation throughput at 4096 blocks, n = 3, sigma = 1e-2."""
+    out = {}
+    for b in (32, 64, 128, 256):
+        th = inputs.make_theta(4096, b, 1e-2, inputs.sweep_seed(b, 1e-2, 3)).to(dev)
+        for dt, nm in ((torch.float32, "f32"), (torch.bfloat16, "bf16")):
+            Q = torch.empty(4096, b, b, dtype=dt, device=dev)
+            for _ in range(2):
+                _lib.poetx_cayley_neumann(th, b, 3, Q)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 5
+            torch.cuda.synchronize()
+            e0.record()
+            for _ in range(reps):
+                _lib.poetx_cayley_neumann(th, b, 3, Q)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            out["b%d_%s" % (b, nm)] = round(4096 / (ms * 1e-3))
+        del th, Q
+    return out
+
+
+def run_poetx(args, world, rank, local):
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+    case = CASE
+    inp = inputs.make_linear_inputs(case)
+    lay = TransformedLinear(inp["W0"].to(dev), inp["theta_P"], inp["theta_R"], inp["perm_in"],
+                            inp["perm_out"], case.b_in, case.b_out, case.n, T_max=case.T,
+                            save_z=True, device=dev)
+    # rotating input sets: set 0 is the seeded draw; the others are seeded device draws
+    gen = torch.Generator(device=dev).manual_seed(4242 + rank)
+    xs = [inp["x"].to(dev)] + [torch.randn(case.T, case.d_in, generator=gen, device=dev).to(
+        torch.bfloat16) for _ in range(ROTATE - 1)]
+    dys = [inp["dy"].to(dev)] + [torch.randn(case.T, case.d_out, generator=gen, device=dev).to(
+        torch.bfloat16) for _ in range(ROTATE - 1)]
+    y = torch.empty(case.T, case.d_out, dtype=torch.bfloat16, device=dev)
+    dX = torch.empty(case.T, case.d_in, dtype=torch.bfloat16, device=dev)
+
+    def step(k):
+        lay.step(xs[k % ROTATE], dys[k % ROTATE], y, dX)
+        allreduce_grads(lay, world)
+
+    for k in range(args.warmup):
+        step(k)
+    _lib.poetx_stream_status()
+    torch.cuda.synchronize()
+    _lib.poetx_profile_report()   # drop anything recorded so far
+
+    # ---------------- timed region (device-resident inputs)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        _lib.poetx_profile_enable(True)
+        barrier(world)
+        torch.cuda.synchronize()
+        n0 = _lib.poetx_launch_count()
+        e0.record(stream)
+        for k in range(args.steps):
+            step(k)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        launches = _lib.poetx_launch_count() - n0
+        _lib.poetx_profile_enable(False)
+    _lib.poetx_stream_status()
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
+    ms_per_step = ms / args.steps
+    value = world * case.T * args.steps / (ms * 1e-3)
+    prof = _lib.poetx_profile_report()
+
+    # ---------------- roofline of the dominant kernel
+    work = kernel_work(case)
+    dom = max(prof.items(), key=lambda kv: kv[1][1])
+    dname, (dcnt, dms) = dom
+    bound, flops, nbytes = work.get(dname, ("alu", float("nan"), float("nan")))
+    avg_s = dms / dcnt * 1e-3
+    if bound == "tensor":
+        peak = peaks["bf16_tflops"]
+        achieved, unit = flops / avg_s / 1e12, "TFLOP/s"
+    elif bound == "hbm":
+        peak = peaks["hbm_gbs"]
+        achieved, unit = nbytes / avg_s / 1e9, "GB/s"
+    else:
+        peak = ALU_FP32_PEAK_TFLOPS
+        achieved, unit = flops / avg_s / 1e12, "TFLOP/s"
+    total_ms = sum(v[1] for v in prof.values())
+    roofline = {"bound": bound, "kernel": dname, "achieved": round(achieved, 2),
+                "peak": round(peak, 1), "unit": unit, "frac": round(achieved / peak, 4),
+                "traffic": read_traffic(dname),
+                "peak_source": "fp32 FFMA 148x128x2x2.032GHz" if bound == "alu" else peaks["source"],
+                "share": round(dms / total_ms, 4) if total_ms else None,
+                "kernels": {k: {"launches": v[0], "ms": round(v[1], 4)} for k, v in prof.items()}}
+
+    # ---------------- end to end through host buffers
+    h_x = [t.cpu().pin_memory() for t in xs[:2]]
+    h_dy = [t.cpu().pin_memory() for t in dys[:2]]
+    d_x = torch.empty_like(xs[0])
+    d_dy = torch.empty_like(dys[0])
+    h_y = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    h_dX = torch.empty(dX.shape, dtype=dX.dtype).pin_memory()
+    h_tp = torch.empty(lay.dtheta_P.shape, dtype=torch.float32).pin_memory()
+    h_tr = torch.empty(lay.dtheta_R.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step(k):
+        d_x.copy_(h_x[k % 2], non_blocking=True)
+        d_dy.copy_(h_dy[k % 2], non_blocking=True)
+        lay.step(d_x, d_dy, y, dX)
+        allreduce_grads(lay, world)
+        h_y.copy_(y, non_blocking=True)
+        h_dX.copy_(dX, non_blocking=True)
+        h_tp.copy_(lay.dtheta_P, non_blocking=True)
+        h_tr.copy_(lay.dtheta_R, non_blocking=True)
+
+    for k in range(2):
+        e2e_step(k)
+    torch.cuda.synchronize()
+    barrier(world)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for k in range(args.steps):
+        e2e_step(k)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), world)
+    h2d = (d_x.numel() + d_dy.numel()) * 2
+    d2h = (y.numel() + dX.numel()) * 2 + 4 * (h_tp.numel() + h_tr.numel())
+    e2e = {"value": world * case.T * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cnp = cnp_points(dev) if rank == 0 else None
+
+    # ---------------- CPU oracle baseline (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs = oracle_step_seconds(case, CPU_SAMPLE_TOKENS, inp)
+        cpu = {"value": CPU_SAMPLE_TOKENS / secs, "unit": "tokens/s", "cores": host_cores(),
+               "kind": "oracle",
+               "sample": "first %d of %d tokens of one step (CNP both sides, fwd, bwd), f64, %.1f s"
+                         % (CPU_SAMPLE_TOKENS, case.T, secs)}
+
+    if rank == 0:
+        flops = step_flops(case)
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": workload_config(world),
+            "step_tflops": round(flops / (ms_per_step * 1e-3) / 1e12 / 1, 2),
+            "step_frac_of_bf16_peak": round(flops / (ms_per_step * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "cnp_blocks_per_s": cnp, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": int(launches), "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="poetx", choices=["poetx", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py: no CUDA device (the library has no CPU path)")
+        run_poetx(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -102,7 +102,7 @@ poetx_status poetx_invert_perm(const int32_t *perm, int32_t *inv, int d, cudaStr
 /* Validator: returns POETX_OK if perm holds each of 0..d-1 exactly once and,
  * when inv is not NULL, inv[perm[i]] == i for all i; POETX_ERR_NOT_PERMUTATION
  * otherwise.  Synchronises `stream` (it returns a verdict).  `scratch` is a
- * device buffer of at least d int32 (overwritten). */
+ * device buffer of at least d + 1 int32 (overwritten). */
 poetx_status poetx_check_perm(const int32_t *perm, const int32_t *inv, int d, int32_t *scratch,
                               cudaStream_t stream);
 
@@ -166,6 +166,25 @@ poetx_status poetx_backward(const void *x, const void *dy, const void *W0m, cons
  * a CUDA error (POETX_ERR_CUDA) or an expired device-side wait
  * (POETX_ERR_TIMEOUT).  Clears the device error word. */
 poetx_status poetx_stream_status(cudaStream_t stream);
+
+
+/* ------------------------------------------------------------------------ */
+/* Measurement (host-side; off by default)                                  */
+/* ------------------------------------------------------------------------ */
+
+/* Number of kernels this library has launched since it was loaded. */
+unsigned long long poetx_launch_count(void);
+
+/* While enabled, every kernel launch of the library is bracketed by a pair of
+ * CUDA events recorded on the launch's own stream (no device memory is
+ * allocated; events are recycled).  Returns POETX_OK. */
+poetx_status poetx_profile_enable(int enable);
+
+/* Waits for the recorded events and writes one line per kernel name,
+ * "<name> <launches> <total_ms>\n", into buf (host memory, NUL-terminated,
+ * truncated to len); then forgets them.  Returns the full report length, or
+ * -1 if an event could not be read. */
+int poetx_profile_report(char *buf, size_t len);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,27 @@
+// tc.cuh -- tensor-core (tcgen05 / TMEM / TMA) path for sm_103a: host-side entry points.
+#pragma once
+
+#include "poetx.h"
+
+namespace poetx {
+
+// Cayley-Neumann forward on the tensor cores.
+bool tc_cnp_supported(int b, poetx_dtype out_dtype);
+poetx_status tc_cnp_fwd(const float* theta, int nb, int b, int n, void* Q, poetx_dtype out_dtype,
+                        cudaStream_t s);
+
+// Transformed linear (bf16 activations, fp32 accumulation) on the tensor cores.
+bool tc_linear_supported(int d_in, int d_out, int b_in, int b_out, poetx_dtype dt);
+size_t tc_workspace_bytes(int T, int d_in, int d_out, int b_in, int b_out, poetx_dtype dt,
+                          bool backward);
+poetx_status tc_forward(const void* x, const void* W0m, const void* Q_P, const void* Q_R,
+                        const int32_t* perm_in, const int32_t* inv_in, const int32_t* perm_out,
+                        const int32_t* inv_out, int T, int d_in, int d_out, int b_in, int b_out,
+                        void* u, void* z, void* y, void* ws, cudaStream_t s);
+poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const void* Q_P,
+                         const void* Q_R, const void* z, const int32_t* perm_in,
+                         const int32_t* inv_in, const int32_t* perm_out, const int32_t* inv_out,
+                         int T, int d_in, int d_out, int b_in, int b_out, void* dX, void* gz,
+                         void* gu, float* dqp, float* dqr, void* ws, cudaStream_t s);
+
+}  // namespace poetx

@@ -1,0 +1,85 @@
+"""One POET-X transformed linear held on the GPU, driven through the C ABI.
+
+``TransformedLinear`` owns the device buffers of one layer (merged weight,
+permutations and their inverses, skew parameters, the Cayley-Neumann blocks,
+the saved activation and the workspace) and calls the C entry points in the
+order of one training step:
+
+  1. poetx_cayley_neumann for P and R      [POET-X §2.D]
+  2. poetx_forward   y = R (W0 (P x))      [POET-X §2.A-§2.C]
+  3. poetx_backward  dX, dtheta_P, dtheta_R
+
+(source: "POET-X: Memory-efficient LLM Training by Scaling Orthogonal
+Transformation", gist.science summary, section 2).  PyTorch only allocates
+the buffers and supplies the stream; every step runs in the library's kernels.
+"""
+import torch
+
+from . import _lib
+
+
+class TransformedLinear:
+    def __init__(self, W0, theta_P, theta_R, perm_in, perm_out, b_in, b_out, n, T_max,
+                 save_z=True, device="cuda"):
+        dev = torch.device(device)
+        self.dtype = W0.dtype
+        self.d_out, self.d_in = W0.shape
+        self.b_in, self.b_out, self.n = int(b_in), int(b_out), int(n)
+        self.T_max = int(T_max)
+        self.save_z = save_z
+        self.W0 = W0.to(dev).contiguous()
+        self.theta_P = theta_P.to(dev, torch.float32).contiguous()
+        self.theta_R = theta_R.to(dev, torch.float32).contiguous()
+        self.perm_in = perm_in.to(dev, torch.int32).contiguous()
+        self.perm_out = perm_out.to(dev, torch.int32).contiguous()
+        self.inv_in = torch.empty_like(self.perm_in)
+        self.inv_out = torch.empty_like(self.perm_out)
+        _lib.poetx_invert_perm(self.perm_in, self.inv_in)
+        _lib.poetx_invert_perm(self.perm_out, self.inv_out)
+        # [§2.B] merge the two inner permutations into W0 once (per inner loop)
+        self.W0m = torch.empty_like(self.W0)
+        _lib.poetx_merge_w0(self.W0, self.W0m, self.perm_out, self.perm_in)
+        nbi, nbo = self.d_in // self.b_in, self.d_out // self.b_out
+        self.Q_P = torch.empty(nbi, self.b_in, self.b_in, dtype=self.dtype, device=dev)
+        self.Q_R = torch.empty(nbo, self.b_out, self.b_out, dtype=self.dtype, device=dev)
+        self.dtheta_P = torch.empty_like(self.theta_P)
+        self.dtheta_R = torch.empty_like(self.theta_R)
+        ws = _lib.poetx_workspace_bytes(self.T_max, self.d_in, self.d_out, self.b_in, self.b_out,
+                                        self.dtype)
+        if ws == 0:
+            raise ValueError("invalid layer sizes")
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+        self.z = (torch.empty(self.T_max, self.d_out, dtype=self.dtype, device=dev)
+                  if save_z else None)
+
+    def cayley_neumann(self):
+        _lib.poetx_cayley_neumann(self.theta_P, self.b_in, self.n, self.Q_P)
+        _lib.poetx_cayley_neumann(self.theta_R, self.b_out, self.n, self.Q_R)
+
+    def forward(self, x, y=None):
+        T = x.shape[0]
+        if y is None:
+            y = torch.empty(T, self.d_out, dtype=self.dtype, device=x.device)
+        z = self.z[:T] if self.z is not None else None
+        _lib.poetx_forward(x, self.W0m, self.Q_P, self.Q_R, self.perm_in, self.inv_in,
+                           self.perm_out, self.inv_out, self.b_in, self.b_out, y, z,
+                           self.workspace)
+        return y
+
+    def backward(self, x, dy, dX=None):
+        T = x.shape[0]
+        if dX is None:
+            dX = torch.empty(T, self.d_in, dtype=self.dtype, device=x.device)
+        z = self.z[:T] if self.z is not None else None
+        _lib.poetx_backward(x, dy, self.W0m, self.theta_P, self.theta_R, self.n, self.Q_P,
+                            self.Q_R, z, self.perm_in, self.inv_in, self.perm_out, self.inv_out,
+                            self.b_in, self.b_out, dX, self.dtheta_P, self.dtheta_R,
+                            self.workspace)
+        return dX, self.dtheta_P, self.dtheta_R
+
+    def step(self, x, dy, y=None, dX=None):
+        """One pass of the whole hot path: CNP of both sides, forward, backward."""
+        self.cayley_neumann()
+        y = self.forward(x, y)
+        dX, dtp, dtr = self.backward(x, dy, dX)
+        return y, dX, dtp, dtr

@@ -1,0 +1,254 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Bars (relative Frobenius error ||gpu - oracle||_F / ||oracle||_F per output):
+fp32 paths <= 1e-5; bf16-input / fp32-accumulate paths <= 2e-2; permutation
+indices and the merged weight bit-exact.  The oracle reads exactly the values
+the GPU reads (bf16 inputs widened exactly to double) and rounds nothing.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from orthogonal_equivalence_neumann_b300 import TransformedLinear, _lib, inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL_F32 = 1e-5
+TOL_BF16 = 2e-2
+
+
+def to64(t):
+    return t.detach().to("cpu", torch.float32).double().numpy()
+
+
+def tol_for(dtype):
+    return TOL_F32 if dtype in ("f32", torch.float32) else TOL_BF16
+
+
+def assert_close(name, got, ref, tol):
+    err = oracle.rel_fro(got, ref)
+    assert err <= tol, "%s: relative Frobenius error %.3e > %.1e" % (name, err, tol)
+    return err
+
+
+def gpu_layer(case, inp, save_z=True, T=None):
+    x = inp["x"].cuda()
+    dy = inp["dy"].cuda()
+    lay = TransformedLinear(inp["W0"].cuda(), inp["theta_P"], inp["theta_R"], inp["perm_in"],
+                            inp["perm_out"], case.b_in, case.b_out, case.n,
+                            T_max=max(1, x.shape[0]), save_z=save_z)
+    y, dX, dtp, dtr = lay.step(x, dy)
+    _lib.poetx_stream_status()
+    torch.cuda.synchronize()
+    return dict(y=to64(y), dX=to64(dX), dtheta_P=dtp.double().cpu().numpy(),
+                dtheta_R=dtr.double().cpu().numpy(), Q_P=to64(lay.Q_P), Q_R=to64(lay.Q_R))
+
+
+def oracle_inputs(inp):
+    return dict(x=to64(inp["x"]), W0=to64(inp["W0"]), dy=to64(inp["dy"]),
+                thP=inp["theta_P"].double().numpy(), thR=inp["theta_R"].double().numpy(),
+                pi=inp["perm_in"].numpy(), po=inp["perm_out"].numpy())
+
+
+def oracle_layer(case, inp, rows=None):
+    """Oracle outputs; y and dX only for `rows` (all when None); dtheta over all tokens."""
+    o = oracle_inputs(inp)
+    QP = oracle.cnp(o["thP"], case.b_in, case.n)
+    QR = oracle.cnp(o["thR"], case.b_out, case.n)
+    xr = o["x"] if rows is None else o["x"][rows]
+    y = oracle.forward(xr, o["W0"], QP, QR, o["pi"], o["po"])
+    dX, dQP, dQR = oracle.backward(o["x"], o["dy"], o["W0"], QP, QR, o["pi"], o["po"])
+    return dict(y=y, dX=dX if rows is None else dX[rows], Q_P=QP, Q_R=QR,
+                dtheta_P=oracle.cnp_backward(o["thP"], case.b_in, case.n, dQP),
+                dtheta_R=oracle.cnp_backward(o["thR"], case.b_out, case.n, dQR))
+
+
+def check_layer(case, inp, save_z=True, rows=None):
+    g = gpu_layer(case, inp, save_z=save_z)
+    r = oracle_layer(case, inp, rows=rows)
+    tol = tol_for(case.dtype)
+    errs = {}
+    for k in ("Q_P", "Q_R", "dtheta_P", "dtheta_R"):
+        errs[k] = assert_close(k, g[k], r[k], tol)
+    for k in ("y", "dX"):
+        got = g[k] if rows is None else g[k][rows]
+        errs[k] = assert_close(k, got, r[k], tol)
+    return errs
+
+
+# ------------------------------------------------------------------ Cayley-Neumann
+
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_cnp_tiny_config(out):
+    th = inputs.make_theta(16, 32, 0.01, 77)
+    Q = torch.empty(16, 32, 32, dtype=torch.float32 if out == "f32" else torch.bfloat16,
+                    device="cuda")
+    _lib.poetx_cayley_neumann(th.cuda(), 32, 4, Q)
+    _lib.poetx_stream_status()
+    assert_close("Q", to64(Q), oracle.cnp(th.double().numpy(), 32, 4), tol_for(out))
+
+
+@pytest.mark.parametrize("b", [2, 4, 8, 16])
+def test_cnp_small_blocks_fp32(b):
+    th = inputs.make_theta(5, b, 0.05, 78 + b)
+    Q = torch.empty(5, b, b, dtype=torch.float32, device="cuda")
+    _lib.poetx_cayley_neumann(th.cuda(), b, 3, Q)
+    _lib.poetx_stream_status()
+    assert_close("Q", to64(Q), oracle.cnp(th.double().numpy(), b, 3), TOL_F32)
+
+
+SWEEP = [(b, s, n, out) for b in inputs.CNP_SWEEP.bs for s in inputs.CNP_SWEEP.sigmas
+         for n in inputs.CNP_SWEEP.ns for out in ("f32", "bf16")]
+
+
+@pytest.mark.parametrize("b,sigma,n,out", SWEEP)
+def test_cnp_sweep_full_size_sampled_blocks(b, sigma, n, out):
+    """4096 blocks per point at full size; the oracle checks sampled blocks one by one."""
+    nb = inputs.CNP_SWEEP.nb
+    th = inputs.make_theta(nb, b, sigma, inputs.sweep_seed(b, sigma, n))
+    dt = torch.float32 if out == "f32" else torch.bfloat16
+    Q = torch.empty(nb, b, b, dtype=dt, device="cuda")
+    _lib.poetx_cayley_neumann(th.cuda(), b, n, Q)
+    _lib.poetx_stream_status()
+    idx = np.array([0, 1, 1234, 2047, 3001, nb - 1])
+    ref = oracle.cnp(th[idx].double().numpy(), b, n)
+    got = to64(Q[torch.as_tensor(idx, device="cuda")])
+    assert_close("Q", got, ref, tol_for(out))
+    if out == "f32":
+        # orthogonality defect ||Q^T Q - I||_F agrees with the oracle's within the
+        # perturbation bound 2 ||Q||_2 ||dQ||_F + ||dQ||_F^2 (plus fp32 rounding of I)
+        e_got, e_ref = oracle.orth_error(got), oracle.orth_error(ref)
+        dq = np.sqrt(((got - ref) ** 2).sum(axis=(1, 2)))
+        q2 = np.linalg.norm(ref, ord=2, axis=(1, 2))
+        bound = 2 * q2 * dq + dq ** 2 + 4 * b * 2.0 ** -24
+        assert np.all(np.abs(e_got - e_ref) <= bound), (e_got, e_ref, bound)
+
+
+@pytest.mark.parametrize("b,n", [(2, 1), (4, 3), (32, 4), (64, 2), (128, 3), (256, 3), (256, 6)])
+def test_cnp_backward_parity(b, n):
+    nb = 6
+    th = inputs.make_theta(nb, b, 0.01, 91 + b + n)
+    g = torch.Generator().manual_seed(92 + b * 7 + n)
+    dQ = torch.randn(nb, b, b, generator=g)
+    dth = torch.empty_like(th, device="cuda")
+    _lib.poetx_cayley_neumann_backward(th.cuda(), dQ.cuda(), b, n, dth)
+    _lib.poetx_stream_status()
+    ref = oracle.cnp_backward(th.double().numpy(), b, n, dQ.double().numpy())
+    assert_close("dtheta", dth.double().cpu().numpy(), ref, TOL_F32)
+
+
+# ------------------------------------------------------------------ index maps
+
+@pytest.mark.parametrize("d", [1, 7, 256, 2048, 5632])
+def test_invert_perm_bit_exact(d):
+    perm = torch.randperm(d, generator=torch.Generator().manual_seed(d)).to(torch.int32)
+    inv = torch.empty(d, dtype=torch.int32, device="cuda")
+    _lib.poetx_invert_perm(perm.cuda(), inv)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(inv.cpu().numpy(), oracle.invert_perm(perm.numpy()))
+    scratch = torch.empty(d + 1, dtype=torch.int32, device="cuda")
+    assert _lib.poetx_check_perm(perm.cuda(), inv, scratch) == 0
+
+
+def test_check_perm_rejects_non_permutations():
+    scratch = torch.empty(9, dtype=torch.int32, device="cuda")
+    for bad in ([0, 0, 1, 2, 3, 4, 5, 6], [0, 1, 2, 3, 4, 5, 6, 8], [-1, 1, 2, 3, 4, 5, 6, 7]):
+        p = torch.tensor(bad, dtype=torch.int32, device="cuda")
+        assert _lib.poetx_check_perm(p, None, scratch) == 4
+    p = torch.arange(8, dtype=torch.int32, device="cuda")
+    wrong_inv = torch.tensor([1, 0, 2, 3, 4, 5, 6, 7], dtype=torch.int32, device="cuda")
+    assert _lib.poetx_check_perm(p, wrong_inv, scratch) == 4
+    assert _lib.poetx_check_perm(p, p, scratch) == 0
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+def test_merge_w0_bit_exact(dt):
+    d_out, d_in = 384, 256
+    g = torch.Generator().manual_seed(5)
+    W0 = torch.randn(d_out, d_in, generator=g).to(dt)
+    po = torch.randperm(d_out, generator=g).to(torch.int32)
+    pi = torch.randperm(d_in, generator=g).to(torch.int32)
+    W0m = torch.empty(d_out, d_in, dtype=dt, device="cuda")
+    _lib.poetx_merge_w0(W0.cuda(), W0m, po.cuda(), pi.cuda())
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to64(W0m), oracle.merge_w0(to64(W0), po.numpy(), pi.numpy()))
+
+
+# ------------------------------------------------------------------ the layer
+
+@pytest.mark.parametrize("save_z", [True, False])
+def test_layer_tiny_fp32_config(save_z):
+    case = inputs.TINY_FP32
+    check_layer(case, inputs.make_linear_inputs(case), save_z=save_z)
+
+
+@pytest.mark.parametrize("b", [2, 4, 8, 16, 64])
+def test_layer_fp32_block_sizes_ragged_tokens(b):
+    case = inputs.LinearCase("fp32_b%d" % b, 128, 192, b, min(2 * b, 64), 3, 37, 0.02, "f32", 600 + b)
+    check_layer(case, inputs.make_linear_inputs(case))
+
+
+@pytest.mark.parametrize("b_in,b_out", [(32, 64), (64, 32), (128, 128), (256, 256), (256, 128)])
+@pytest.mark.parametrize("T", [1, 200, 384])
+def test_layer_bf16_tiles_and_ragged_tail(b_in, b_out, T):
+    case = inputs.LinearCase("bf16_%d_%d_%d" % (b_in, b_out, T), 512, 768, b_in, b_out, 3, T,
+                             0.005, "bf16", 700 + b_in + b_out + T)
+    check_layer(case, inputs.make_linear_inputs(case))
+
+
+def test_xfast_and_xmem_give_the_same_gradients():
+    case = inputs.LinearCase("xmem", 512, 512, 128, 128, 3, 300, 0.005, "bf16", 801)
+    inp = inputs.make_linear_inputs(case)
+    a = gpu_layer(case, inp, save_z=True)
+    b = gpu_layer(case, inp, save_z=False)
+    for k in ("y", "dX", "dtheta_P", "dtheta_R"):
+        assert_close(k, b[k], a[k], 1e-6)
+
+
+def test_zero_tokens_is_a_no_op_with_zero_gradients():
+    case = inputs.LinearCase("empty", 256, 256, 32, 32, 3, 0, 0.01, "f32", 802)
+    inp = inputs.make_linear_inputs(case, T=0)
+    lay = TransformedLinear(inp["W0"].cuda(), inp["theta_P"], inp["theta_R"], inp["perm_in"],
+                            inp["perm_out"], 32, 32, 3, T_max=1)
+    x = torch.empty(0, 256, device="cuda")
+    dy = torch.empty(0, 256, device="cuda")
+    lay.dtheta_P.fill_(7.0)
+    y, dX, dtp, dtr = lay.step(x, dy)
+    _lib.poetx_stream_status()
+    assert y.shape == (0, 256) and dX.shape == (0, 256)
+    assert float(dtp.abs().max()) == 0.0 and float(dtr.abs().max()) == 0.0
+
+
+def test_small_workspace_is_rejected():
+    case = inputs.TINY_FP32
+    inp = inputs.make_linear_inputs(case)
+    lay = TransformedLinear(inp["W0"].cuda(), inp["theta_P"], inp["theta_R"], inp["perm_in"],
+                            inp["perm_out"], 32, 32, 4, T_max=64)
+    lay.workspace = lay.workspace[:1024]
+    lay.cayley_neumann()
+    with pytest.raises(_lib.PoetxError) as e:
+        lay.forward(inp["x"].cuda())
+    assert e.value.code == 2
+
+
+# ------------------------------------------------------------------ full-size configs
+
+SAMPLE_ROWS = lambda T: np.unique(np.concatenate([[0, 1, T // 2, T - 2, T - 1],
+                                                   np.random.default_rng(T).integers(0, T, 27)]))
+
+
+def test_full_size_square_2048():
+    case = inputs.SQUARE_2048
+    check_layer(case, inputs.make_linear_inputs(case), rows=SAMPLE_ROWS(case.T))
+
+
+def test_full_size_upproj_2048x5632():
+    case = inputs.UPPROJ
+    check_layer(case, inputs.make_linear_inputs(case), rows=SAMPLE_ROWS(case.T))
+
+
+@pytest.mark.parametrize("which", [0, 4, 6])   # q (2048->2048), gate (2048->5632), down (5632->2048)
+def test_full_size_stack_layer_shapes(which):
+    case = inputs.stack_cases()[which]
+    check_layer(case, inputs.make_linear_inputs(case), rows=SAMPLE_ROWS(case.T))
