@@ -162,6 +162,41 @@ poetx_status poetx_backward(const void *x, const void *dy, const void *W0m, cons
                             float *dtheta_P, float *dtheta_R, void *workspace, size_t ws_bytes,
                             cudaStream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Forward for callers that cannot allocate device memory                   */
+/* (this entry point has no counterpart in the paper)                       */
+/* ------------------------------------------------------------------------ */
+
+/* Size of the library's own static device array that serves as the
+ * workspace of poetx_forward_noalloc: 32 MiB, held by every device that
+ * loads the library until the process exits. */
+#define POETX_NOALLOC_WORKSPACE_BYTES ((size_t)32 << 20)
+
+/* poetx_forward for callers that cannot call cudaMalloc (for instance a host
+ * framework that owns all device memory through its own pool, or a loop in
+ * which allocating is forbidden after start-up).  Same arguments and result
+ * as poetx_forward, without `workspace`: the scratch is a file-scope static
+ * device array of POETX_NOALLOC_WORKSPACE_BYTES inside the library.  The
+ * caller still owns x, the weights, y and z_save.  This call allocates no
+ * device memory.
+ *   - Sizes for which poetx_workspace_bytes(T, d_in, d_out, b_in, b_out,
+ *     act_dtype) exceeds POETX_NOALLOC_WORKSPACE_BYTES are rejected with
+ *     POETX_ERR_SHAPE before anything is launched (e.g. T up to about 2300
+ *     tokens for d_in = d_out = 2048 in bf16).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last
+ *     call's contents; calls that overlap on the GPU (on streams with no
+ *     ordering between them) race on it and must be serialised by the
+ *     caller. */
+poetx_status poetx_forward_noalloc(const void *x, const void *W0m, const void *Q_P,
+                                   const void *Q_R, const int32_t *perm_in, const int32_t *inv_in,
+                                   const int32_t *perm_out, const int32_t *inv_out, int T,
+                                   int d_in, int d_out, int b_in, int b_out,
+                                   poetx_dtype act_dtype, void *y, void *z_save,
+                                   cudaStream_t stream);
+
 /* Synchronises `stream` and reports the first error since the last call:
  * a CUDA error (POETX_ERR_CUDA) or an expired device-side wait
  * (POETX_ERR_TIMEOUT).  Clears the device error word. */

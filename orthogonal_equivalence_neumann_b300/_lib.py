@@ -24,7 +24,7 @@ EXPORTS = ["poetx_status_string", "poetx_version", "poetx_cayley_neumann",
            "poetx_cayley_neumann_backward", "poetx_invert_perm", "poetx_check_perm",
            "poetx_merge_w0", "poetx_workspace_bytes", "poetx_forward", "poetx_backward",
            "poetx_stream_status", "poetx_launch_count", "poetx_profile_enable",
-           "poetx_profile_report"]
+           "poetx_profile_report", "poetx_forward_noalloc"]
 
 
 class PoetxError(RuntimeError):
@@ -59,6 +59,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "poetx_backward": (I, [P, P, P, P, P, I, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P,
                                P, Z, P]),
         "poetx_stream_status": (I, [P]),
+        "poetx_forward_noalloc": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P]),
         "poetx_launch_count": (ctypes.c_ulonglong, []),
         "poetx_profile_enable": (I, [I]),
         "poetx_profile_report": (I, [ctypes.c_char_p, Z]),
@@ -166,6 +167,17 @@ def poetx_backward(x, dy, W0m, theta_P, theta_R, n, Q_P, Q_R, z_saved, perm_in, 
         _ptr(z_saved), _ptr(perm_in), _ptr(inv_in), _ptr(perm_out), _ptr(inv_out), T, d_in, d_out,
         b_in, b_out, dtype_code(x.dtype), _ptr(dX), _ptr(dtheta_P), _ptr(dtheta_R),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def poetx_forward_noalloc(x, W0m, Q_P, Q_R, perm_in, inv_in, perm_out, inv_out, b_in, b_out, y,
+                          z_save, stream=None):
+    """poetx_forward with the library's static device workspace (no allocation)."""
+    T, d_in = x.shape
+    d_out = W0m.shape[0]
+    _check("poetx_forward_noalloc", load().poetx_forward_noalloc(
+        _ptr(x), _ptr(W0m), _ptr(Q_P), _ptr(Q_R), _ptr(perm_in), _ptr(inv_in), _ptr(perm_out),
+        _ptr(inv_out), T, d_in, d_out, b_in, b_out, dtype_code(x.dtype), _ptr(y), _ptr(z_save),
+        _stream(stream)))
 
 
 def poetx_stream_status(stream=None):
