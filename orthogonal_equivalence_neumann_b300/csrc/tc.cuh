@@ -24,4 +24,12 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
                          int T, int d_in, int d_out, int b_in, int b_out, void* dX, void* gz,
                          void* gu, float* dqp, float* dqr, void* ws, cudaStream_t s);
 
+namespace tc {
+// C[M,N] (bf16) = A[M,K] . B^T with A [M,K] and B [N,K] (b_mn == false) or
+// B [K,N] (b_mn == true), all bf16 row-major, fp32 accumulation (tcgen05).
+bool gemm_supported(int N, int K);
+poetx_status gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, bool b_mn,
+                       cudaStream_t s);
+}  // namespace tc
+
 }  // namespace poetx

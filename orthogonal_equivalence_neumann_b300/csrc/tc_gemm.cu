@@ -1,0 +1,216 @@
+// tc_gemm.cu -- the frozen-weight products on the 5th-generation tensor cores.
+//
+// [POET-X §2.A] ("POET-X: Memory-efficient LLM Training by Scaling Orthogonal
+// Transformation", gist.science summary, section 2.A): the layer is applied
+// to the activations; the only dense product is the one with the frozen,
+// permutation-merged weight W0m:
+//   forward   z   = u   . W0m^T   (B = W0m [N = d_out, K = d_in], K-major)
+//   backward  g_u = g_z . W0m     (B = W0m [K = d_out, N = d_in], MN-major)
+// C[M, N] (bf16) = A[M, K] (bf16, K-major) . B^T, fp32 accumulation in TMEM.
+//
+// Persistent kernel, one CTA per SM, 128 x 256 output tiles, 64-deep k steps:
+//   warp 0  one thread issues TMA loads of A and B tiles (128-byte swizzle)
+//           into a 4-stage shared-memory ring;
+//   warp 1  allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
+//           and one thread issues tcgen05.mma (M=128, N=256, K=16), freeing
+//           each stage with tcgen05.commit;
+//   warps 2-5  drain an accumulator (tcgen05.ld), round to bf16 and store
+//           while the MMA thread fills the other accumulator.
+// Every wait is bounded (see tc_ptx.cuh); on expiry the kernel records
+// POETX_ERR_TIMEOUT in the library's error word and winds down.
+#include "common.cuh"
+#include "profile.cuh"
+#include "tc.cuh"
+#include "tc_ptx.cuh"
+#include "tmap.cuh"
+
+namespace poetx {
+namespace tc {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;   // 16 KB
+constexpr int B_BYTES = BN * BK * 2;   // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     __nv_bfloat16* __restrict__ C, int M, int N, int K, int b_mn, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int m_tiles = (M + BM - 1) / BM, n_tiles = N / BN;
+  const int num_tiles = m_tiles * n_tiles;
+  const int k_iters = K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull + a, 1);
+      mbar_init(tempty + a, 128);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int m_blk = tile % m_tiles, n_blk = tile / m_tiles;
+        for (int kb = 0; kb < k_iters; ++kb) {
+          if (!(ok = mbar_wait(empty + stage, phase ^ 1, err))) break;
+          mbar_arrive_expect_tx(full + stage, STAGE_BYTES);
+          tma_load_2d(sA + stage * A_BYTES, &tmA, kb * BK, m_blk * BM, full + stage);
+          if (!b_mn) {
+            tma_load_2d(sB + stage * B_BYTES, &tmB, kb * BK, n_blk * BN, full + stage);
+          } else {
+#pragma unroll
+            for (int q = 0; q < BN / 64; ++q)
+              tma_load_2d(sB + stage * B_BYTES + q * (BK * 128), &tmB, n_blk * BN + q * 64,
+                          kb * BK, full + stage);
+          }
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(BM, BN, false, b_mn != 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        if (!(ok = mbar_wait(tempty + acc, acc_phase ^ 1, err))) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < k_iters; ++kb) {
+          if (!(ok = mbar_wait(full + stage, phase, err))) break;
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + stage * A_BYTES);
+          const uint32_t b_base = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t adesc = sw128_desc(a_base + k * 32, 16, 1024);
+            const uint64_t bdesc = b_mn ? sw128_desc(b_base + k * 2048, BK * 128, 1024)
+                                        : sw128_desc(b_base + k * 32, 16, 1024);
+            mma_bf16(d_tmem, adesc, bdesc, idesc, (kb | k) != 0);
+          }
+          mma_commit(empty + stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        mma_commit(tfull + acc);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+    }
+  } else {
+    // epilogue warps 2..5 own TMEM lane quarters (warp % 4)
+    const int quarter = warp % 4;
+    const int row_in_tile = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int m_blk = tile % m_tiles, n_blk = tile / m_tiles;
+      if (!mbar_wait(tfull + acc, acc_phase, err)) break;
+      tc_fence_after();
+      const int row = m_blk * BM + row_in_tile;
+      __nv_bfloat16* crow = C + (size_t)row * N + (size_t)n_blk * BN;
+      const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tbase + c, r);
+        tmem_ld_wait();
+        if (row < M) {
+          uint4* dst = reinterpret_cast<uint4*>(crow + c);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+            o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+            o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+            o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+            dst[v] = o;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty + acc);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+int sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+}  // namespace
+
+bool gemm_supported(int N, int K) { return N % BN == 0 && K % BK == 0 && N > 0 && K > 0; }
+
+// C[M,N] = A[M,K] . B^T; B is [N,K] (b_mn == false) or [K,N] (b_mn == true), all bf16 row-major.
+poetx_status gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, bool b_mn,
+                       cudaStream_t s) {
+  if (M <= 0) return POETX_OK;
+  if (!gemm_supported(N, K)) return POETX_ERR_UNSUPPORTED;
+  CUtensorMap ta, tb;
+  if (!make_tmap_2d(&ta, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)M, (uint64_t)K, BM, BK,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+    return POETX_ERR_CUDA;
+  const bool okb =
+      b_mn ? make_tmap_2d(&tb, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K, (uint64_t)N, BK,
+                          64, CU_TENSOR_MAP_SWIZZLE_128B)
+           : make_tmap_2d(&tb, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)N, (uint64_t)K, BN,
+                          BK, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!okb) return POETX_ERR_CUDA;
+  const int tiles = ((M + BM - 1) / BM) * (N / BN);
+  const int grid = tiles < sm_count() ? tiles : sm_count();
+  cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  {
+    KernelScope ks_(b_mn ? "tc_gemm_nn" : "tc_gemm_nt", s);
+    gemm_bf16_kernel<<<grid, kThreads, SMEM_BYTES, s>>>(ta, tb, (__nv_bfloat16*)C, M, N, K,
+                                                         b_mn ? 1 : 0, device_error_word());
+  }
+  return check_launch();
+}
+
+}  // namespace tc
+}  // namespace poetx

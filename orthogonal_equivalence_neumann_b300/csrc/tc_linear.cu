@@ -1,25 +1,64 @@
-// tc_linear.cu -- tensor-core path (filled in by the tcgen05 kernels).
+// tc_linear.cu -- the bf16 transformed linear on the tensor-core path.
+//
+// [POET-X §2.A-§2.C] ("POET-X: Memory-efficient LLM Training by Scaling
+// Orthogonal Transformation", gist.science summary): the chain
+//   u = gather(x, perm_in) . B_P^T,  z = u . W0m^T,  y = scatter(z . B_R^T, perm_out)
+// and its backward.  The frozen-weight products run on tcgen05 (tc_gemm.cu);
+// the block-diagonal applies and the dQ token sums use the CUDA-core kernels.
 #include "common.cuh"
+#include "kernels.cuh"
 #include "tc.cuh"
 
 namespace poetx {
+
+#define TC_TRY(expr)                 \
+  do {                               \
+    poetx_status _st = (expr);       \
+    if (_st != POETX_OK) return _st; \
+  } while (0)
 
 bool tc_cnp_supported(int, poetx_dtype) { return false; }
 poetx_status tc_cnp_fwd(const float*, int, int, int, void*, poetx_dtype, cudaStream_t) {
   return POETX_ERR_UNSUPPORTED;
 }
-bool tc_linear_supported(int, int, int, int, poetx_dtype) { return false; }
-size_t tc_workspace_bytes(int, int, int, int, int, poetx_dtype, bool) { return 0; }
-poetx_status tc_forward(const void*, const void*, const void*, const void*, const int32_t*,
-                        const int32_t*, const int32_t*, const int32_t*, int, int, int, int, int,
-                        void*, void*, void*, void*, cudaStream_t) {
-  return POETX_ERR_UNSUPPORTED;
+
+bool tc_linear_supported(int d_in, int d_out, int b_in, int b_out, poetx_dtype dt) {
+  (void)b_in;
+  (void)b_out;
+  return dt == POETX_BF16 && tc::gemm_supported(d_out, d_in) && tc::gemm_supported(d_in, d_out);
 }
-poetx_status tc_backward(const void*, const void*, const void*, const void*, const void*,
-                         const void*, const int32_t*, const int32_t*, const int32_t*,
-                         const int32_t*, int, int, int, int, int, void*, void*, void*, float*,
-                         float*, void*, cudaStream_t) {
-  return POETX_ERR_UNSUPPORTED;
+
+size_t tc_workspace_bytes(int, int, int, int, int, poetx_dtype, bool) { return 0; }
+
+poetx_status tc_forward(const void* x, const void* W0m, const void* Q_P, const void* Q_R,
+                        const int32_t* perm_in, const int32_t* inv_in, const int32_t* perm_out,
+                        const int32_t* inv_out, int T, int d_in, int d_out, int b_in, int b_out,
+                        void* u, void* z, void* y, void* ws, cudaStream_t s) {
+  (void)inv_in;
+  (void)inv_out;
+  (void)ws;
+  const poetx_dtype dt = POETX_BF16;
+  TC_TRY(launch_block_apply_simt(x, u, Q_P, T, d_in, b_in, perm_in, nullptr, false, dt, s));
+  TC_TRY(tc::gemm_bf16(u, W0m, z, T, d_out, d_in, false, s));
+  if (y) TC_TRY(launch_block_apply_simt(z, y, Q_R, T, d_out, b_out, nullptr, perm_out, false, dt, s));
+  return POETX_OK;
+}
+
+poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const void* Q_P,
+                         const void* Q_R, const void* z, const int32_t* perm_in,
+                         const int32_t* inv_in, const int32_t* perm_out, const int32_t* inv_out,
+                         int T, int d_in, int d_out, int b_in, int b_out, void* dX, void* gz,
+                         void* gu, float* dqp, float* dqr, void* ws, cudaStream_t s) {
+  (void)inv_in;
+  (void)inv_out;
+  (void)ws;
+  const poetx_dtype dt = POETX_BF16;
+  TC_TRY(launch_block_apply_simt(dy, gz, Q_R, T, d_out, b_out, perm_out, nullptr, true, dt, s));
+  TC_TRY(launch_dq_simt(dy, z, T, d_out, b_out, perm_out, nullptr, dqr, dt, s));
+  TC_TRY(tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s));
+  TC_TRY(launch_block_apply_simt(gu, dX, Q_P, T, d_in, b_in, nullptr, perm_in, true, dt, s));
+  TC_TRY(launch_dq_simt(gu, x, T, d_in, b_in, nullptr, perm_in, dqp, dt, s));
+  return POETX_OK;
 }
 
 }  // namespace poetx
