@@ -30,6 +30,14 @@ namespace tc {
 bool gemm_supported(int N, int K);
 poetx_status gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, bool b_mn,
                        cudaStream_t s);
+
+// Permuted block-diagonal apply, bf16 in/out, fp32 accumulation (tcgen05):
+//   scatter == false: out[t][jb+i] = sum_k Qop_j[i][k] in[t][perm[jb+k]]
+//   scatter == true:  out[t][perm[jb+i]] = sum_k Qop_j[i][k] in[t][jb+k]
+// with Qop_j = Q_j, or Q_j^T when transpose_q.  b in {128, 256}.
+bool blockapply_supported(int d, int b);
+poetx_status blockapply_bf16(const void* in, void* out, const void* Q, const int32_t* perm, int T,
+                             int d, int b, bool transpose_q, bool scatter, cudaStream_t s);
 }  // namespace tc
 
 }  // namespace poetx

@@ -3,8 +3,9 @@
 // [POET-X §2.A-§2.C] ("POET-X: Memory-efficient LLM Training by Scaling
 // Orthogonal Transformation", gist.science summary): the chain
 //   u = gather(x, perm_in) . B_P^T,  z = u . W0m^T,  y = scatter(z . B_R^T, perm_out)
-// and its backward.  The frozen-weight products run on tcgen05 (tc_gemm.cu);
-// the block-diagonal applies and the dQ token sums use the CUDA-core kernels.
+// and its backward.  The frozen-weight products run on tcgen05 (tc_gemm.cu),
+// so do the permuted block-diagonal applies (tc_blockapply.cu) for b in
+// {128, 256}; other block sizes and the dQ token sums use CUDA-core kernels.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tc.cuh"
@@ -30,6 +31,16 @@ bool tc_linear_supported(int d_in, int d_out, int b_in, int b_out, poetx_dtype d
 
 size_t tc_workspace_bytes(int, int, int, int, int, poetx_dtype, bool) { return 0; }
 
+// Permuted block apply: tensor cores when the shape allows, CUDA cores otherwise.
+static poetx_status block_apply(const void* in, void* out, const void* Q, int T, int d, int b,
+                                const int32_t* gath, const int32_t* scat, bool transpose_q,
+                                cudaStream_t s) {
+  if (tc::blockapply_supported(d, b))
+    return tc::blockapply_bf16(in, out, Q, gath ? gath : scat, T, d, b, transpose_q,
+                               scat != nullptr, s);
+  return launch_block_apply_simt(in, out, Q, T, d, b, gath, scat, transpose_q, POETX_BF16, s);
+}
+
 poetx_status tc_forward(const void* x, const void* W0m, const void* Q_P, const void* Q_R,
                         const int32_t* perm_in, const int32_t* inv_in, const int32_t* perm_out,
                         const int32_t* inv_out, int T, int d_in, int d_out, int b_in, int b_out,
@@ -37,10 +48,9 @@ poetx_status tc_forward(const void* x, const void* W0m, const void* Q_P, const v
   (void)inv_in;
   (void)inv_out;
   (void)ws;
-  const poetx_dtype dt = POETX_BF16;
-  TC_TRY(launch_block_apply_simt(x, u, Q_P, T, d_in, b_in, perm_in, nullptr, false, dt, s));
+  TC_TRY(block_apply(x, u, Q_P, T, d_in, b_in, perm_in, nullptr, false, s));
   TC_TRY(tc::gemm_bf16(u, W0m, z, T, d_out, d_in, false, s));
-  if (y) TC_TRY(launch_block_apply_simt(z, y, Q_R, T, d_out, b_out, nullptr, perm_out, false, dt, s));
+  if (y) TC_TRY(block_apply(z, y, Q_R, T, d_out, b_out, nullptr, perm_out, false, s));
   return POETX_OK;
 }
 
@@ -53,10 +63,10 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
   (void)inv_out;
   (void)ws;
   const poetx_dtype dt = POETX_BF16;
-  TC_TRY(launch_block_apply_simt(dy, gz, Q_R, T, d_out, b_out, perm_out, nullptr, true, dt, s));
+  TC_TRY(block_apply(dy, gz, Q_R, T, d_out, b_out, perm_out, nullptr, true, s));
   TC_TRY(launch_dq_simt(dy, z, T, d_out, b_out, perm_out, nullptr, dqr, dt, s));
   TC_TRY(tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s));
-  TC_TRY(launch_block_apply_simt(gu, dX, Q_P, T, d_in, b_in, nullptr, perm_in, true, dt, s));
+  TC_TRY(block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, perm_in, true, s));
   TC_TRY(launch_dq_simt(gu, x, T, d_in, b_in, nullptr, perm_in, dqp, dt, s));
   return POETX_OK;
 }
