@@ -38,6 +38,12 @@ poetx_status gemm_bf16(const void* A, const void* B, void* C, int M, int N, int 
 bool blockapply_supported(int d, int b);
 poetx_status blockapply_bf16(const void* in, void* out, const void* Q, const int32_t* perm, int T,
                              int d, int b, bool transpose_q, bool scatter, cudaStream_t s);
+
+// dQ_j[i][k] = sum_t G[t][gG(jb+i)] V[t][gV(jb+k)], exactly one of gG, gV a
+// permutation (the other NULL = identity); fp32 out [d/b, b, b], overwritten.
+bool dq_supported(int d, int b);
+poetx_status dq_bf16(const void* G, const void* V, int T, int d, int b, const int32_t* gG,
+                     const int32_t* gV, float* dQ, cudaStream_t s);
 }  // namespace tc
 
 }  // namespace poetx

@@ -5,7 +5,8 @@
 //   u = gather(x, perm_in) . B_P^T,  z = u . W0m^T,  y = scatter(z . B_R^T, perm_out)
 // and its backward.  The frozen-weight products run on tcgen05 (tc_gemm.cu),
 // so do the permuted block-diagonal applies (tc_blockapply.cu) for b in
-// {128, 256}; other block sizes and the dQ token sums use CUDA-core kernels.
+// {128, 256}, and so do the dQ token sums (tc_dq.cu); other block sizes use
+// the CUDA-core kernels.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tc.cuh"
@@ -41,6 +42,13 @@ static poetx_status block_apply(const void* in, void* out, const void* Q, int T,
   return launch_block_apply_simt(in, out, Q, T, d, b, gath, scat, transpose_q, POETX_BF16, s);
 }
 
+// dQ token sums: tensor cores when the shape allows, CUDA cores otherwise.
+static poetx_status dq(const void* G, const void* V, int T, int d, int b, const int32_t* gG,
+                       const int32_t* gV, float* out, cudaStream_t s) {
+  if (tc::dq_supported(d, b)) return tc::dq_bf16(G, V, T, d, b, gG, gV, out, s);
+  return launch_dq_simt(G, V, T, d, b, gG, gV, out, POETX_BF16, s);
+}
+
 poetx_status tc_forward(const void* x, const void* W0m, const void* Q_P, const void* Q_R,
                         const int32_t* perm_in, const int32_t* inv_in, const int32_t* perm_out,
                         const int32_t* inv_out, int T, int d_in, int d_out, int b_in, int b_out,
@@ -62,12 +70,11 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
   (void)inv_in;
   (void)inv_out;
   (void)ws;
-  const poetx_dtype dt = POETX_BF16;
   TC_TRY(block_apply(dy, gz, Q_R, T, d_out, b_out, perm_out, nullptr, true, s));
-  TC_TRY(launch_dq_simt(dy, z, T, d_out, b_out, perm_out, nullptr, dqr, dt, s));
+  TC_TRY(dq(dy, z, T, d_out, b_out, perm_out, nullptr, dqr, s));
   TC_TRY(tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s));
   TC_TRY(block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, perm_in, true, s));
-  TC_TRY(launch_dq_simt(gu, x, T, d_in, b_in, nullptr, perm_in, dqp, dt, s));
+  TC_TRY(dq(gu, x, T, d_in, b_in, nullptr, perm_in, dqp, s));
   return POETX_OK;
 }
 
