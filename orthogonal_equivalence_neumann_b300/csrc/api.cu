@@ -125,7 +125,8 @@ poetx_status poetx_cayley_neumann(const float* theta, int nb, int b, int n, void
   if (!valid_block(b)) return POETX_ERR_UNSUPPORTED;
   if (nb == 0) return POETX_OK;
   if (!theta || !Q || !aligned16(theta) || !aligned16(Q)) return POETX_ERR_INVALID_ARG;
-  if (tc_cnp_supported(b, out_dtype)) return tc_cnp_fwd(theta, nb, b, n, Q, out_dtype, stream);
+  if (tc_cnp_supported(b, out_dtype) && nb <= 65535)
+    return tc_cnp_fwd(theta, nb, b, n, Q, out_dtype, stream);
   return launch_cnp_fwd_simt(theta, nb, b, n, Q, out_dtype, stream);
 }
 
@@ -265,8 +266,14 @@ poetx_status poetx_backward(const void* x, const void* dy, const void* W0m, cons
     // dQ_P,j = sum_t g_u,j^T gather(x)_j
     POETX_TRY(launch_dq_simt(gu, x, T, d_in, b_in, nullptr, perm_in, dqp, dt, stream));
   }
-  POETX_TRY(launch_cnp_bwd_simt(theta_P, dqp, nb_in, b_in, n, dtheta_P, stream));
-  POETX_TRY(launch_cnp_bwd_simt(theta_R, dqr, nb_out, b_out, n, dtheta_R, stream));
+  // [§2.D] backward of the Cayley-Neumann blocks; the bf16 layer runs it on the
+  // tensor cores (bf16 operands), the fp32 layer on the exact CUDA-core kernel
+  const bool tc_cnp_in = dt == POETX_BF16 && tc::cnp_supported(b_in) && nb_in <= 65535;
+  const bool tc_cnp_out = dt == POETX_BF16 && tc::cnp_supported(b_out) && nb_out <= 65535;
+  POETX_TRY(tc_cnp_in ? tc::cnp_bwd_bf16ops(theta_P, dqp, nb_in, b_in, n, dtheta_P, stream)
+                      : launch_cnp_bwd_simt(theta_P, dqp, nb_in, b_in, n, dtheta_P, stream));
+  POETX_TRY(tc_cnp_out ? tc::cnp_bwd_bf16ops(theta_R, dqr, nb_out, b_out, n, dtheta_R, stream)
+                       : launch_cnp_bwd_simt(theta_R, dqr, nb_out, b_out, n, dtheta_R, stream));
   return POETX_OK;
 }
 

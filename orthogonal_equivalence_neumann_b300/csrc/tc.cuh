@@ -44,6 +44,14 @@ poetx_status blockapply_bf16(const void* in, void* out, const void* Q, const int
 bool dq_supported(int d, int b);
 poetx_status dq_bf16(const void* G, const void* V, int T, int d, int b, const int32_t* gG,
                      const int32_t* gV, float* dQ, cudaStream_t s);
+
+// Cayley-Neumann forward / backward with bf16 operands and fp32 accumulation
+// (tcgen05), b in {128, 256}.  The backward overwrites dtheta.
+bool cnp_supported(int b);
+poetx_status cnp_fwd_bf16ops(const float* theta, int nb, int b, int n, void* Q, bool out_f32,
+                             cudaStream_t s);
+poetx_status cnp_bwd_bf16ops(const float* theta, const float* dQ, int nb, int b, int n,
+                             float* dtheta, cudaStream_t s);
 }  // namespace tc
 
 }  // namespace poetx

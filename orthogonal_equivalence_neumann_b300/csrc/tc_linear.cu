@@ -19,9 +19,13 @@ namespace poetx {
     if (_st != POETX_OK) return _st; \
   } while (0)
 
-bool tc_cnp_supported(int, poetx_dtype) { return false; }
-poetx_status tc_cnp_fwd(const float*, int, int, int, void*, poetx_dtype, cudaStream_t) {
-  return POETX_ERR_UNSUPPORTED;
+// bf16 Q: tensor-core chain with bf16 operands (the fp32 path stays exact on the CUDA cores).
+bool tc_cnp_supported(int b, poetx_dtype out_dtype) {
+  return out_dtype == POETX_BF16 && tc::cnp_supported(b);
+}
+poetx_status tc_cnp_fwd(const float* theta, int nb, int b, int n, void* Q, poetx_dtype out_dtype,
+                        cudaStream_t s) {
+  return tc::cnp_fwd_bf16ops(theta, nb, b, n, Q, out_dtype == POETX_F32, s);
 }
 
 bool tc_linear_supported(int d_in, int d_out, int b_in, int b_out, poetx_dtype dt) {
