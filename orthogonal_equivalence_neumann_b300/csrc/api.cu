@@ -266,14 +266,17 @@ poetx_status poetx_backward(const void* x, const void* dy, const void* W0m, cons
     // dQ_P,j = sum_t g_u,j^T gather(x)_j
     POETX_TRY(launch_dq_simt(gu, x, T, d_in, b_in, nullptr, perm_in, dqp, dt, stream));
   }
-  // [§2.D] backward of the Cayley-Neumann blocks; the bf16 layer runs it on the
-  // tensor cores (bf16 operands), the fp32 layer on the exact CUDA-core kernel
-  const bool tc_cnp_in = dt == POETX_BF16 && tc::cnp_supported(b_in) && nb_in <= 65535;
-  const bool tc_cnp_out = dt == POETX_BF16 && tc::cnp_supported(b_out) && nb_out <= 65535;
-  POETX_TRY(tc_cnp_in ? tc::cnp_bwd_bf16ops(theta_P, dqp, nb_in, b_in, n, dtheta_P, stream)
-                      : launch_cnp_bwd_simt(theta_P, dqp, nb_in, b_in, n, dtheta_P, stream));
-  POETX_TRY(tc_cnp_out ? tc::cnp_bwd_bf16ops(theta_R, dqr, nb_out, b_out, n, dtheta_R, stream)
-                       : launch_cnp_bwd_simt(theta_R, dqr, nb_out, b_out, n, dtheta_R, stream));
+  // [§2.D] backward of the Cayley-Neumann blocks: the bf16 layer runs both sides
+  // in one tensor-core launch (bf16 operands), the fp32 layer the exact
+  // CUDA-core kernel per side
+  if (dt == POETX_BF16 && tc::cnp_supported(b_in) && tc::cnp_supported(b_out) &&
+      nb_in + nb_out <= 65535) {
+    POETX_TRY(tc::cnp_bwd_layer(theta_P, dqp, nb_in, b_in, theta_R, dqr, nb_out, b_out, n,
+                                dtheta_P, dtheta_R, tc_ws, stream));
+  } else {
+    POETX_TRY(launch_cnp_bwd_simt(theta_P, dqp, nb_in, b_in, n, dtheta_P, stream));
+    POETX_TRY(launch_cnp_bwd_simt(theta_R, dqr, nb_out, b_out, n, dtheta_R, stream));
+  }
   return POETX_OK;
 }
 

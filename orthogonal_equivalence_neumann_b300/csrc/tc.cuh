@@ -50,8 +50,12 @@ poetx_status dq_bf16(const void* G, const void* V, int T, int d, int b, const in
 bool cnp_supported(int b);
 poetx_status cnp_fwd_bf16ops(const float* theta, int nb, int b, int n, void* Q, bool out_f32,
                              cudaStream_t s);
-poetx_status cnp_bwd_bf16ops(const float* theta, const float* dQ, int nb, int b, int n,
-                             float* dtheta, cudaStream_t s);
+// Backward of both sides of a layer in one launch (after a prep kernel that
+// writes dense bf16 K and G into `ws`, cnp_bwd_workspace_bytes of it).
+size_t cnp_bwd_workspace_bytes(int d_in, int b_in, int d_out, int b_out);
+poetx_status cnp_bwd_layer(const float* theta_P, const float* dQ_P, int nb_P, int b_P,
+                           const float* theta_R, const float* dQ_R, int nb_R, int b_R, int n,
+                           float* dtheta_P, float* dtheta_R, void* ws, cudaStream_t s);
 }  // namespace tc
 
 }  // namespace poetx

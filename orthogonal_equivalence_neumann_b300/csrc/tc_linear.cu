@@ -34,7 +34,14 @@ bool tc_linear_supported(int d_in, int d_out, int b_in, int b_out, poetx_dtype d
   return dt == POETX_BF16 && tc::gemm_supported(d_out, d_in) && tc::gemm_supported(d_in, d_out);
 }
 
-size_t tc_workspace_bytes(int, int, int, int, int, poetx_dtype, bool) { return 0; }
+// The backward's tensor-core scratch: dense bf16 K and G of every block (CNP backward).
+size_t tc_workspace_bytes(int T, int d_in, int d_out, int b_in, int b_out, poetx_dtype dt,
+                          bool backward) {
+  (void)T;
+  if (!backward || dt != POETX_BF16 || !tc::cnp_supported(b_in) || !tc::cnp_supported(b_out))
+    return 0;
+  return tc::cnp_bwd_workspace_bytes(d_in, b_in, d_out, b_out);
+}
 
 // Permuted block apply: tensor cores when the shape allows, CUDA cores otherwise.
 static poetx_status block_apply(const void* in, void* out, const void* Q, int T, int d, int b,
