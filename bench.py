@@ -22,6 +22,7 @@ import subprocess
 import sys
 import time
 
+import numpy as np
 import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -32,8 +33,8 @@ from orthogonal_equivalence_neumann_b300 import TransformedLinear, _lib, inputs 
 METRIC = "transformed-linear tokens/s (fwd+bwd) and Cayley-Neumann blocks/s; % of roofline"
 CASE = inputs.SQUARE_2048
 ROTATE = 4            # input sets cycled over the steps: 4 x (x + dy) = 268 MB > 126 MB L2
-CPU_SAMPLE_TOKENS = 2048
-REF_SAMPLE_TOKENS = 512
+CPU_SAMPLE_FRACTION = 0.25   # cpu_baseline: 3 sampled steps of a quarter step each
+REF_BUDGET_S = 90.0          # reference arm: wall time of warm-up plus timed oracle steps
 
 # Peak of the fp32 FFMA pipes: 148 SMs x 128 lanes x 2 flop x 2.032 GHz.
 ALU_FP32_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
@@ -65,12 +66,25 @@ def kernel_work(case):
     cnp_fb = 4 * (nbi * bi * (bi - 1) / 2 + nbo * bo * (bo - 1) / 2) / 2 + es * (nbi * bi * bi + nbo * bo * bo) / 2
     cnpb_f = 3 * cnp_f
     cnpb_b = 4 * (nbi * bi * bi + nbo * bo * bo) / 2 + 8 * (nbi * bi * (bi - 1) / 2 + nbo * bo * (bo - 1) / 2) / 2
+    cnp_prep_b = 4 * (nbi * bi * (bi - 1) / 2 + nbo * bo * (bo - 1) / 2) + 4 * (nbi * bi * bi + nbo * bo * bo) \
+        + 2 * 2 * (nbi * bi * bi + nbo * bo * bo)
     return {
         "gemm_simt": ("alu", gemm_flops, gemm_bytes),
         "block_apply_simt": ("alu", blk_flops, blk_bytes),
         "dq_simt": ("alu", dq_flops, dq_bytes),
         "cnp_fwd_simt": ("alu", cnp_f, cnp_fb),
         "cnp_bwd_simt": ("alu", cnpb_f, cnpb_b),
+        # tensor-core path (one launch per product; the CNP backward serves both sides)
+        "tc_gemm_nt": ("tensor", gemm_flops, gemm_bytes),
+        "tc_gemm_nn": ("tensor", gemm_flops, gemm_bytes),
+        "tc_blockapply_gather": ("hbm", blk_flops, blk_bytes),
+        "tc_blockapply_scatter": ("hbm", blk_flops, blk_bytes),
+        "tc_dq_gather_rows": ("hbm", dq_flops, dq_bytes),
+        "tc_dq_gather_cols": ("hbm", dq_flops, dq_bytes),
+        "tc_cnp_fwd": ("tensor", cnp_f, cnp_fb),
+        "tc_cnp_bwd_prep": ("hbm", 0.0, cnp_prep_b),
+        "tc_cnp_bwd": ("tensor", 2 * cnpb_f, 2 * 2 * 2 * (nbi * bi * bi + nbo * bo * bo) / 2
+                       + 4 * (nbi * bi * (bi - 1) / 2 + nbo * bo * (bo - 1) / 2)),
     }
 
 
@@ -98,52 +112,90 @@ def read_traffic(kernel):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event reasons sampled during the timed region.
 
-    def __init__(self, gpu_index):
+    Reads NVML (the library nvidia-smi reports from) every few milliseconds
+    from a background thread, so that even a short timed region gets samples;
+    falls back to `nvidia-smi -lms` when NVML cannot be loaded.  Read-only:
+    no GPU setting is changed."""
+    REASONS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40),
+               ("sw_thermal_slowdown", 0x20), ("sw_power_cap", 0x4),
+               ("hw_power_brake_slowdown", 0x80))
+
+    def __init__(self, gpu_index, period_s=0.002):
         self.gpu = gpu_index
-        self.proc = None
+        self.period = period_s
+        self.samples = []       # (sm_mhz, reasons bitmask)
+        self.max_mhz = None
+        self._stop = None
+        self._thread = None
+        self.source = None
+
+    def _loop(self, nv, h):
+        while not self._stop.is_set():
+            try:
+                sm = nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)
+                rs = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
+                self.samples.append((float(sm), int(rs)))
+            except Exception:
+                pass
+            self._stop.wait(self.period)
 
     def __enter__(self):
+        import threading
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+            import pynvml as nv
+            nv.nvmlInit()
+            idx = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(self.gpu)).split(",")[self.gpu]) \
+                if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else self.gpu
+            h = nv.nvmlDeviceGetHandleByIndex(idx)
+            self.max_mhz = float(nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM))
+            self._stop = threading.Event()
+            self._thread = threading.Thread(target=self._loop, args=(nv, h), daemon=True)
+            self._thread.start()
+            self.source = "nvml"
+        except Exception:
+            self._thread = None
+            self._smi_start()
         return self
 
+    def _smi_start(self):
+        fields = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + fields,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.proc.stdout.readline()    # running before the timed region starts
+            self.source = "nvidia-smi"
+        except OSError:
+            self.proc = None
+
     def __exit__(self, *a):
-        self.out = ""
-        if self.proc is not None:
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+            return
+        if getattr(self, "proc", None) is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                out, _ = self.proc.communicate(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out, _ = self.proc.communicate()
+                out, _ = self.proc.communicate()
+            for line in out.splitlines():
+                f = [x.strip() for x in line.split(",")]
+                try:
+                    self.samples.append((float(f[1]), int(f[4], 16)))
+                    self.max_mhz = float(f[2])
+                except (ValueError, IndexError):
+                    continue
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in (self.out or "").splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
-            except ValueError:
-                continue
-            for nm, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        sm = [s for s, _ in self.samples]
+        reasons = sorted({nm for _, r in self.samples for nm, bit in self.REASONS if r & bit})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(sm), "source": self.source}
 
 
 def dist_setup():
@@ -185,17 +237,60 @@ def allreduce_grads(layer, world):
     dist.all_reduce(layer.dtheta_R)
 
 
-def oracle_step_seconds(case, T_sample, inp):
-    """Time the CPU oracle (as it stands) on the first T_sample tokens: Cayley-
-    Neumann of both sides, forward, backward to dX and dtheta."""
-    import oracle
-    x = inp["x"][:T_sample].float().double().numpy()
-    dy = inp["dy"][:T_sample].float().double().numpy()
-    W0 = inp["W0"].float().double().numpy()
-    t0 = time.perf_counter()
-    oracle.layer(x, W0, inp["theta_P"].double().numpy(), inp["theta_R"].double().numpy(), case.n,
-                 inp["perm_in"].numpy(), inp["perm_out"].numpy(), case.b_in, case.b_out, dy=dy)
-    return time.perf_counter() - t0
+class OracleSample:
+    """The CPU oracle (as it stands) on a proportional sample of the step.
+
+    A fraction f of one step of `case`: f*T tokens of the forward and the
+    backward (through the oracle's unmerged-weight, four-permutation path with
+    the layer's Cayley-Neumann blocks), and f*(nb_P + nb_R) block
+    Cayley-Neumann forward+backward evaluations (whole blocks, carried over
+    from step to step by a credit counter), so each sampled step is the same
+    mix of work as a full step, scaled by f.  Inputs are converted to float64
+    once, outside the timing."""
+
+    def __init__(self, case, inp):
+        import oracle
+        self.o = oracle
+        self.case = case
+        self.x = inp["x"].float().double().numpy()
+        self.dy = inp["dy"].float().double().numpy()
+        self.W0 = inp["W0"].float().double().numpy()
+        self.thP = inp["theta_P"].double().numpy()
+        self.thR = inp["theta_R"].double().numpy()
+        self.pin = inp["perm_in"].numpy()
+        self.pout = inp["perm_out"].numpy()
+        self.QP = oracle.cnp(self.thP, case.b_in, case.n)
+        self.QR = oracle.cnp(self.thR, case.b_out, case.n)
+        self.dQP = np.zeros_like(self.QP)
+        self.dQR = np.zeros_like(self.QR)
+        self.credit = 0.0
+        self.next_block = 0
+        self.tok = 0
+
+    def step(self, f):
+        """Run one sampled step; returns (seconds, tokens credited = f*T)."""
+        c, o = self.case, self.o
+        nbi, nbo = c.d_in // c.b_in, c.d_out // c.b_out
+        T_s = max(1, int(round(f * c.T)))
+        t0 = time.perf_counter()
+        self.credit += f * (nbi + nbo)
+        while self.credit >= 1.0:
+            j = self.next_block % (nbi + nbo)
+            if j < nbi:
+                th, b, dQ = self.thP[j:j + 1], c.b_in, self.dQP[j:j + 1]
+            else:
+                th, b, dQ = self.thR[j - nbi:j - nbi + 1], c.b_out, self.dQR[j - nbi:j - nbi + 1]
+            o.cnp(th, b, c.n)
+            o.cnp_backward(th, b, c.n, dQ)
+            self.next_block += 1
+            self.credit -= 1.0
+        lo = self.tok % c.T
+        hi = min(c.T, lo + T_s)
+        x, dy = self.x[lo:hi], self.dy[lo:hi]
+        o.forward(x, self.W0, self.QP, self.QR, self.pin, self.pout)
+        _, self.dQP, self.dQR = o.backward(x, dy, self.W0, self.QP, self.QR, self.pin, self.pout)
+        self.tok = hi % c.T
+        return time.perf_counter() - t0, (hi - lo) * 1.0
 
 
 def host_cores():
@@ -203,16 +298,28 @@ def host_cores():
 
 
 def run_reference(args, world, rank):
-    """The reference arm: the CPU oracle on a bounded token sample per step."""
+    """The reference arm: the CPU oracle, each step a proportional sample of the
+    step sized so that warm-up plus timed steps take about REF_BUDGET_S."""
     if rank != 0:
         return
     inp = inputs.make_linear_inputs(CASE)
+    smp = OracleSample(CASE, inp)
+    cal_f = 1.0 / 64
+    t_cal, _ = smp.step(cal_f)
+    f = min(1.0 / 8, cal_f * REF_BUDGET_S / max(1, args.steps + args.warmup) / max(t_cal, 1e-6))
+    f = max(f, 1.0 / CASE.T)
     for _ in range(args.warmup):
-        oracle_step_seconds(CASE, REF_SAMPLE_TOKENS, inp)
-    ts = [oracle_step_seconds(CASE, REF_SAMPLE_TOKENS, inp) for _ in range(args.steps)]
-    total = sum(ts)
-    value = REF_SAMPLE_TOKENS * args.steps / total
-    sample = "first %d of %d tokens of the square 2048 layer per step" % (REF_SAMPLE_TOKENS, CASE.T)
+        smp.step(f)
+    total, toks = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, n = smp.step(f)
+        total += dt
+        toks += n
+    value = toks / total
+    sample = ("oracle on %.4g of each step: %d of %d tokens fwd+bwd and the matching share "
+              "of the %d block Cayley-Neumann fwd+bwd, f64" % (
+                  f, max(1, int(round(f * CASE.T))), CASE.T,
+                  CASE.d_in // CASE.b_in + CASE.d_out // CASE.b_out))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
@@ -293,10 +400,12 @@ def run_poetx(args, world, rank, local):
         barrier(world)
         torch.cuda.synchronize()
         n0 = _lib.poetx_launch_count()
+        torch.cuda.nvtx.range_push("poetx_timed")
         e0.record(stream)
         for k in range(args.steps):
             step(k)
         e1.record(stream)
+        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         barrier(world)
         launches = _lib.poetx_launch_count() - n0
@@ -372,11 +481,16 @@ def run_poetx(args, world, rank, local):
     # ---------------- CPU oracle baseline (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        secs = oracle_step_seconds(case, CPU_SAMPLE_TOKENS, inp)
-        cpu = {"value": CPU_SAMPLE_TOKENS / secs, "unit": "tokens/s", "cores": host_cores(),
-               "kind": "oracle",
-               "sample": "first %d of %d tokens of one step (CNP both sides, fwd, bwd), f64, %.1f s"
-                         % (CPU_SAMPLE_TOKENS, case.T, secs)}
+        smp = OracleSample(case, inp)
+        secs, toks = 0.0, 0.0
+        for _ in range(3):
+            dt, n = smp.step(CPU_SAMPLE_FRACTION)
+            secs += dt
+            toks += n
+        cpu = {"value": toks / secs, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
+               "sample": "3 x %.2f of one step (%d tokens fwd+bwd and the matching share of the "
+                         "block Cayley-Neumann fwd+bwd each), f64, %.1f s"
+                         % (CPU_SAMPLE_FRACTION, int(CPU_SAMPLE_FRACTION * case.T), secs)}
 
     if rank == 0:
         flops = step_flops(case)
@@ -396,8 +510,8 @@ def run_poetx(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="poetx", choices=["poetx", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
