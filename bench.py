@@ -81,6 +81,8 @@ def kernel_work(case):
         "tc_blockapply_scatter": ("hbm", blk_flops, blk_bytes),
         "tc_dq_gather_rows": ("hbm", dq_flops, dq_bytes),
         "tc_dq_gather_cols": ("hbm", dq_flops, dq_bytes),
+        "tc_dq": ("hbm", dq_flops, dq_bytes),
+        "tc_permute_cols": ("hbm", 0.0, es * (T * di + T * do)),
         "tc_cnp_fwd": ("tensor", cnp_f, cnp_fb),
         "tc_cnp_bwd_prep": ("hbm", 0.0, cnp_prep_b),
         "tc_cnp_bwd": ("tensor", 2 * cnpb_f, 2 * 2 * 2 * (nbi * bi * bi + nbo * bo * bo) / 2
@@ -146,15 +148,20 @@ class ClockSampler:
         try:
             import pynvml as nv
             nv.nvmlInit()
-            idx = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(self.gpu)).split(",")[self.gpu]) \
-                if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else self.gpu
-            h = nv.nvmlDeviceGetHandleByIndex(idx)
+            h = None
+            try:   # the NVML device of this CUDA device, by PCI address
+                p = torch.cuda.get_device_properties(self.gpu)
+                bus = "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+                h = nv.nvmlDeviceGetHandleByPciBusId(bus.encode())
+            except Exception:
+                h = nv.nvmlDeviceGetHandleByIndex(self.gpu)
             self.max_mhz = float(nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM))
             self._stop = threading.Event()
             self._thread = threading.Thread(target=self._loop, args=(nv, h), daemon=True)
             self._thread.start()
             self.source = "nvml"
-        except Exception:
+        except Exception as e:   # NVML unusable here: sample through nvidia-smi instead
+            self.nvml_error = repr(e)[:200]
             self._thread = None
             self._smi_start()
         return self
@@ -194,8 +201,11 @@ class ClockSampler:
     def summary(self):
         sm = [s for s, _ in self.samples]
         reasons = sorted({nm for _, r in self.samples for nm, bit in self.REASONS if r & bit})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
-                "reasons": reasons, "samples": len(sm), "source": self.source}
+        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+               "reasons": reasons, "samples": len(sm), "source": self.source}
+        if getattr(self, "nvml_error", None):
+            out["nvml_error"] = self.nvml_error
+        return out
 
 
 def dist_setup():

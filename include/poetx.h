@@ -82,6 +82,15 @@ int poetx_version(void);
 poetx_status poetx_cayley_neumann(const float *theta, int nb, int b, int n, void *Q,
                                   poetx_dtype out_dtype, cudaStream_t stream);
 
+/* Both factors of one layer, Q_P from theta_P and Q_R from theta_R, with the
+ * same n [§2.C: all blocks are processed as one batch]: identical results to
+ * two poetx_cayley_neumann calls, in a single launch when b_P == b_R (bf16
+ * output).  Arguments as poetx_cayley_neumann, per factor; nb_P or nb_R may be
+ * 0 (that factor is skipped and its pointers are not read). */
+poetx_status poetx_cayley_neumann_pair(const float *theta_P, int nb_P, int b_P,
+                                       const float *theta_R, int nb_R, int b_R, int n, void *Q_P,
+                                       void *Q_R, poetx_dtype out_dtype, cudaStream_t stream);
+
 /* Backward of poetx_cayley_neumann (not on the page, which only says
  * "autograd" [§2.E]; this is the chain rule of the forward):
  *   dK = sum_{m=1}^{n+1} c_m sum_{a=0}^{m-1} (K^a)^T dQ (K^{m-1-a})^T,

@@ -21,6 +21,7 @@ STATUS = {0: "POETX_OK", 1: "POETX_ERR_INVALID_ARG", 2: "POETX_ERR_SHAPE",
 
 # every symbol include/poetx.h declares
 EXPORTS = ["poetx_status_string", "poetx_version", "poetx_cayley_neumann",
+           "poetx_cayley_neumann_pair",
            "poetx_cayley_neumann_backward", "poetx_invert_perm", "poetx_check_perm",
            "poetx_merge_w0", "poetx_workspace_bytes", "poetx_forward", "poetx_backward",
            "poetx_stream_status", "poetx_launch_count", "poetx_profile_enable",
@@ -50,6 +51,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "poetx_status_string": (ctypes.c_char_p, [I]),
         "poetx_version": (I, []),
         "poetx_cayley_neumann": (I, [P, I, I, I, P, I, P]),
+        "poetx_cayley_neumann_pair": (I, [P, I, I, P, I, I, I, P, P, I, P]),
         "poetx_cayley_neumann_backward": (I, [P, P, I, I, I, P, P]),
         "poetx_invert_perm": (I, [P, P, I, P]),
         "poetx_check_perm": (I, [P, P, I, P, P]),
@@ -115,6 +117,15 @@ def poetx_cayley_neumann(theta, b, n, Q, stream=None):
     nb = theta.shape[0]
     _check("poetx_cayley_neumann", load().poetx_cayley_neumann(
         _ptr(theta), nb, b, n, _ptr(Q), dtype_code(Q.dtype), _stream(stream)))
+
+
+def poetx_cayley_neumann_pair(theta_P, b_P, theta_R, b_R, n, Q_P, Q_R, stream=None):
+    """Both factors of a layer in one call (Q_P and Q_R share a dtype)."""
+    if Q_P.dtype != Q_R.dtype:
+        raise TypeError("Q_P and Q_R must share a dtype")
+    _check("poetx_cayley_neumann_pair", load().poetx_cayley_neumann_pair(
+        _ptr(theta_P), theta_P.shape[0], b_P, _ptr(theta_R), theta_R.shape[0], b_R, n,
+        _ptr(Q_P), _ptr(Q_R), dtype_code(Q_P.dtype), _stream(stream)))
 
 
 def poetx_cayley_neumann_backward(theta, dQ, b, n, dtheta, stream=None):

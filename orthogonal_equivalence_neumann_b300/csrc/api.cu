@@ -130,6 +130,21 @@ poetx_status poetx_cayley_neumann(const float* theta, int nb, int b, int n, void
   return launch_cnp_fwd_simt(theta, nb, b, n, Q, out_dtype, stream);
 }
 
+poetx_status poetx_cayley_neumann_pair(const float* theta_P, int nb_P, int b_P,
+                                       const float* theta_R, int nb_R, int b_R, int n, void* Q_P,
+                                       void* Q_R, poetx_dtype out_dtype, cudaStream_t stream) {
+  if (!valid_dtype(out_dtype) || n < 1) return POETX_ERR_INVALID_ARG;
+  if (nb_P < 0 || nb_R < 0) return POETX_ERR_SHAPE;
+  if (!valid_block(b_P) || !valid_block(b_R)) return POETX_ERR_UNSUPPORTED;
+  if ((nb_P > 0 && (!theta_P || !Q_P || !aligned16(theta_P) || !aligned16(Q_P))) ||
+      (nb_R > 0 && (!theta_R || !Q_R || !aligned16(theta_R) || !aligned16(Q_R))))
+    return POETX_ERR_INVALID_ARG;
+  if (b_P == b_R && tc_cnp_supported(b_P, out_dtype) && nb_P + nb_R <= 65535)
+    return tc::cnp_fwd_pair_bf16ops(theta_P, nb_P, theta_R, nb_R, b_P, n, Q_P, Q_R, false, stream);
+  POETX_TRY(poetx_cayley_neumann(theta_P, nb_P, b_P, n, Q_P, out_dtype, stream));
+  return poetx_cayley_neumann(theta_R, nb_R, b_R, n, Q_R, out_dtype, stream);
+}
+
 poetx_status poetx_cayley_neumann_backward(const float* theta, const float* dQ, int nb, int b,
                                            int n, float* dtheta, cudaStream_t stream) {
   if (n < 1) return POETX_ERR_INVALID_ARG;
@@ -272,7 +287,10 @@ poetx_status poetx_backward(const void* x, const void* dy, const void* W0m, cons
   if (dt == POETX_BF16 && tc::cnp_supported(b_in) && tc::cnp_supported(b_out) &&
       nb_in + nb_out <= 65535) {
     POETX_TRY(tc::cnp_bwd_layer(theta_P, dqp, nb_in, b_in, theta_R, dqr, nb_out, b_out, n,
-                                dtheta_P, dtheta_R, tc_ws, stream));
+                                dtheta_P, dtheta_R,
+                                static_cast<char*>(tc_ws) +
+                                    tc_cnp_ws_offset(T, d_in, d_out, b_in, b_out),
+                                stream));
   } else {
     POETX_TRY(launch_cnp_bwd_simt(theta_P, dqp, nb_in, b_in, n, dtheta_P, stream));
     POETX_TRY(launch_cnp_bwd_simt(theta_R, dqr, nb_out, b_out, n, dtheta_R, stream));

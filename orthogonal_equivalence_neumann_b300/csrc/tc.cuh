@@ -14,6 +14,7 @@ poetx_status tc_cnp_fwd(const float* theta, int nb, int b, int n, void* Q, poetx
 bool tc_linear_supported(int d_in, int d_out, int b_in, int b_out, poetx_dtype dt);
 size_t tc_workspace_bytes(int T, int d_in, int d_out, int b_in, int b_out, poetx_dtype dt,
                           bool backward);
+size_t tc_cnp_ws_offset(int T, int d_in, int d_out, int b_in, int b_out);
 poetx_status tc_forward(const void* x, const void* W0m, const void* Q_P, const void* Q_R,
                         const int32_t* perm_in, const int32_t* inv_in, const int32_t* perm_out,
                         const int32_t* inv_out, int T, int d_in, int d_out, int b_in, int b_out,
@@ -39,17 +40,32 @@ bool blockapply_supported(int d, int b);
 poetx_status blockapply_bf16(const void* in, void* out, const void* Q, const int32_t* perm, int T,
                              int d, int b, bool transpose_q, bool scatter, cudaStream_t s);
 
-// dQ_j[i][k] = sum_t G[t][gG(jb+i)] V[t][gV(jb+k)], exactly one of gG, gV a
-// permutation (the other NULL = identity); fp32 out [d/b, b, b], overwritten.
+// The same permuted block apply over a thread-block cluster: the permutation
+// travels between the CTAs' shared memories and each CTA keeps its blocks'
+// Qop in tensor memory.  `inv` is the inverse of `perm` (gather form only).
+bool cluster_apply_supported(int d, int b, bool scatter);
+poetx_status cluster_apply_bf16(const void* in, void* out, const void* Q, const int32_t* perm,
+                                const int32_t* inv, int T, int d, int b, bool transpose_q,
+                                bool scatter, cudaStream_t s);
+
+// dQ_j[i][k] = sum_t G[t][jb+i] V[t][jb+k] (both operands already gathered);
+// fp32 out [d/b, b, b], overwritten.
 bool dq_supported(int d, int b);
-poetx_status dq_bf16(const void* G, const void* V, int T, int d, int b, const int32_t* gG,
-                     const int32_t* gV, float* dQ, cudaStream_t s);
+poetx_status dq_bf16(const void* G, const void* V, int T, int d, int b, float* dQ, cudaStream_t s);
+
+// out[t][c] = in[t][perm[c]] for bf16 token-major [T, d] (one pass over HBM).
+bool permute_supported(int d);
+poetx_status permute_cols_bf16(const void* in, void* out, const int32_t* perm, int T, int d,
+                               cudaStream_t s);
 
 // Cayley-Neumann forward / backward with bf16 operands and fp32 accumulation
 // (tcgen05), b in {128, 256}.  The backward overwrites dtheta.
 bool cnp_supported(int b);
 poetx_status cnp_fwd_bf16ops(const float* theta, int nb, int b, int n, void* Q, bool out_f32,
                              cudaStream_t s);
+// Both factors of a layer (same b) in one launch.
+poetx_status cnp_fwd_pair_bf16ops(const float* theta0, int nb0, const float* theta1, int nb1,
+                                  int b, int n, void* Q0, void* Q1, bool out_f32, cudaStream_t s);
 // Backward of both sides of a layer in one launch (after a prep kernel that
 // writes dense bf16 K and G into `ws`, cnp_bwd_workspace_bytes of it).
 size_t cnp_bwd_workspace_bytes(int d_in, int b_in, int d_out, int b_out);

@@ -5,7 +5,7 @@ permutations and their inverses, skew parameters, the Cayley-Neumann blocks,
 the saved activation and the workspace) and calls the C entry points in the
 order of one training step:
 
-  1. poetx_cayley_neumann for P and R      [POET-X §2.D]
+  1. poetx_cayley_neumann_pair (P and R)  [POET-X §2.C-§2.D]
   2. poetx_forward   y = R (W0 (P x))      [POET-X §2.A-§2.C]
   3. poetx_backward  dX, dtheta_P, dtheta_R
 
@@ -53,8 +53,8 @@ class TransformedLinear:
                   if save_z else None)
 
     def cayley_neumann(self):
-        _lib.poetx_cayley_neumann(self.theta_P, self.b_in, self.n, self.Q_P)
-        _lib.poetx_cayley_neumann(self.theta_R, self.b_out, self.n, self.Q_R)
+        _lib.poetx_cayley_neumann_pair(self.theta_P, self.b_in, self.theta_R, self.b_out, self.n,
+                                       self.Q_P, self.Q_R)
 
     def forward(self, x, y=None):
         T = x.shape[0]

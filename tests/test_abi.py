@@ -73,6 +73,12 @@ def test_host_validation_rejects_before_launch(lib):
     # misaligned pointer
     assert lib.poetx_cayley_neumann(ctypes.c_void_p(8), 4, 32, 3, ctypes.c_void_p(16),
                                     _lib.F32, null) == 1
+    pair = lib.poetx_cayley_neumann_pair
+    assert pair(null, 4, 24, null, 4, 32, 3, null, null, _lib.BF16, null) == 3   # b_P unsupported
+    assert pair(null, 4, 32, null, -1, 32, 3, null, null, _lib.BF16, null) == 2  # nb_R < 0
+    assert pair(null, 4, 32, null, 4, 32, 0, null, null, _lib.BF16, null) == 1   # n < 1
+    assert pair(null, 4, 32, null, 0, 32, 3, null, null, _lib.BF16, null) == 1   # null theta_P
+    assert pair(null, 0, 32, null, 0, 32, 3, null, null, _lib.BF16, null) == 0   # nothing to do
     assert lib.poetx_cayley_neumann_backward(null, null, 4, 32, 0, null, null) == 1
     assert lib.poetx_invert_perm(null, null, -3, null) == 2
     assert lib.poetx_merge_w0(null, null, 0, 4, _lib.F32, null, null, null) == 2

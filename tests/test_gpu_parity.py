@@ -140,6 +140,25 @@ def test_cnp_backward_parity(b, n):
 
 # ------------------------------------------------------------------ index maps
 
+@pytest.mark.parametrize("b_P,b_R", [(256, 256), (128, 128), (256, 128), (32, 64)])
+def test_cnp_pair_matches_single_calls(b_P, b_R):
+    """poetx_cayley_neumann_pair (both factors of a layer, one launch when the
+    block sizes agree) computes exactly what two single calls compute."""
+    thP = inputs.make_theta(8, b_P, 0.01, 77).cuda()
+    thR = inputs.make_theta(6, b_R, 0.01, 78).cuda()
+    bf = torch.bfloat16
+    QP = torch.empty(8, b_P, b_P, dtype=bf, device="cuda")
+    QR = torch.empty(6, b_R, b_R, dtype=bf, device="cuda")
+    _lib.poetx_cayley_neumann_pair(thP, b_P, thR, b_R, 3, QP, QR)
+    QP1, QR1 = torch.empty_like(QP), torch.empty_like(QR)
+    _lib.poetx_cayley_neumann(thP, b_P, 3, QP1)
+    _lib.poetx_cayley_neumann(thR, b_R, 3, QR1)
+    _lib.poetx_stream_status()
+    assert torch.equal(QP, QP1) and torch.equal(QR, QR1)
+    ref = oracle.cnp(thR.double().cpu().numpy(), b_R, 3)
+    assert_close("Q_R", to64(QR), ref, TOL_BF16)
+
+
 @pytest.mark.parametrize("d", [1, 7, 256, 2048, 5632])
 def test_invert_perm_bit_exact(d):
     perm = torch.randperm(d, generator=torch.Generator().manual_seed(d)).to(torch.int32)
@@ -198,12 +217,20 @@ def test_layer_bf16_tiles_and_ragged_tail(b_in, b_out, T):
 
 
 def test_xfast_and_xmem_give_the_same_gradients():
+    """POET-Xmem recomputes z with the forward's own kernels, so y and dX are
+    bit-identical to POET-Xfast.  The block gradients are token sums reduced
+    with fp32 atomics, whose order varies from run to run; the bf16 rounding of
+    dQ inside the Cayley-Neumann backward can turn a last-bit difference into a
+    bf16 step, so dtheta is compared at 1e-5 (one fp32 reduction-order effect
+    through bf16 operands), far below the 2e-2 parity bar."""
     case = inputs.LinearCase("xmem", 512, 512, 128, 128, 3, 300, 0.005, "bf16", 801)
     inp = inputs.make_linear_inputs(case)
     a = gpu_layer(case, inp, save_z=True)
     b = gpu_layer(case, inp, save_z=False)
-    for k in ("y", "dX", "dtheta_P", "dtheta_R"):
-        assert_close(k, b[k], a[k], 1e-6)
+    for k in ("y", "dX"):
+        assert np.array_equal(b[k], a[k]), k
+    for k in ("dtheta_P", "dtheta_R"):
+        assert_close(k, b[k], a[k], 1e-5)
 
 
 def test_zero_tokens_is_a_no_op_with_zero_gradients():
