@@ -43,10 +43,12 @@ poetx_status blockapply_bf16(const void* in, void* out, const void* Q, const int
 // The same permuted block apply over a thread-block cluster: the permutation
 // travels between the CTAs' shared memories and each CTA keeps its blocks'
 // Qop in tensor memory.  `inv` is the inverse of `perm` (gather form only).
+// Scratch: a small exchange ring in `ws` (cluster_apply_workspace_bytes).
 bool cluster_apply_supported(int d, int b, bool scatter);
+size_t cluster_apply_workspace_bytes(int d, int b, bool scatter);
 poetx_status cluster_apply_bf16(const void* in, void* out, const void* Q, const int32_t* perm,
                                 const int32_t* inv, int T, int d, int b, bool transpose_q,
-                                bool scatter, cudaStream_t s);
+                                bool scatter, void* ws, size_t ws_bytes, cudaStream_t s);
 
 // dQ_j[i][k] = sum_t G[t][jb+i] V[t][jb+k] (both operands already gathered);
 // fp32 out [d/b, b, b], overwritten.

@@ -11,29 +11,29 @@
 // scatter(z B_R^T) and dX = scatter(g_u B_P)).
 //
 // A cluster of C CTAs works on one 64-token tile at a time.  CTA c owns the
-// natural feature columns [c*F, (c+1)*F) (F = d/C) for loading or storing, and
-// the blocks [c*G, (c+1)*G) (G = d/(b*C)) for the products, whose Qop blocks
-// it keeps in tensor memory for the whole launch (the MMA reads A from TMEM).
-// The permutation is carried out on chip: 16-byte pieces (8 tokens of one
-// feature) travel between the CTAs' shared memories with st.async, each
-// counted against the receiving CTA's mbarrier, so no permuted copy of an
-// activation is ever written to HBM and every activation byte crosses HBM
-// once.
-//   GATHER_IN:   TMA loads the tile's own columns [64 tokens x F] -> worker
-//                warps cut them into feature pieces and send each to the CTA
-//                that owns its block, at its gathered position -> that CTA's
-//                MMA (M = 128 outputs, N = 64 tokens, K = 16) reads the
-//                received [b features x 64 tokens] operand -> the epilogue
-//                writes the block's contiguous output columns.
+// natural feature columns [c*F, (c+1)*F) (F = d/C) for loading or storing,
+// and the blocks [c*G, (c+1)*G) (G = d/(b*C)) for the products, whose Qop it
+// keeps in tensor memory for the whole launch (the MMA reads A from TMEM).
+// Activations cross HBM once.  The permutation is carried out in 128-byte
+// feature rows (the 64 tokens of one feature): a CTA writes each row it
+// produces straight to its place in a small per-cluster exchange ring in the
+// workspace (a few MB, rewritten every few microseconds, so it lives in L2),
+// and the CTA that needs the rows fetches its whole part with one bulk copy.
+// Hand-offs use cluster mbarriers (remote arrive after a cluster-scope fence).
+//   GATHER_IN:   TMA loads the tile's own columns [64 tokens x F] -> mover
+//                warps write each feature row to the part of the CTA owning
+//                its block, at its gathered position -> that CTA's loader
+//                fetches its [G*b features x 64 tokens] operand -> MMA
+//                (M = 128 outputs, N = 64 tokens, K = 16) -> the epilogue
+//                stages the output tile in token rows and stores it by TMA.
 //   SCATTER_OUT: TMA loads the own blocks' contiguous input columns -> MMA ->
-//                the epilogue sends each output feature (a TMEM lane) to the
-//                CTA owning its scattered column -> that CTA transposes the
-//                received [F features x 64 tokens] to token rows and stores
-//                them with TMA.
-// Flow control: a receive buffer is refilled only after its owner has
-// released it to every sender (remote mbarrier arrive).  Every wait is
-// bounded (see tc_ptx.cuh); the cluster barriers at start and end are
-// reached by every thread unconditionally.
+//                the epilogue writes each output feature row (a TMEM lane)
+//                to the part of the CTA owning its scattered column -> that
+//                CTA's loader fetches its [F features x 64 tokens] -> mover
+//                warps transpose it to token rows -> TMA store.
+// Flow control: a slot is rewritten only after every CTA that reads it has
+// fetched it.  Every wait is bounded (see tc_ptx.cuh); the cluster barriers
+// at start and end are reached by every thread unconditionally.
 #include "common.cuh"
 #include "profile.cuh"
 #include "tc.cuh"
@@ -46,14 +46,19 @@ namespace tc {
 namespace {
 
 constexpr int TT = 64;                 // tokens per tile (MMA N)
-constexpr int kCaThreads = 448;        // warp 0 TMA, warp 1 MMA, warps 2..9 movers, 10..13 epilogue
+constexpr int kCaThreads = 480;        // warp 0 TMA, 1 MMA, 2..9 movers, 10..13 epilogue, 14 loader
 constexpr int kMovers = 256;
 constexpr int kSmemLimit = 232448;
+constexpr int kMaxSlots = 4;           // exchange slots in the workspace ring
 
 struct CaGeo {
   int C, G, F;        // cluster size, blocks per CTA, features per CTA
-  int NS, NR, NA;     // ring depths: staged input, receive buffers, accumulators
-  int s_bytes, r_bytes, st_bytes;
+  int NS, NR, NA;     // ring depths: staged input, fetched parts in shared memory, accumulators
+  int NST;            // output staging tiles (TMA store sources)
+  int NX;             // exchange slots in the workspace ring
+  int s_bytes;        // input tile in shared memory
+  int r_bytes;        // one CTA's part of an exchange slot (rows of 128 bytes)
+  int st_bytes;       // token-row staging of the output tile for the TMA store
   int q_cols, a_cols, tmem_cols;
   int hdr;            // barriers + routing table, in front of the pipeline buffers
   int smem;
@@ -62,68 +67,154 @@ struct CaGeo {
 __device__ __forceinline__ void movers_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(kMovers) : "memory");
 }
+__device__ __forceinline__ void epi_bar() {
+  asm volatile("bar.sync 2, 128;" ::: "memory");
+}
 
 __device__ __forceinline__ uint4 pack8f(const float* v) {
   return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
                     pack_bf16x2(v[6], v[7]));
 }
 
-// Loads Qop_j of the CTA's G blocks into tensor memory (lanes = rows i, two
-// bf16 of consecutive k per 32-bit column), staging Q through shared memory.
-// Called by all threads; `stage` must hold G * B * B bf16.
+// Set-up shared by both forms: thread 0 brings the CTA's G blocks of Q into
+// shared memory by TMA (128-byte swizzled 64 x 64 boxes, which makes both the
+// row reads and the column reads below conflict-free); the four epilogue
+// warps then write Qop_j into tensor memory (lanes = rows i, two bf16 of
+// consecutive k per 32-bit column).
+__device__ __forceinline__ void issue_q_loads(const CUtensorMap* tmQ, uint8_t* stage, int j0, int G,
+                                              int B, uint64_t* q_full) {
+  mbar_arrive_expect_tx(q_full, (uint32_t)(G * B * B * 2));
+  for (int jj = 0; jj < G; ++jj)
+    for (int rb = 0; rb < B / 64; ++rb)
+      for (int cb = 0; cb < B / 64; ++cb)
+        tma_load_2d(stage + jj * (B * B * 2) + cb * (B * 128) + rb * (64 * 128), tmQ, cb * 64,
+                    (j0 + jj) * B + rb * 64, q_full);
+}
+
+// Byte offset of Q[row][col] in the staged block.
 template <int B>
-__device__ void load_q_to_tmem(const __nv_bfloat16* __restrict__ Q, int j0, int G, int transpose_q,
-                               uint8_t* stage, uint32_t tmem_base) {
-  constexpr int P = B + 8;   // padded row pitch (elements): row reads of 16 bytes avoid conflicts
-  const uint4* src = reinterpret_cast<const uint4*>(Q + (size_t)j0 * B * B);
-  for (int u = threadIdx.x; u < G * B * B / 8; u += blockDim.x) {
-    const int row = u / (B / 8), c8 = u % (B / 8);
-    *reinterpret_cast<uint4*>(stage + ((size_t)row * P + c8 * 8) * 2) = __ldg(src + u);
-  }
-  __syncthreads();
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  if (warp >= 10) {
-    const int quarter = warp % 4;
-    const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(stage);
-    constexpr int halves = B / 128;
-    for (int jj = 0; jj < G; ++jj)
-      for (int h = 0; h < halves; ++h) {
-        const int i = h * 128 + quarter * 32 + lane;
-        const __nv_bfloat16* blk = qs + (size_t)jj * B * P;
-        const uint32_t col0 = (uint32_t)((jj * halves + h) * (B / 2));
-        for (int c = 0; c < B / 2; c += 32) {
-          uint32_t r[32];
-          if (transpose_q) {
-            // row i of Q^T is column i of Q: lanes read consecutive columns of one row
+__device__ __forceinline__ uint32_t qst_off(int row, int col) {
+  return (uint32_t)((col >> 6) * (B * 128) + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) +
+                    (col & 7) * 2);
+}
+
+template <int B>
+__device__ void q_stage_to_tmem(const uint8_t* stage, int G, int transpose_q, uint32_t tmem_base,
+                                int quarter, int lane) {
+  constexpr int halves = B / 128;
+  for (int jj = 0; jj < G; ++jj)
+    for (int h = 0; h < halves; ++h) {
+      const int i = h * 128 + quarter * 32 + lane;
+      const uint8_t* blk = stage + (size_t)jj * B * B * 2;
+      const uint32_t col0 = (uint32_t)((jj * halves + h) * (B / 2));
+      for (int c = 0; c < B / 2; c += 32) {
+        uint32_t r[32];
+        if (transpose_q) {
+          // row i of Q^T is column i of Q: lanes read consecutive columns of one row
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int k = 2 * (c + e);
-              r[e] = (uint32_t)__bfloat16_as_ushort(blk[(size_t)k * P + i]) |
-                     ((uint32_t)__bfloat16_as_ushort(blk[(size_t)(k + 1) * P + i]) << 16);
-            }
-          } else {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const uint4 v = *reinterpret_cast<const uint4*>(blk + (size_t)i * P + 2 * c + 8 * q);
-              r[4 * q] = v.x; r[4 * q + 1] = v.y; r[4 * q + 2] = v.z; r[4 * q + 3] = v.w;
-            }
+          for (int e = 0; e < 32; ++e) {
+            const int k = 2 * (c + e);
+            const uint16_t lo = *reinterpret_cast<const uint16_t*>(blk + qst_off<B>(k, i));
+            const uint16_t hi = *reinterpret_cast<const uint16_t*>(blk + qst_off<B>(k + 1, i));
+            r[e] = (uint32_t)lo | ((uint32_t)hi << 16);
           }
-          tmem_st32(tmem_base + col0 + (uint32_t)c + ((uint32_t)(quarter * 32) << 16), r);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint4 v = *reinterpret_cast<const uint4*>(blk + qst_off<B>(i, 2 * c + 8 * q));
+            r[4 * q] = v.x; r[4 * q + 1] = v.y; r[4 * q + 2] = v.z; r[4 * q + 3] = v.w;
+          }
         }
+        tmem_st32(tmem_base + col0 + (uint32_t)c + ((uint32_t)(quarter * 32) << 16), r);
       }
-    tmem_st_wait();
+    }
+  tmem_st_wait();
+}
+
+// Barrier block (uint64 words) shared by both kernels.
+struct Bars {
+  uint64_t* s_full;     // [4] input tile landed (TMA)
+  uint64_t* s_empty;    // [4] input tile consumed
+  uint64_t* x_full;     // [4] every writer has written this CTA's part of an exchange slot
+  uint64_t* x_free;     // [4] every reader has fetched its part of an exchange slot
+  uint64_t* r_full;     // [2] fetched part landed in shared memory
+  uint64_t* r_empty;    // [2] fetched part consumed
+  uint64_t* a_full;     // [2] accumulators ready
+  uint64_t* a_empty;    // [2] accumulators drained
+  uint64_t* q_full;
+  uint32_t* tmem_slot;
+};
+
+__device__ __forceinline__ Bars bars_at(uint8_t* smem) {
+  uint64_t* b = reinterpret_cast<uint64_t*>(smem);
+  Bars r;
+  r.s_full = b;
+  r.s_empty = b + 4;
+  r.x_full = b + 8;
+  r.x_free = b + 12;
+  r.r_full = b + 16;
+  r.r_empty = b + 18;
+  r.a_full = b + 20;
+  r.a_empty = b + 22;
+  r.q_full = b + 24;
+  r.tmem_slot = reinterpret_cast<uint32_t*>(b + 25);
+  return r;
+}
+
+// s_empty arrivals: GATHER = the 256 movers, SCATTER = the MMA commit.
+// r_empty arrivals: GATHER = the MMA commit, SCATTER = one mover.
+__device__ __forceinline__ void init_bars(const Bars& br, int C, uint32_t s_empty_count) {
+  for (int i = 0; i < kMaxSlots; ++i) {
+    mbar_init(br.x_full + i, (uint32_t)C);
+    mbar_init(br.x_free + i, (uint32_t)C);
+    mbar_init(br.s_full + i, 1);
+    mbar_init(br.s_empty + i, s_empty_count);
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
+  for (int i = 0; i < 2; ++i) {
+    mbar_init(br.r_full + i, 1);
+    mbar_init(br.r_empty + i, 1);
+    mbar_init(br.a_full + i, 1);
+    mbar_init(br.a_empty + i, 128);
+  }
+  mbar_init(br.q_full, 1);
+  fence_mbar_init();
+}
+
+// The loader warp (one thread): fetches this CTA's part of every exchange
+// slot once all C writers have filled it.
+__device__ __forceinline__ void loader_loop(const Bars& br, const CaGeo& g, uint8_t* rbuf,
+                                            const uint8_t* part0, size_t slot_stride, int cluster_id,
+                                            int n_clusters, int n_tiles, bool& ok, int* err) {
+  for (int it = 0, tile = cluster_id; tile < n_tiles && ok; tile += n_clusters, ++it) {
+    const int r = it % g.NR, x = it % g.NX;
+    if (!(ok = mbar_wait(br.r_empty + r, ((it / g.NR) & 1) ^ 1, err))) break;   // buffer free
+    if (!(ok = mbar_wait_cluster(br.x_full + x, (it / g.NX) & 1, err))) break;  // slot written
+    fence_proxy_async_global();
+    mbar_arrive_expect_tx(br.r_full + r, (uint32_t)g.r_bytes);
+    bulk_load_g2s(rbuf + r * g.r_bytes, part0 + (size_t)x * slot_stride, (uint32_t)g.r_bytes,
+                  br.r_full + r);
+  }
+}
+
+// Remote arrives on barrier `bar` of every CTA of the cluster, one per
+// calling thread: thread `who` (0 <= who < C) signals CTA `who`, so the C
+// arrivals go out in parallel.  `release` orders the memory accesses the
+// caller has made or observed (e.g. through a CTA barrier) before the
+// arrival, cluster-wide; without it the arrival is a pure signal.
+__device__ __forceinline__ void arrive_one(uint64_t* bar, int who, int C, bool release) {
+  if (who < C) {
+    const uint32_t ra = mapa_shared(smem_u32(bar), (uint32_t)who);
+    if (release) mbar_arrive_remote(ra);
+    else mbar_arrive_remote_relaxed(ra);
+  }
 }
 
 // ======================================================================== GATHER_IN
 template <int B>
 __global__ void __launch_bounds__(kCaThreads, 1)
-    ca_gather_kernel(const __grid_constant__ CUtensorMap tmIn, const __nv_bfloat16* __restrict__ Q,
-                     const int32_t* __restrict__ inv, __nv_bfloat16* __restrict__ out, int T, int d,
-                     CaGeo g, int transpose_q, int* err) {
+    ca_gather_kernel(const __grid_constant__ CUtensorMap tmIn, const __grid_constant__ CUtensorMap tmOut,
+                     const __grid_constant__ CUtensorMap tmQ, const int32_t* __restrict__ inv,
+                     uint8_t* __restrict__ xchg, int T, CaGeo g, int transpose_q, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -131,14 +222,8 @@ __global__ void __launch_bounds__(kCaThreads, 1)
   const int C = g.C, G = g.G, F = g.F;
   const int s_off = g.hdr;
   const int r_off = s_off + g.NS * g.s_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* s_full = bars;          // [2]
-  uint64_t* s_empty = bars + 2;     // [2]
-  uint64_t* r_full = bars + 4;      // [2]
-  uint64_t* dst_free = bars + 6;    // [2]
-  uint64_t* a_full = bars + 8;      // [2]
-  uint64_t* a_empty = bars + 10;    // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  const int o_off = r_off + g.NR * g.r_bytes;
+  const Bars br = bars_at(smem);
   uint32_t* table = reinterpret_cast<uint32_t*>(smem + 256);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -146,63 +231,77 @@ __global__ void __launch_bounds__(kCaThreads, 1)
   const int cluster_id = blockIdx.x / C;
   const int n_clusters = gridDim.x / C;
   const int n_tiles = (T + TT - 1) / TT;
-  const int r_bytes = g.r_bytes;
+  // exchange ring of this cluster: [slot r][reader CTA q][r_bytes]
+  const size_t slot_stride = (size_t)C * g.r_bytes;
+  uint8_t* ring = xchg + (size_t)cluster_id * g.NX * slot_stride;
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(s_full + i, 1);
-      mbar_init(s_empty + i, kMovers);
-      mbar_init(r_full + i, 1);
-      mbar_init(dst_free + i, C);
-      mbar_init(a_full + i, 1);
-      mbar_init(a_empty + i, 128);
-    }
-    fence_mbar_init();
-    // the first use of every receive buffer expects G blocks x b features x 64 tokens
-    for (int i = 0; i < g.NR; ++i) mbar_arrive_expect_tx(r_full + i, (uint32_t)r_bytes);
-  }
-  if (warp == 1) tmem_alloc(tmem_slot, (uint32_t)g.tmem_cols);
-  // destination of each owned feature: (CTA << 24) | byte offset of its K row in the buffer
+  if (threadIdx.x == 0) init_bars(br, C, kMovers);
+  if (warp == 1) tmem_alloc(br.tmem_slot, (uint32_t)g.tmem_cols);
+  // each owned feature's row: (reader CTA << 24) | byte offset of its row in that CTA's part
   for (int f = threadIdx.x; f < F; f += blockDim.x) {
     const int p = __ldg(inv + c * F + f);
     const int j = p / B, k = p % B;
-    const int dest = j / G, jj = j % G;
-    table[f] = ((uint32_t)dest << 24) |
-               (uint32_t)(jj * (B * TT * 2) + (k >> 3) * 1024 + (k & 7) * 128);
+    table[f] = ((uint32_t)(j / G) << 24) | (uint32_t)(((j % G) * B + k) * 128);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  load_q_to_tmem<B>(Q, c * G, G, transpose_q, smem + g.hdr, tmem_base);
+  const uint32_t tmem_base = *br.tmem_slot;
+  // Q through the (still idle) pipeline buffers into tensor memory
+  if (threadIdx.x == 0) issue_q_loads(&tmQ, smem + s_off, c * G, G, B, br.q_full);
+  bool ok = true;
+  if (warp >= 10 && warp < 14) {
+    if ((ok = mbar_wait(br.q_full, 0, err)))
+      q_stage_to_tmem<B>(smem + s_off, G, transpose_q, tmem_base, warp % 4, lane);
+  }
+  tc_fence_before();
+  __syncthreads();
+  // the first input tiles (the Q stage they overwrite has been read)
+  int prefetched = 0;
+  if (threadIdx.x == 0) {
+    fence_proxy_async_smem();
+    for (int tile = cluster_id; tile < n_tiles && prefetched < g.NS; tile += n_clusters, ++prefetched) {
+      mbar_arrive_expect_tx(br.s_full + prefetched, (uint32_t)g.s_bytes);
+      uint8_t* dst = smem + s_off + prefetched * g.s_bytes;
+      for (int q = 0; q < F / 64; ++q)
+        tma_load_2d(dst + q * (TT * 128), &tmIn, c * F + q * 64, tile * TT, br.s_full + prefetched);
+    }
+  }
   cluster_sync();   // every CTA's barriers are initialised before any remote access
+  tc_fence_after();
 
   const uint32_t acc0 = tmem_base + (uint32_t)g.q_cols;
-  bool ok = true;
   if (warp == 0) {
-    // ---------------------------------------------------------------- TMA
+    // ---------------------------------------------------------------- TMA: own columns of the tile
     if (lane == 0) {
       for (int it = 0, tile = cluster_id; tile < n_tiles && ok; tile += n_clusters, ++it) {
+        if (it < prefetched) continue;
         const int s = it % g.NS;
-        if (!(ok = mbar_wait(s_empty + s, ((it / g.NS) & 1) ^ 1, err))) break;
-        mbar_arrive_expect_tx(s_full + s, (uint32_t)g.s_bytes);
+        if (!(ok = mbar_wait(br.s_empty + s, ((it / g.NS) & 1) ^ 1, err))) break;
+        mbar_arrive_expect_tx(br.s_full + s, (uint32_t)g.s_bytes);
         uint8_t* dst = smem + s_off + s * g.s_bytes;
         for (int q = 0; q < F / 64; ++q)
-          tma_load_2d(dst + q * (TT * 128), &tmIn, c * F + q * 64, tile * TT, s_full + s);
+          tma_load_2d(dst + q * (TT * 128), &tmIn, c * F + q * 64, tile * TT, br.s_full + s);
       }
     }
+  } else if (warp == 14) {
+    // ---------------------------------------------------------------- loader
+    if (lane == 0)
+      loader_loop(br, g, smem + r_off, ring + (size_t)c * g.r_bytes, slot_stride, cluster_id,
+                  n_clusters, n_tiles, ok, err);
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(128, TT, false, true);
-      for (int it = 0, tile = cluster_id; tile < n_tiles && ok; tile += n_clusters, ++it) {
-        const int r = it % g.NR, a = it % g.NA;
-        if (!(ok = mbar_wait_cluster(r_full + r, (it / g.NR) & 1, err))) break;
-        mbar_arrive_expect_tx(r_full + r, (uint32_t)r_bytes);   // the buffer's next use
-        fence_proxy_async_smem();
-        if (!(ok = mbar_wait(a_empty + a, ((it / g.NA) & 1) ^ 1, err))) break;
+    // The whole warp follows the fetched parts; lanes 1..C tell the writers
+    // that this CTA's part of the slot has been fetched, lane 0 issues the MMAs.
+    const uint32_t idesc = idesc_bf16(128, TT, false, true);
+    for (int it = 0, tile = cluster_id; tile < n_tiles && ok; tile += n_clusters, ++it) {
+      const int r = it % g.NR, a = it % g.NA;
+      if (!(ok = mbar_wait(br.r_full + r, (it / g.NR) & 1, err))) break;
+      if (lane >= 1) arrive_one(br.x_free + it % g.NX, lane - 1, C, false);
+      if (lane == 0) {
+        if (!(ok = mbar_wait(br.a_empty + a, ((it / g.NA) & 1) ^ 1, err))) break;
         tc_fence_after();
-        const uint32_t rb = smem_u32(smem + r_off + r * r_bytes);
+        const uint32_t rb = smem_u32(smem + r_off + r * g.r_bytes);
         for (int jj = 0; jj < G; ++jj)
           for (int h = 0; h < halves; ++h) {
             const uint32_t d_tmem = acc0 + (uint32_t)(((a * G + jj) * halves + h) * TT);
@@ -213,71 +312,102 @@ __global__ void __launch_bounds__(kCaThreads, 1)
               mma_bf16_ts(d_tmem, a_tmem + (uint32_t)(kk * 8), bdesc, idesc, kk != 0);
             }
           }
-        mma_commit(a_full + a);
+        mma_commit(br.r_empty + r);
+        mma_commit(br.a_full + a);
       }
     }
   } else if (warp < 10) {
-    // ---------------------------------------------------------------- movers: send feature pieces
+    // ---------------------------------------------------------------- movers: write feature rows
+    // A mover owns features of the tile: it collects the 64 tokens of a
+    // feature (8 x 16 bytes, placed in the row's 128-byte swizzle order) and
+    // writes the row into the exchange part of the CTA owning its block.
     const int pt = threadIdx.x - 64;
-    const uint32_t rbase = smem_u32(smem + r_off);
-    const uint32_t rfull0 = smem_u32(r_full);
     for (int it = 0, tile = cluster_id; tile < n_tiles && ok; tile += n_clusters, ++it) {
-      const int s = it % g.NS, r = it % g.NR;
-      if (!(ok = mbar_wait(s_full + s, (it / g.NS) & 1, err))) break;
-      if (!(ok = mbar_wait_cluster(dst_free + r, ((it / g.NR) & 1) ^ 1, err))) break;
+      const int s = it % g.NS, x = it % g.NX;
+      if (!(ok = mbar_wait(br.s_full + s, (it / g.NS) & 1, err))) break;
+      // every reader has fetched this slot's previous contents
+      if (!(ok = mbar_wait_cluster(br.x_free + x, ((it / g.NX) & 1) ^ 1, err))) break;
       const uint8_t* S = smem + s_off + s * g.s_bytes;
-      for (int w = pt; w < F * (TT / 8); w += kMovers) {
-        const int f = w % F, grp = w / F, t8 = grp * 8;
-        float v[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int row = t8 + e;
-          const uint32_t off = (uint32_t)((f >> 6) * (TT * 128) + row * 128 +
-                                          ((((f >> 3) & 7) ^ (row & 7)) << 4) + (f & 7) * 2);
-          v[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(S + off));
-        }
+      uint8_t* slot = ring + (size_t)x * slot_stride;
+      for (int f = pt; f < F; f += kMovers) {
         const uint32_t ent = table[f];
-        const uint32_t dest = ent >> 24, roff = ent & 0xFFFFFFu;
+        const uint32_t roff = ent & 0xFFFFFFu;
         const uint32_t k7 = (roff >> 7) & 7u;
-        const uint32_t laddr = rbase + (uint32_t)(r * r_bytes) + roff + ((((uint32_t)grp) ^ k7) << 4);
-        st_async_v4(mapa_shared(laddr, dest), pack8f(v), mapa_shared(rfull0 + 8u * r, dest));
+        uint8_t* row = slot + (size_t)(ent >> 24) * g.r_bytes + roff;
+#pragma unroll
+        for (int grp = 0; grp < TT / 8; ++grp) {
+          float v[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int tr = grp * 8 + e;
+            const uint32_t off = (uint32_t)((f >> 6) * (TT * 128) + tr * 128 +
+                                            ((((f >> 3) & 7) ^ (tr & 7)) << 4) + (f & 7) * 2);
+            v[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(S + off));
+          }
+          *reinterpret_cast<uint4*>(row + ((((uint32_t)grp) ^ k7) << 4)) = pack8f(v);
+        }
       }
-      mbar_arrive(s_empty + s);
+      mbar_arrive(br.s_empty + s);
+      movers_bar();
+      // the movers' rows are visible before the hand-off (release, after the barrier)
+      arrive_one(br.x_full + x, pt, C, true);
     }
   } else {
     // ---------------------------------------------------------------- epilogue
+    // TMEM lanes are output features, columns tokens: each thread writes its
+    // feature's 64 tokens into a token-row staging tile (128-byte swizzle, the
+    // TMA store layout); one thread then stores the tile with TMA.
     const int quarter = warp % 4;
-    const uint32_t dfree0 = smem_u32(dst_free);
+    const int et = threadIdx.x - 320;   // 0..127
+    bool pending = false;
     for (int it = 0, tile = cluster_id; tile < n_tiles && ok; tile += n_clusters, ++it) {
-      const int r = it % g.NR, a = it % g.NA;
-      if (!(ok = mbar_wait(a_full + a, (it / g.NA) & 1, err))) break;
+      const int a = it % g.NA;
+      uint8_t* ostg = smem + o_off + (it % g.NST) * g.st_bytes;
+      if (!(ok = mbar_wait(br.a_full + a, (it / g.NA) & 1, err))) break;
       tc_fence_after();
-      if (warp == 10 && lane == 0)   // this tile's receive buffer has been read by the MMAs
-        for (int q = 0; q < C; ++q) mbar_arrive_remote(mapa_shared(dfree0 + 8u * r, (uint32_t)q));
-      const int t0 = tile * TT;
+      if (pending) {   // the store that last used this staging tile has finished reading it
+        if (et == 0) {
+          if (g.NST > 1) bulk_wait_read1();
+          else bulk_wait_read0();
+        }
+        epi_bar();
+      }
       for (int jj = 0; jj < G; ++jj)
         for (int h = 0; h < halves; ++h) {
-          const int i = h * 128 + quarter * 32 + lane;
-          __nv_bfloat16* o = out + (size_t)((c * G + jj) * B + i);
+          const int f = jj * B + h * 128 + quarter * 32 + lane;   // column within the CTA's blocks
+          uint8_t* col = ostg + (f >> 6) * (TT * 128) + (f & 7) * 2;
+          const uint32_t fu = (uint32_t)((f & 63) >> 3);
           const uint32_t tacc = acc0 + (uint32_t)(((a * G + jj) * halves + h) * TT) +
                                 ((uint32_t)(quarter * 32) << 16);
-#pragma unroll 1
+#pragma unroll
           for (int cc = 0; cc < TT; cc += 32) {
             uint32_t rr[32];
             tmem_ld32(tacc + (uint32_t)cc, rr);
             tmem_ld_wait();
 #pragma unroll
-            for (int t = 0; t < 32; ++t)
-              if (t0 + cc + t < T) o[(size_t)(t0 + cc + t) * d] = __float2bfloat16_rn(__uint_as_float(rr[t]));
+            for (int t = 0; t < 32; ++t) {
+              const int tr = cc + t;
+              *reinterpret_cast<__nv_bfloat16*>(col + tr * 128 + ((fu ^ (uint32_t)(tr & 7)) << 4)) =
+                  __float2bfloat16_rn(__uint_as_float(rr[t]));
+            }
           }
         }
       tc_fence_before();
-      mbar_arrive(a_empty + a);
+      mbar_arrive(br.a_empty + a);   // the accumulators may be refilled
+      fence_proxy_async_smem();
+      epi_bar();
+      if (et == 0) {
+        for (int q = 0; q < G * B / 64; ++q)
+          tma_store_2d(&tmOut, ostg + q * (TT * 128), c * G * B + q * 64, tile * TT);
+        bulk_commit();
+      }
+      pending = true;
     }
+    if (et == 0 && pending) bulk_wait0();
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();   // no CTA leaves while another may still reach its shared memory
+  cluster_sync();   // no CTA leaves while another may still arrive on its barriers
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, (uint32_t)g.tmem_cols);
@@ -288,8 +418,8 @@ __global__ void __launch_bounds__(kCaThreads, 1)
 template <int B>
 __global__ void __launch_bounds__(kCaThreads, 1)
     ca_scatter_kernel(const __grid_constant__ CUtensorMap tmIn, const __grid_constant__ CUtensorMap tmOut,
-                      const __nv_bfloat16* __restrict__ Q, const int32_t* __restrict__ perm, int T,
-                      int d, CaGeo g, int transpose_q, int* err) {
+                      const __grid_constant__ CUtensorMap tmQ, const int32_t* __restrict__ perm,
+                      uint8_t* __restrict__ xchg, int T, CaGeo g, int transpose_q, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -298,14 +428,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
   const int s_off = g.hdr;
   const int r_off = s_off + g.NS * g.s_bytes;
   const int st_off = r_off + g.NR * g.r_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* s_full = bars;          // [2] input tile landed
-  uint64_t* s_empty = bars + 2;     // [2] input tile read by the MMAs
-  uint64_t* r_full = bars + 4;      // [2] receive buffer complete (st.async bytes)
-  uint64_t* dst_free = bars + 6;    // [2] every owner released its receive buffer
-  uint64_t* a_full = bars + 8;      // [2]
-  uint64_t* a_empty = bars + 10;    // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  const Bars br = bars_at(smem);
   uint32_t* table = reinterpret_cast<uint32_t*>(smem + 256);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -313,22 +436,12 @@ __global__ void __launch_bounds__(kCaThreads, 1)
   const int cluster_id = blockIdx.x / C;
   const int n_clusters = gridDim.x / C;
   const int n_tiles = (T + TT - 1) / TT;
-  const int r_bytes = g.r_bytes;
+  const size_t slot_stride = (size_t)C * g.r_bytes;
+  uint8_t* ring = xchg + (size_t)cluster_id * g.NX * slot_stride;
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(s_full + i, 1);
-      mbar_init(s_empty + i, 1);
-      mbar_init(r_full + i, 1);
-      mbar_init(dst_free + i, C);
-      mbar_init(a_full + i, 1);
-      mbar_init(a_empty + i, 128);
-    }
-    fence_mbar_init();
-    for (int i = 0; i < g.NR; ++i) mbar_arrive_expect_tx(r_full + i, (uint32_t)r_bytes);
-  }
-  if (warp == 1) tmem_alloc(tmem_slot, (uint32_t)g.tmem_cols);
-  // owner of each output feature of the own blocks: (CTA << 24) | byte offset of its row
+  if (threadIdx.x == 0) init_bars(br, C, 1);
+  if (warp == 1) tmem_alloc(br.tmem_slot, (uint32_t)g.tmem_cols);
+  // each output feature of the own blocks: (owner CTA << 24) | byte offset of its row there
   for (int e = threadIdx.x; e < G * B; e += blockDim.x) {
     const int nc = __ldg(perm + c * G * B + e);
     table[e] = ((uint32_t)(nc / F) << 24) | (uint32_t)((nc % F) * 128);
@@ -336,34 +449,61 @@ __global__ void __launch_bounds__(kCaThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  load_q_to_tmem<B>(Q, c * G, G, transpose_q, smem + g.hdr, tmem_base);
-  cluster_sync();
+  const uint32_t tmem_base = *br.tmem_slot;
+  // Q through the (still idle) pipeline buffers into tensor memory
+  if (threadIdx.x == 0) issue_q_loads(&tmQ, smem + s_off, c * G, G, B, br.q_full);
+  bool ok = true;
+  if (warp >= 10 && warp < 14) {
+    if ((ok = mbar_wait(br.q_full, 0, err)))
+      q_stage_to_tmem<B>(smem + s_off, G, transpose_q, tmem_base, warp % 4, lane);
+  }
+  tc_fence_before();
+  __syncthreads();
+  // the first input tiles (the Q stage they overwrite has been read)
+  int prefetched = 0;
+  if (threadIdx.x == 0) {
+    fence_proxy_async_smem();
+    for (int tile = cluster_id; tile < n_tiles && prefetched < g.NS; tile += n_clusters, ++prefetched) {
+      mbar_arrive_expect_tx(br.s_full + prefetched, (uint32_t)g.s_bytes);
+      uint8_t* dst = smem + s_off + prefetched * g.s_bytes;
+      for (int jj = 0; jj < G; ++jj)
+        for (int q = 0; q < B / 64; ++q)
+          tma_load_2d(dst + jj * (TT * B * 2) + q * (TT * 128), &tmIn, (c * G + jj) * B + q * 64,
+                      tile * TT, br.s_full + prefetched);
+    }
+  }
+  cluster_sync();   // every CTA's barriers are initialised before any remote access
+  tc_fence_after();
 
   const uint32_t acc0 = tmem_base + (uint32_t)g.q_cols;
-  bool ok = true;
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA: own blocks' columns
     if (lane == 0) {
       for (int it = 0, tile = cluster_id; tile < n_tiles && ok; tile += n_clusters, ++it) {
+        if (it < prefetched) continue;
         const int s = it % g.NS;
-        if (!(ok = mbar_wait(s_empty + s, ((it / g.NS) & 1) ^ 1, err))) break;
-        mbar_arrive_expect_tx(s_full + s, (uint32_t)g.s_bytes);
+        if (!(ok = mbar_wait(br.s_empty + s, ((it / g.NS) & 1) ^ 1, err))) break;
+        mbar_arrive_expect_tx(br.s_full + s, (uint32_t)g.s_bytes);
         uint8_t* dst = smem + s_off + s * g.s_bytes;
         for (int jj = 0; jj < G; ++jj)
           for (int q = 0; q < B / 64; ++q)
             tma_load_2d(dst + jj * (TT * B * 2) + q * (TT * 128), &tmIn, (c * G + jj) * B + q * 64,
-                        tile * TT, s_full + s);
+                        tile * TT, br.s_full + s);
       }
     }
+  } else if (warp == 14) {
+    // ---------------------------------------------------------------- loader
+    if (lane == 0)
+      loader_loop(br, g, smem + r_off, ring + (size_t)c * g.r_bytes, slot_stride, cluster_id,
+                  n_clusters, n_tiles, ok, err);
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(128, TT, false, false);
       for (int it = 0, tile = cluster_id; tile < n_tiles && ok; tile += n_clusters, ++it) {
         const int s = it % g.NS, a = it % g.NA;
-        if (!(ok = mbar_wait(s_full + s, (it / g.NS) & 1, err))) break;
-        if (!(ok = mbar_wait(a_empty + a, ((it / g.NA) & 1) ^ 1, err))) break;
+        if (!(ok = mbar_wait(br.s_full + s, (it / g.NS) & 1, err))) break;
+        if (!(ok = mbar_wait(br.a_empty + a, ((it / g.NA) & 1) ^ 1, err))) break;
         tc_fence_after();
         const uint32_t sb = smem_u32(smem + s_off + s * g.s_bytes);
         for (int jj = 0; jj < G; ++jj)
@@ -377,32 +517,33 @@ __global__ void __launch_bounds__(kCaThreads, 1)
               mma_bf16_ts(d_tmem, a_tmem + (uint32_t)(kk * 8), bdesc, idesc, kk != 0);
             }
           }
-        mma_commit(s_empty + s);
-        mma_commit(a_full + a);
+        mma_commit(br.s_empty + s);
+        mma_commit(br.a_full + a);
       }
     }
   } else if (warp >= 10) {
-    // ---------------------------------------------------------------- epilogue: send output features
+    // ---------------------------------------------------------------- epilogue: write output feature rows
+    // A thread owns one output feature (its TMEM lane): its 64 tokens become a
+    // 128-byte row (8 x 16 bytes in the row's swizzle order), written into the
+    // exchange part of the CTA owning the feature's scattered column.
     const int quarter = warp % 4;
-    const uint32_t rbase = smem_u32(smem + r_off);
-    const uint32_t rfull0 = smem_u32(r_full);
+    const int et = threadIdx.x - 320;
     for (int it = 0, tile = cluster_id; tile < n_tiles && ok; tile += n_clusters, ++it) {
-      const int r = it % g.NR, a = it % g.NA;
-      if (!(ok = mbar_wait(a_full + a, (it / g.NA) & 1, err))) break;
-      if (!(ok = mbar_wait_cluster(dst_free + r, ((it / g.NR) & 1) ^ 1, err))) break;
+      const int x = it % g.NX, a = it % g.NA;
+      if (!(ok = mbar_wait(br.a_full + a, (it / g.NA) & 1, err))) break;
+      if (!(ok = mbar_wait_cluster(br.x_free + x, ((it / g.NX) & 1) ^ 1, err))) break;
       tc_fence_after();
+      uint8_t* slot = ring + (size_t)x * slot_stride;
       for (int jj = 0; jj < G; ++jj)
         for (int h = 0; h < halves; ++h) {
           const int i = h * 128 + quarter * 32 + lane;
           const uint32_t ent = table[jj * B + i];
-          const uint32_t owner = ent >> 24, roff = ent & 0xFFFFFFu;
+          const uint32_t roff = ent & 0xFFFFFFu;
           const uint32_t f7 = (roff >> 7) & 7u;
-          const uint32_t laddr = rbase + (uint32_t)(r * r_bytes) + roff;
-          const uint32_t raddr = mapa_shared(laddr, owner);
-          const uint32_t rbar = mapa_shared(rfull0 + 8u * r, owner);
+          uint8_t* row = slot + (size_t)(ent >> 24) * g.r_bytes + roff;
           const uint32_t tacc = acc0 + (uint32_t)(((a * G + jj) * halves + h) * TT) +
                                 ((uint32_t)(quarter * 32) << 16);
-#pragma unroll 1
+#pragma unroll
           for (int cc = 0; cc < TT; cc += 32) {
             uint32_t rr[32];
             tmem_ld32(tacc + (uint32_t)cc, rr);
@@ -415,28 +556,31 @@ __global__ void __launch_bounds__(kCaThreads, 1)
                   pack_bf16x2(__uint_as_float(rr[8 * u + 2]), __uint_as_float(rr[8 * u + 3])),
                   pack_bf16x2(__uint_as_float(rr[8 * u + 4]), __uint_as_float(rr[8 * u + 5])),
                   pack_bf16x2(__uint_as_float(rr[8 * u + 6]), __uint_as_float(rr[8 * u + 7])));
-              st_async_v4(raddr + ((grp ^ f7) << 4), v, rbar);
+              *reinterpret_cast<uint4*>(row + ((grp ^ f7) << 4)) = v;
             }
           }
         }
       tc_fence_before();
-      mbar_arrive(a_empty + a);
+      mbar_arrive(br.a_empty + a);
+      epi_bar();
+      // the epilogue's rows are visible before the hand-off (release, after the barrier)
+      arrive_one(br.x_full + x, et, C, true);
     }
   } else {
-    // ---------------------------------------------------------------- movers: received features -> token rows
+    // ---------------------------------------------------------------- movers: fetched features -> token rows
     const int pt = threadIdx.x - 64;
-    const uint32_t dfree0 = smem_u32(dst_free);
-    uint8_t* ST = smem + st_off;
     bool pending = false;
     for (int it = 0, tile = cluster_id; tile < n_tiles && ok; tile += n_clusters, ++it) {
       const int r = it % g.NR;
-      if (!(ok = mbar_wait_cluster(r_full + r, (it / g.NR) & 1, err))) break;
-      if (pt == 0) {
-        mbar_arrive_expect_tx(r_full + r, (uint32_t)r_bytes);   // the buffer's next use
-        if (pending) bulk_wait_read0();                        // the staging tile is free again
+      uint8_t* ST = smem + st_off + (it % g.NST) * g.st_bytes;
+      if (!(ok = mbar_wait(br.r_full + r, (it / g.NR) & 1, err))) break;
+      arrive_one(br.x_free + it % g.NX, pt, C, false);   // this CTA's part has been fetched
+      if (pt == 0 && pending) {   // the store that last used this staging tile has read it
+        if (g.NST > 1) bulk_wait_read1();
+        else bulk_wait_read0();
       }
       movers_bar();
-      const uint8_t* R = smem + r_off + r * r_bytes;
+      const uint8_t* R = smem + r_off + r * g.r_bytes;
       for (int w = pt; w < TT * (F / 8); w += kMovers) {
         const int t = w % TT, f8 = (w / TT) * 8;
         float v[8];
@@ -453,7 +597,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
       fence_proxy_async_smem();
       movers_bar();
       if (pt == 0) {
-        for (int q = 0; q < C; ++q) mbar_arrive_remote(mapa_shared(dfree0 + 8u * r, (uint32_t)q));
+        mbar_arrive(br.r_empty + r);            // the fetched part has been read
         for (int q = 0; q < F / 64; ++q) tma_store_2d(&tmOut, ST + q * (TT * 128), c * F + q * 64, tile * TT);
         bulk_commit();
         pending = true;
@@ -463,7 +607,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();
+  cluster_sync();   // no CTA leaves while another may still arrive on its barriers
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, (uint32_t)g.tmem_cols);
@@ -502,33 +646,49 @@ bool ca_geometry(int d, int b, bool gather, CaGeo* out) {
     g.tmem_cols = tmem_alloc_cols(g.q_cols + g.a_cols);
     if (gather) {
       g.s_bytes = TT * g.F * 2;            // own columns of the tile
-      g.r_bytes = g.G * b * TT * 2;        // received operand of the own blocks
-      g.st_bytes = 0;
+      g.r_bytes = g.G * b * TT * 2;        // fetched operand of the own blocks
+      g.st_bytes = g.G * b * TT * 2;       // output tile of the own blocks, token rows
     } else {
       g.s_bytes = g.G * TT * b * 2;        // own blocks' input columns
-      g.r_bytes = g.F * TT * 2;            // received output features
+      g.r_bytes = g.F * TT * 2;            // fetched output features
       g.st_bytes = TT * g.F * 2;           // token-row staging for the TMA store
     }
     const int table = 4 * (gather ? g.F : g.G * b);
     g.hdr = (256 + table + 1023) / 1024 * 1024;
-    const int qstage = g.G * b * (b + 8) * 2;
+    const int qstage = g.G * b * b * 2;   // staged in the pipeline buffers before first use
+    // deeper input rings first (they hide the HBM latency), then double
+    // output staging (the TMA store of one tile overlaps the next)
+    const int cand[8][3] = {{4, 2, 2}, {3, 2, 2}, {4, 1, 2}, {3, 1, 2},
+                            {2, 2, 2}, {2, 1, 2}, {2, 1, 1}, {1, 1, 1}};
     bool found = false;
-    for (int NS = 2; NS >= 1 && !found; --NS)
-      for (int NR = 2; NR >= 1 && !found; --NR) {
-        const int body = NS * g.s_bytes + NR * g.r_bytes + g.st_bytes;
-        const int smem = 1024 + g.hdr + (body > qstage ? body : qstage);
-        if (smem <= kSmemLimit) {
-          g.NS = NS;
-          g.NR = NR;
-          g.smem = smem;
-          found = true;
-        }
+    for (int ci = 0; ci < 8 && !found; ++ci) {
+      const int NS = cand[ci][0], NST = cand[ci][1], NR = cand[ci][2];
+      const int body = NS * g.s_bytes + NR * g.r_bytes + NST * g.st_bytes;
+      const int smem = 1024 + g.hdr + body;
+      if (smem <= kSmemLimit && qstage <= body) {
+        g.NS = NS;
+        g.NR = NR;
+        g.NST = NST;
+        g.smem = smem;
+        found = true;
       }
+    }
     if (!found) continue;
+    g.NX = kMaxSlots;
     *out = g;
     return true;
   }
   return false;
+}
+
+int device_sms() {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    cudaGetLastError();
+    sms = 148;
+  }
+  return sms;
 }
 
 }  // namespace
@@ -538,18 +698,30 @@ bool cluster_apply_supported(int d, int b, bool scatter) {
   return ca_geometry(d, b, !scatter, &g);
 }
 
+// Exchange ring: at most one cluster per C SMs, NX slots of C parts each.
+size_t cluster_apply_workspace_bytes(int d, int b, bool scatter) {
+  CaGeo g;
+  if (!ca_geometry(d, b, !scatter, &g)) return 0;
+  const int clusters = device_sms() / g.C;
+  return (size_t)clusters * g.NX * g.C * g.r_bytes;
+}
+
 poetx_status cluster_apply_bf16(const void* in, void* out, const void* Q, const int32_t* perm,
                                 const int32_t* inv, int T, int d, int b, bool transpose_q,
-                                bool scatter, cudaStream_t s) {
+                                bool scatter, void* ws, size_t ws_bytes, cudaStream_t s) {
   if (T <= 0) return POETX_OK;
   CaGeo g;
   if (!ca_geometry(d, b, !scatter, &g)) return POETX_ERR_UNSUPPORTED;
-  CUtensorMap tin, tout;
+  if (!ws || ws_bytes < cluster_apply_workspace_bytes(d, b, scatter) ||
+      (reinterpret_cast<uintptr_t>(ws) & 255))
+    return POETX_ERR_SHAPE;
+  CUtensorMap tin, tout, tq;
   if (!make_tmap_2d(&tin, in, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)T, (uint64_t)d, TT, 64,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&tout, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)T, (uint64_t)d, TT,
+                    64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&tq, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d, (uint64_t)b, 64, 64,
                     CU_TENSOR_MAP_SWIZZLE_128B))
-    return POETX_ERR_CUDA;
-  if (scatter && !make_tmap_2d(&tout, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)T,
-                               (uint64_t)d, TT, 64, CU_TENSOR_MAP_SWIZZLE_128B))
     return POETX_ERR_CUDA;
   const void* kern;
   if (scatter)
@@ -572,10 +744,9 @@ poetx_status cluster_apply_bf16(const void* in, void* out, const void* Q, const 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // as many clusters as can be resident at once (persistent), but no more than tiles
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // as many clusters as can be resident at once (persistent), but no more than
+  // tiles, nor than the exchange ring was sized for
+  const int sms = device_sms();
   cfg.gridDim = dim3((sms / g.C) * g.C);
   int active = 0;
   if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess || active < 1) {
@@ -583,25 +754,25 @@ poetx_status cluster_apply_bf16(const void* in, void* out, const void* Q, const 
     return POETX_ERR_UNSUPPORTED;
   }
   const int n_tiles = (T + TT - 1) / TT;
-  const int clusters = active < n_tiles ? active : n_tiles;
+  int clusters = active < n_tiles ? active : n_tiles;
+  if (clusters > sms / g.C) clusters = sms / g.C;
   cfg.gridDim = dim3(clusters * g.C);
   int* err = device_error_word();
-  const int tq = transpose_q ? 1 : 0;
-  const __nv_bfloat16* qp = static_cast<const __nv_bfloat16*>(Q);
+  const int tqf = transpose_q ? 1 : 0;
+  uint8_t* xchg = static_cast<uint8_t*>(ws);
   {
     KernelScope ks_(scatter ? "tc_cluster_scatter" : "tc_cluster_gather", s);
     cudaError_t e;
     if (scatter) {
       if (b == 256)
-        e = cudaLaunchKernelEx(&cfg, ca_scatter_kernel<256>, tin, tout, qp, perm, T, d, g, tq, err);
+        e = cudaLaunchKernelEx(&cfg, ca_scatter_kernel<256>, tin, tout, tq, perm, xchg, T, g, tqf, err);
       else
-        e = cudaLaunchKernelEx(&cfg, ca_scatter_kernel<128>, tin, tout, qp, perm, T, d, g, tq, err);
+        e = cudaLaunchKernelEx(&cfg, ca_scatter_kernel<128>, tin, tout, tq, perm, xchg, T, g, tqf, err);
     } else {
-      __nv_bfloat16* op = static_cast<__nv_bfloat16*>(out);
       if (b == 256)
-        e = cudaLaunchKernelEx(&cfg, ca_gather_kernel<256>, tin, qp, inv, op, T, d, g, tq, err);
+        e = cudaLaunchKernelEx(&cfg, ca_gather_kernel<256>, tin, tout, tq, inv, xchg, T, g, tqf, err);
       else
-        e = cudaLaunchKernelEx(&cfg, ca_gather_kernel<128>, tin, qp, inv, op, T, d, g, tq, err);
+        e = cudaLaunchKernelEx(&cfg, ca_gather_kernel<128>, tin, tout, tq, inv, xchg, T, g, tqf, err);
     }
     if (e != cudaSuccess) return check_launch();
   }

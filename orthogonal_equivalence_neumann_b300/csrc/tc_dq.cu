@@ -31,6 +31,7 @@ constexpr int kThreads = 192;        // warp 0: TMA; warp 1: MMA; warps 2..5: ep
 constexpr int KT = 64;               // tokens per pipeline stage
 constexpr int kSmemMax = 232448;
 constexpr int kMaxStages = 8;
+constexpr int kMaxSplit = 9;
 
 __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
@@ -164,7 +165,11 @@ poetx_status dq_bf16(const void* G, const void* V, int T, int d, int b, float* d
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int nb = d / b;
   const int n_chunks = (T + KT - 1) / KT;
+  // Token splits per block: enough CTAs to keep HBM busy, few enough that the
+  // fp32 partial sums (b x b per CTA, reduced into dQ with vector atomics at
+  // the end) stay a small fraction of the traffic.
   int n_split = sms / nb;
+  if (n_split > kMaxSplit) n_split = kMaxSplit;
   if (n_split < 1) n_split = 1;
   if (n_split > n_chunks) n_split = n_chunks;
   const int tile_bytes = KT * b * 2;

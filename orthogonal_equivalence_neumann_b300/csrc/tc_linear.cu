@@ -34,27 +34,45 @@ bool tc_linear_supported(int d_in, int d_out, int b_in, int b_out, poetx_dtype d
   return dt == POETX_BF16 && tc::gemm_supported(d_out, d_in) && tc::gemm_supported(d_in, d_out);
 }
 
-// The backward's tensor-core scratch: one gathered activation [T, max(d_in, d_out)]
-// (dy by perm_out, then x by perm_in) for the dQ token sums, and the dense
-// bf16 K and G of every block (CNP backward).
+// Tensor-core scratch.  Forward: the exchange ring of the cluster block
+// applies.  Backward: one region that serves, in turn, the exchange ring of
+// the block applies and the gathered activation [T, max(d_in, d_out)] of the
+// dQ token sums (dy by perm_out, then x by perm_in); after it, the dense bf16
+// K and G of every block (CNP backward).
 static bool dq_tc(int d, int b) { return tc::dq_supported(d, b) && tc::permute_supported(d); }
+
+static size_t ring_bytes(int d, int b, bool scatter) {
+  return tc::cluster_apply_supported(d, b, scatter) ? tc::cluster_apply_workspace_bytes(d, b, scatter)
+                                                    : 0;
+}
+
+static size_t shared_region_bytes(int T, int d_in, int d_out, int b_in, int b_out, bool backward) {
+  // the backward may also run the forward applies (z recomputed without a saved copy)
+  size_t bytes = 0;
+  const size_t rings[4] = {ring_bytes(d_in, b_in, false), ring_bytes(d_out, b_out, true),
+                           backward ? ring_bytes(d_out, b_out, false) : 0,
+                           backward ? ring_bytes(d_in, b_in, true) : 0};
+  for (size_t r : rings)
+    if (r > bytes) bytes = r;
+  if (backward && (dq_tc(d_in, b_in) || dq_tc(d_out, b_out))) {
+    const size_t g = (size_t)T * (d_in > d_out ? d_in : d_out) * 2;
+    if (g > bytes) bytes = g;
+  }
+  return round_up(bytes, 256);
+}
 
 size_t tc_workspace_bytes(int T, int d_in, int d_out, int b_in, int b_out, poetx_dtype dt,
                           bool backward) {
-  if (!backward || dt != POETX_BF16) return 0;
-  size_t bytes = 0;
-  if (dq_tc(d_in, b_in) || dq_tc(d_out, b_out))
-    bytes += round_up((size_t)T * (d_in > d_out ? d_in : d_out) * 2, 256);
-  if (tc::cnp_supported(b_in) && tc::cnp_supported(b_out))
+  if (dt != POETX_BF16) return 0;
+  size_t bytes = shared_region_bytes(T, d_in, d_out, b_in, b_out, backward);
+  if (backward && tc::cnp_supported(b_in) && tc::cnp_supported(b_out))
     bytes += tc::cnp_bwd_workspace_bytes(d_in, b_in, d_out, b_out);
   return bytes;
 }
 
 // Offset of the CNP backward's part of the tensor-core scratch.
 size_t tc_cnp_ws_offset(int T, int d_in, int d_out, int b_in, int b_out) {
-  if (dq_tc(d_in, b_in) || dq_tc(d_out, b_out))
-    return round_up((size_t)T * (d_in > d_out ? d_in : d_out) * 2, 256);
-  return 0;
+  return shared_region_bytes(T, d_in, d_out, b_in, b_out, true);
 }
 
 // Permuted block apply: a thread-block cluster when the shape allows, else one
@@ -62,11 +80,11 @@ size_t tc_cnp_ws_offset(int T, int d_in, int d_out, int b_in, int b_out) {
 // inverse of the gather permutation.
 static poetx_status block_apply(const void* in, void* out, const void* Q, int T, int d, int b,
                                 const int32_t* gath, const int32_t* inv, const int32_t* scat,
-                                bool transpose_q, cudaStream_t s) {
+                                bool transpose_q, void* ws, cudaStream_t s) {
   const bool scatter = scat != nullptr;
   if (tc::cluster_apply_supported(d, b, scatter))
     return tc::cluster_apply_bf16(in, out, Q, scatter ? scat : gath, inv, T, d, b, transpose_q,
-                                  scatter, s);
+                                  scatter, ws, tc::cluster_apply_workspace_bytes(d, b, scatter), s);
   if (tc::blockapply_supported(d, b))
     return tc::blockapply_bf16(in, out, Q, gath ? gath : scat, T, d, b, transpose_q, scatter, s);
   return launch_block_apply_simt(in, out, Q, T, d, b, gath, scat, transpose_q, POETX_BF16, s);
@@ -90,10 +108,9 @@ poetx_status tc_forward(const void* x, const void* W0m, const void* Q_P, const v
                         const int32_t* perm_in, const int32_t* inv_in, const int32_t* perm_out,
                         const int32_t* inv_out, int T, int d_in, int d_out, int b_in, int b_out,
                         void* u, void* z, void* y, void* ws, cudaStream_t s) {
-  (void)ws;
-  TC_TRY(block_apply(x, u, Q_P, T, d_in, b_in, perm_in, inv_in, nullptr, false, s));
+  TC_TRY(block_apply(x, u, Q_P, T, d_in, b_in, perm_in, inv_in, nullptr, false, ws, s));
   TC_TRY(tc::gemm_bf16(u, W0m, z, T, d_out, d_in, false, s));
-  if (y) TC_TRY(block_apply(z, y, Q_R, T, d_out, b_out, nullptr, nullptr, perm_out, false, s));
+  if (y) TC_TRY(block_apply(z, y, Q_R, T, d_out, b_out, nullptr, nullptr, perm_out, false, ws, s));
   return POETX_OK;
 }
 
@@ -102,10 +119,10 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
                          const int32_t* inv_in, const int32_t* perm_out, const int32_t* inv_out,
                          int T, int d_in, int d_out, int b_in, int b_out, void* dX, void* gz,
                          void* gu, float* dqp, float* dqr, void* ws, cudaStream_t s) {
-  TC_TRY(block_apply(dy, gz, Q_R, T, d_out, b_out, perm_out, inv_out, nullptr, true, s));
+  TC_TRY(block_apply(dy, gz, Q_R, T, d_out, b_out, perm_out, inv_out, nullptr, true, ws, s));
   TC_TRY(dq(dy, z, T, d_out, b_out, perm_out, nullptr, dqr, ws, s));
   TC_TRY(tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s));
-  TC_TRY(block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, nullptr, perm_in, true, s));
+  TC_TRY(block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, nullptr, perm_in, true, ws, s));
   TC_TRY(dq(gu, x, T, d_in, b_in, nullptr, perm_in, dqp, ws, s));
   return POETX_OK;
 }

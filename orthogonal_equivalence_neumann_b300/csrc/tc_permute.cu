@@ -65,27 +65,45 @@ __global__ void __launch_bounds__(kPermThreads, 1)
       }
     }
   } else {
+    // a worker owns output column groups (8 columns); their 8 source columns
+    // are fixed, so their slab offsets are computed once and reused for every
+    // token of every slab
     const int wt = threadIdx.x - 32;
-    const int units_per_row = d / 8;
+    const int groups = d / 8;
+    constexpr int kMaxGroups = 4;   // d <= 8 * 256 * kMaxGroups
+    uint32_t base[kMaxGroups][8], unit[kMaxGroups][8];
+#pragma unroll
+    for (int gi = 0; gi < kMaxGroups; ++gi) {
+      const int c8 = (wt + gi * kPermWorkers) * 8;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int a = c8 < d ? __ldg(perm + c8 + e) : 0;
+        base[gi][e] = (uint32_t)((a >> 6) * TM * 128 + (a & 7) * 2);
+        unit[gi][e] = (uint32_t)((a >> 3) & 7);
+      }
+    }
     for (int it = 0, s = blockIdx.x; s < n_slabs; s += gridDim.x, ++it) {
       const int buf = it & 1;
       if (!mbar_wait(full + buf, (it >> 1) & 1, err)) break;
       const uint8_t* slab = smem + buf * slab_bytes;
       const int t0 = s * TM;
       const int rows = min(TM, T - t0);
-      for (int u = wt; u < rows * units_per_row; u += kPermWorkers) {
-        const int t = u / units_per_row, c8 = (u % units_per_row) * 8;
-        uint32_t w[4];
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          const int a = __ldg(perm + c8 + e), b = __ldg(perm + c8 + e + 1);
-          const uint16_t va = *reinterpret_cast<const uint16_t*>(
-              slab + (a >> 6) * TM * 128 + t * 128 + ((((a >> 3) & 7) ^ (t & 7)) << 4) + (a & 7) * 2);
-          const uint16_t vb = *reinterpret_cast<const uint16_t*>(
-              slab + (b >> 6) * TM * 128 + t * 128 + ((((b >> 3) & 7) ^ (t & 7)) << 4) + (b & 7) * 2);
-          w[e / 2] = (uint32_t)va | ((uint32_t)vb << 16);
+      for (int gi = 0; gi < kMaxGroups; ++gi) {
+        const int g = wt + gi * kPermWorkers;
+        if (g >= groups) break;
+        for (int t = 0; t < rows; ++t) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const uint16_t va = *reinterpret_cast<const uint16_t*>(
+                slab + base[gi][e] + t * 128 + ((unit[gi][e] ^ (uint32_t)(t & 7)) << 4));
+            const uint16_t vb = *reinterpret_cast<const uint16_t*>(
+                slab + base[gi][e + 1] + t * 128 + ((unit[gi][e + 1] ^ (uint32_t)(t & 7)) << 4));
+            w[e / 2] = (uint32_t)va | ((uint32_t)vb << 16);
+          }
+          *reinterpret_cast<uint4*>(out + (size_t)(t0 + t) * d + g * 8) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        *reinterpret_cast<uint4*>(out + (size_t)(t0 + t) * d + c8) = make_uint4(w[0], w[1], w[2], w[3]);
       }
       mbar_arrive(empty + buf);
     }
@@ -94,7 +112,9 @@ __global__ void __launch_bounds__(kPermThreads, 1)
 
 }  // namespace
 
-bool permute_supported(int d) { return d % 64 == 0 && permute_rows(d) > 0; }
+bool permute_supported(int d) {
+  return d % 64 == 0 && d <= 8 * kPermWorkers * 4 && permute_rows(d) > 0;
+}
 
 poetx_status permute_cols_bf16(const void* in, void* out, const int32_t* perm, int T, int d,
                                cudaStream_t s) {

@@ -109,6 +109,12 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
                : "memory");
 }
 
+// Remote arrive without memory ordering (a pure signal).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+               : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -127,6 +133,40 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     if (mbar_try_wait_cluster(bar, parity)) return true;
   raise_device_error(err, POETX_ERR_TIMEOUT);
   return false;
+}
+
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory into
+// the shared memory of a CTA of the cluster (both addresses 16-byte aligned);
+// the bytes count against that CTA's mbarrier `remote_bar` (complete_tx).
+__device__ __forceinline__ void bulk_copy_s2s(uint32_t remote_dst, uint32_t local_src, uint32_t bytes,
+                                              uint32_t remote_bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(remote_dst),
+      "r"(local_src), "r"(bytes), "r"(remote_bar)
+      : "memory");
+}
+
+// Orders this thread's prior memory accesses (and, cumulatively, those it has
+// observed, e.g. through a CTA barrier) before its later ones, cluster-wide.
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+
+// Makes global-memory data observed through the generic proxy visible to this
+// thread's subsequent async-proxy (TMA / bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Bulk copy global -> this CTA's shared memory (both 16-byte aligned, size a
+// multiple of 16), counted against the local mbarrier `bar` (complete_tx).
+__device__ __forceinline__ void bulk_load_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // 16-byte asynchronous store into the shared memory of a CTA of the cluster;
@@ -160,6 +200,9 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
