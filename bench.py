@@ -66,27 +66,27 @@ def kernel_work(case):
     cnp_fb = 4 * (nbi * bi * (bi - 1) / 2 + nbo * bo * (bo - 1) / 2) / 2 + es * (nbi * bi * bi + nbo * bo * bo) / 2
     cnpb_f = 3 * cnp_f
     cnpb_b = 4 * (nbi * bi * bi + nbo * bo * bo) / 2 + 8 * (nbi * bi * (bi - 1) / 2 + nbo * bo * (bo - 1) / 2) / 2
-    cnp_prep_b = 4 * (nbi * bi * (bi - 1) / 2 + nbo * bo * (bo - 1) / 2) + 4 * (nbi * bi * bi + nbo * bo * bo) \
-        + 2 * 2 * (nbi * bi * bi + nbo * bo * bo)
+    nbb = nbi * bi * bi + nbo * bo * bo                 # entries of all blocks of both sides
+    npk = nbi * bi * (bi - 1) / 2 + nbo * bo * (bo - 1) / 2  # packed parameters of both sides
     return {
         "gemm_simt": ("alu", gemm_flops, gemm_bytes),
         "block_apply_simt": ("alu", blk_flops, blk_bytes),
         "dq_simt": ("alu", dq_flops, dq_bytes),
         "cnp_fwd_simt": ("alu", cnp_f, cnp_fb),
         "cnp_bwd_simt": ("alu", cnpb_f, cnpb_b),
-        # tensor-core path (one launch per product; the CNP backward serves both sides)
+        # tensor-core path (one launch per product; the CNP kernels serve both sides)
         "tc_gemm_nt": ("tensor", gemm_flops, gemm_bytes),
         "tc_gemm_nn": ("tensor", gemm_flops, gemm_bytes),
         "tc_blockapply_gather": ("hbm", blk_flops, blk_bytes),
         "tc_blockapply_scatter": ("hbm", blk_flops, blk_bytes),
-        "tc_dq_gather_rows": ("hbm", dq_flops, dq_bytes),
-        "tc_dq_gather_cols": ("hbm", dq_flops, dq_bytes),
+        "tc_cluster_gather": ("hbm", blk_flops, blk_bytes),
+        "tc_cluster_scatter": ("hbm", blk_flops, blk_bytes),
         "tc_dq": ("hbm", dq_flops, dq_bytes),
         "tc_permute_cols": ("hbm", 0.0, es * (T * di + T * do)),
-        "tc_cnp_fwd": ("tensor", cnp_f, cnp_fb),
-        "tc_cnp_bwd_prep": ("hbm", 0.0, cnp_prep_b),
-        "tc_cnp_bwd": ("tensor", 2 * cnpb_f, 2 * 2 * 2 * (nbi * bi * bi + nbo * bo * bo) / 2
-                       + 4 * (nbi * bi * (bi - 1) / 2 + nbo * bo * (bo - 1) / 2)),
+        "tc_cnp_unpack": ("hbm", 0.0, 4 * npk + 2 * nbb),
+        "tc_cnp_fwd": ("tensor", 2 * cnp_f, 2 * nbb + 2 * nbb),
+        "tc_cnp_bwd_prep": ("hbm", 0.0, 4 * npk + 4 * nbb + 3 * 2 * nbb),
+        "tc_cnp_bwd": ("tensor", 2 * cnpb_f, 3 * 2 * nbb + 4 * nbb + 4 * npk),
     }
 
 

@@ -44,12 +44,29 @@ struct Workspace {
   // backward
   size_t gz = 0;       // g_z                                      [T, d_out] act
   size_t gu = 0;       // g_u (also u while z is recomputed)       [T, d_in]  act
-  size_t dqp = 0;      // dQ_P                                     [d_in * b_in]  f32
-  size_t dqr = 0;      // dQ_R                                     [d_out * b_out] f32
+  size_t dqp = 0;      // dQ_P partial sums                 [slots][d_in * b_in]  f32
+  size_t dqr = 0;      // dQ_R partial sums                 [slots][d_out * b_out] f32
   size_t z = 0;        // recomputed z when none was saved         [T, d_out] act
   size_t tc = 0;       // tensor-core path scratch
   size_t bwd_bytes = 0;
+  int slots_p = 1;     // dQ_P / dQ_R partial-sum slot counts
+  int slots_r = 1;
 };
+
+// Whether the backward runs the Cayley-Neumann blocks on the tensor cores.
+bool tc_cnp_backward(int d_in, int d_out, int b_in, int b_out, poetx_dtype dt) {
+  return dt == POETX_BF16 && tc::cnp_supported(b_in) && tc::cnp_supported(b_out) &&
+         d_in / b_in + d_out / b_out <= 65535;
+}
+
+// dQ partial-sum slots of one side: several only when the tensor-core dQ feeds
+// the tensor-core block backward (which adds them in slot order), else one.
+int dq_slots(int T, int d_in, int d_out, int b_in, int b_out, poetx_dtype dt, bool in_side) {
+  if (!tc_linear_supported(d_in, d_out, b_in, b_out, dt) ||
+      !tc_cnp_backward(d_in, d_out, b_in, b_out, dt))
+    return 1;
+  return in_side ? tc_dq_slots(T, d_in, b_in, dt) : tc_dq_slots(T, d_out, b_out, dt);
+}
 
 Workspace layout(int T, int d_in, int d_out, int b_in, int b_out, poetx_dtype dt) {
   Workspace w;
@@ -63,8 +80,10 @@ Workspace layout(int T, int d_in, int d_out, int b_in, int b_out, poetx_dtype dt
   off = 0;
   w.gz = off;  off += round_up((size_t)T * d_out * es, A);
   w.gu = off;  off += round_up((size_t)T * d_in * es, A);
-  w.dqp = off; off += round_up((size_t)d_in * b_in * 4, A);
-  w.dqr = off; off += round_up((size_t)d_out * b_out * 4, A);
+  w.slots_p = dq_slots(T, d_in, d_out, b_in, b_out, dt, true);
+  w.slots_r = dq_slots(T, d_in, d_out, b_in, b_out, dt, false);
+  w.dqp = off; off += round_up((size_t)w.slots_p * d_in * b_in * 4, A);
+  w.dqr = off; off += round_up((size_t)w.slots_r * d_out * b_out * 4, A);
   w.z = off;   off += round_up((size_t)T * d_out * es, A);
   w.tc = off;  off += round_up(tc_workspace_bytes(T, d_in, d_out, b_in, b_out, dt, true), A);
   w.bwd_bytes = off;
@@ -268,7 +287,8 @@ poetx_status poetx_backward(const void* x, const void* dy, const void* W0m, cons
   const poetx_dtype dt = act_dtype;
   if (tc_linear_supported(d_in, d_out, b_in, b_out, dt)) {
     POETX_TRY(tc_backward(x, dy, W0m, Q_P, Q_R, z, perm_in, inv_in, perm_out, inv_out, T, d_in,
-                          d_out, b_in, b_out, dX, gz, gu, dqp, dqr, tc_ws, stream));
+                          d_out, b_in, b_out, dX, gz, gu, dqp, w.slots_p, dqr, w.slots_r, tc_ws,
+                          stream));
   } else {
     // g_z = gather(dy, perm_out) . B_R
     POETX_TRY(launch_block_apply_simt(dy, gz, Q_R, T, d_out, b_out, perm_out, nullptr, true, dt, stream));
@@ -284,9 +304,9 @@ poetx_status poetx_backward(const void* x, const void* dy, const void* W0m, cons
   // [§2.D] backward of the Cayley-Neumann blocks: the bf16 layer runs both sides
   // in one tensor-core launch (bf16 operands), the fp32 layer the exact
   // CUDA-core kernel per side
-  if (dt == POETX_BF16 && tc::cnp_supported(b_in) && tc::cnp_supported(b_out) &&
-      nb_in + nb_out <= 65535) {
-    POETX_TRY(tc::cnp_bwd_layer(theta_P, dqp, nb_in, b_in, theta_R, dqr, nb_out, b_out, n,
+  if (tc_cnp_backward(d_in, d_out, b_in, b_out, dt)) {
+    POETX_TRY(tc::cnp_bwd_layer(theta_P, dqp, w.slots_p, nb_in, b_in, theta_R, dqr, w.slots_r,
+                                nb_out, b_out, n,
                                 dtheta_P, dtheta_R,
                                 static_cast<char*>(tc_ws) +
                                     tc_cnp_ws_offset(T, d_in, d_out, b_in, b_out),

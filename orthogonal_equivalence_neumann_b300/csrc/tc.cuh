@@ -15,6 +15,8 @@ bool tc_linear_supported(int d_in, int d_out, int b_in, int b_out, poetx_dtype d
 size_t tc_workspace_bytes(int T, int d_in, int d_out, int b_in, int b_out, poetx_dtype dt,
                           bool backward);
 size_t tc_cnp_ws_offset(int T, int d_in, int d_out, int b_in, int b_out);
+// Partial-sum slots the tensor-core dQ would use for a side (1 off that path).
+int tc_dq_slots(int T, int d, int b, poetx_dtype dt);
 poetx_status tc_forward(const void* x, const void* W0m, const void* Q_P, const void* Q_R,
                         const int32_t* perm_in, const int32_t* inv_in, const int32_t* perm_out,
                         const int32_t* inv_out, int T, int d_in, int d_out, int b_in, int b_out,
@@ -23,7 +25,8 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
                          const void* Q_R, const void* z, const int32_t* perm_in,
                          const int32_t* inv_in, const int32_t* perm_out, const int32_t* inv_out,
                          int T, int d_in, int d_out, int b_in, int b_out, void* dX, void* gz,
-                         void* gu, float* dqp, float* dqr, void* ws, cudaStream_t s);
+                         void* gu, float* dqp, int slots_p, float* dqr, int slots_r, void* ws,
+                         cudaStream_t s);
 
 namespace tc {
 // C[M,N] (bf16) = A[M,K] . B^T with A [M,K] and B [N,K] (b_mn == false) or
@@ -50,10 +53,14 @@ poetx_status cluster_apply_bf16(const void* in, void* out, const void* Q, const 
                                 const int32_t* inv, int T, int d, int b, bool transpose_q,
                                 bool scatter, void* ws, size_t ws_bytes, cudaStream_t s);
 
-// dQ_j[i][k] = sum_t G[t][jb+i] V[t][jb+k] (both operands already gathered);
-// fp32 out [d/b, b, b], overwritten.
+// dQ_j[i][k] = sum_t G[t][jb+i] V[t][jb+k] (both operands already gathered),
+// as n_split partial sums over token ranges: part [n_split][d/b, b, b] fp32,
+// every slot written (the sum over slots is dQ).  dq_splits gives the count
+// that keeps the GPU busy.
 bool dq_supported(int d, int b);
-poetx_status dq_bf16(const void* G, const void* V, int T, int d, int b, float* dQ, cudaStream_t s);
+int dq_splits(int T, int d, int b);
+poetx_status dq_bf16(const void* G, const void* V, int T, int d, int b, int n_split, float* part,
+                     cudaStream_t s);
 
 // out[t][c] = in[t][perm[c]] for bf16 token-major [T, d] (one pass over HBM).
 bool permute_supported(int d);
@@ -71,9 +78,10 @@ poetx_status cnp_fwd_pair_bf16ops(const float* theta0, int nb0, const float* the
 // Backward of both sides of a layer in one launch (after a prep kernel that
 // writes dense bf16 K and G into `ws`, cnp_bwd_workspace_bytes of it).
 size_t cnp_bwd_workspace_bytes(int d_in, int b_in, int d_out, int b_out);
-poetx_status cnp_bwd_layer(const float* theta_P, const float* dQ_P, int nb_P, int b_P,
-                           const float* theta_R, const float* dQ_R, int nb_R, int b_R, int n,
-                           float* dtheta_P, float* dtheta_R, void* ws, cudaStream_t s);
+// dQ_P / dQ_R come as `splits_P` / `splits_R` partial-sum slots [splits][nb, b, b].
+poetx_status cnp_bwd_layer(const float* theta_P, const float* dQ_P, int splits_P, int nb_P, int b_P,
+                           const float* theta_R, const float* dQ_R, int splits_R, int nb_R, int b_R,
+                           int n, float* dtheta_P, float* dtheta_R, void* ws, cudaStream_t s);
 }  // namespace tc
 
 }  // namespace poetx

@@ -59,22 +59,6 @@ constexpr int kFwdWorkers = 256;
 // First packed index of row i (entries (i, i+1) .. (i, b-1)).
 __device__ __forceinline__ int skew_row_start(int i, int b) { return (i * (2 * b - i - 1)) >> 1; }
 
-// Row and column of packed index p (the inverse of skew_index): the root of
-// the quadratic row-start formula, then an exact integer correction.
-__device__ __forceinline__ void skew_rowcol(int p, int b, int& i, int& k) {
-  const float t = (float)(2 * b - 1);
-  int r = (int)((t - sqrtf(fmaxf(t * t - 8.f * (float)p, 0.f))) * 0.5f);
-  r = max(0, min(r, b - 2));
-  while (r < b - 2 && skew_row_start(r + 1, b) <= p) ++r;
-  while (r > 0 && skew_row_start(r, b) > p) --r;
-  i = r;
-  k = p - skew_row_start(r, b) + r + 1;
-}
-
-__device__ __forceinline__ void st_bf16(uint8_t* base, uint32_t off, float v) {
-  *reinterpret_cast<__nv_bfloat16*>(base + off) = __float2bfloat16_rn(v);
-}
-
 // 8 bf16 of a 16-byte shared-memory unit, widened.
 __device__ __forceinline__ void ld_bf16x8(const uint8_t* p, float* v) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
@@ -86,11 +70,6 @@ __device__ __forceinline__ void ld_bf16x8(const uint8_t* p, float* v) {
   }
 }
 
-// One CTA = one 128-row slab of one block.  Shared memory holds Kop, the MMA
-// B operand of X -> X K (Kop[c][k] = K[k][c] = -K[c][k], K-major), unpacked
-// once from the packed parameters with coalesced 16-byte loads, and the bf16
-// A operand X_i of the slab.  The packed parameters are staged again into the
-// freed shared memory for the epilogue, which adds the last 2K exactly in fp32.
 // Two parameter sets (the P and R factors of a layer) may share a launch:
 // blockIdx.y < nb0 selects the first, the rest the second.
 struct FwdSide {
@@ -99,41 +78,119 @@ struct FwdSide {
   int nb;
 };
 
+constexpr int kUnpackThreads = 256;
+constexpr int kUnpackRows = 32;
+
+// Writes Kop = -K (bf16, row-major) of every block into the block's own Q
+// buffer, which the chain kernel then loads by TMA and finally overwrites
+// with Q.  One CTA per 32-row group of one block; the rows are assembled in
+// shared memory (row pitch B + 2 halves, so the column writes fall in
+// distinct banks): Kop[c][k] = -theta(c, k) right of the diagonal (packed row
+// c), +theta(k, c) left of it (packed rows k hold the group's columns
+// contiguously).  All loads are issued before the stores that use them.
+template <int B>
+__global__ void __launch_bounds__(kUnpackThreads)
+    cnp_unpack_kernel(FwdSide f0, FwdSide f1) {
+  __shared__ __nv_bfloat16 tile[kUnpackRows * (B + 2)];
+  constexpr int LD = B + 2;
+  constexpr int P = B * (B - 1) / 2;
+  const bool second = (int)blockIdx.y >= f0.nb;
+  const FwdSide& sd = second ? f1 : f0;
+  const int j = second ? (int)blockIdx.y - f0.nb : (int)blockIdx.y;
+  const int c0 = blockIdx.x * kUnpackRows;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const float* th = sd.theta + (size_t)j * P;
+  constexpr int W = kUnpackThreads / 32;
+  // right of the diagonal (and the diagonal): warp w takes rows c0 + w, c0 + w + 8, ...
+#pragma unroll
+  for (int rr0 = 0; rr0 < kUnpackRows; rr0 += W) {
+    const int rr = rr0 + warp, c = c0 + rr;
+    const float* prow = th + skew_row_start(c, B) - (c + 1);   // prow[k] = theta(c, k)
+    float v[B / 32];
+#pragma unroll
+    for (int q = 0; q < B / 32; ++q) {
+      const int k = q * 32 + lane;
+      v[q] = k > c ? __ldg(prow + k) : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < B / 32; ++q) {
+      const int k = q * 32 + lane;
+      if (k >= c) tile[rr * LD + k] = __float2bfloat16_rn(-v[q]);
+    }
+  }
+  // left of the diagonal: lane = row c0 + lane, warp w takes packed rows k = w, w + 8, ...
+  {
+    const int c = c0 + lane;
+    constexpr int U = 8;
+    for (int k0 = warp; k0 < c0 + kUnpackRows - 1; k0 += W * U) {
+      float v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int k = k0 + u * W;
+        v[u] = k < c ? __ldg(th + skew_row_start(k, B) + (c - k - 1)) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int k = k0 + u * W;
+        if (k < c) tile[lane * LD + k] = __float2bfloat16_rn(v[u]);
+      }
+    }
+  }
+  __syncthreads();
+  uint32_t* kd = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(sd.Q) + ((size_t)j * B + c0) * B);
+  for (int u = threadIdx.x; u < kUnpackRows * B / 2; u += kUnpackThreads) {
+    const int r = u / (B / 2), c2 = (u % (B / 2)) * 2;
+    kd[u] = *reinterpret_cast<const uint32_t*>(tile + r * LD + c2);
+  }
+}
+
+// One CTA = one 128-row slab of one block; for B = 256 the two slabs of a
+// block form a cluster.  Kop (the MMA B operand of X -> X K: Kop[c][k] =
+// K[k][c] = -K[c][k], K-major) arrives by TMA from the block's Q buffer,
+// where the unpack kernel left it; once every slab of the block holds it
+// (cluster barrier) the buffer may be overwritten with Q.  The steps
+//   X_1 = K,  X_{i+1} = X_i K + 2K,  Q = I + X_n K + 2K
+// add 2K from the same bf16 operand (the output is bf16).
 template <int B>
 __global__ void __launch_bounds__(kFwdThreads, 1)
-    cnp_fwd_kernel(FwdSide f0, FwdSide f1, int out_f32, int n, int* err) {
+    cnp_fwd_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_constant__ CUtensorMap tk1,
+                   FwdSide f0, FwdSide f1, int n, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  constexpr int P = B * (B - 1) / 2;   // packed parameters per block (a multiple of 4)
-  uint8_t* kop = smem;                 // [B rows c][B k] bf16
+  uint8_t* kop = smem;                 // [B rows c][B k] bf16, 128-byte swizzle
   uint8_t* amat = smem + B * B * 2;    // [128 rows][B k] bf16
-  float* ths = reinterpret_cast<float*>(smem);   // epilogue: packed parameters (reuses both)
   uint64_t* afull = reinterpret_cast<uint64_t*>(amat + 128 * B * 2);
   uint64_t* stepdone = afull + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stepdone + 1);
-  static_assert(P * 4 <= B * B * 2 + 128 * B * 2, "parameter stage must fit the operands");
+  uint64_t* kfull = stepdone + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(kfull + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const bool second = (int)blockIdx.y >= f0.nb;
   const int j = second ? (int)blockIdx.y - f0.nb : (int)blockIdx.y;
   void* __restrict__ out = second ? f1.Q : f0.Q;
+  const CUtensorMap* tk = second ? &tk1 : &tk0;
   const int r0 = blockIdx.x * 128;
-  const float* th = (second ? f1.theta : f0.theta) + (size_t)j * P;
 
   if (threadIdx.x == 0) {
     mbar_init(afull, kFwdWorkers);
     mbar_init(stepdone, 1);
+    mbar_init(kfull, 1);
     fence_mbar_init();
+    mbar_arrive_expect_tx(kfull, (uint32_t)(B * B * 2));
+    for (int q = 0; q < B / 64; ++q) tma_load_2d(kop + q * (B * 128), tk, q * 64, j * B, kfull);
   }
   if (warp == 0) tmem_alloc(tmem_slot, B);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  bool ok = mbar_wait(kfull, 0, err);
+  // every slab of the block holds Kop: the Q buffer may now be overwritten
+  if constexpr (B == 256) cluster_sync();
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane == 0 && ok) {
       const uint32_t idesc = idesc_bf16(128, B, false, false);
       const uint32_t ab = smem_u32(amat), bb = smem_u32(kop);
       for (int i = 1; i <= n; ++i) {
@@ -148,44 +205,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mma_commit(stepdone);
       }
     }
-  } else {
+  } else if (ok) {
     const int wt = threadIdx.x - 32;
     const int quarter = warp % 4;
     const int half = (warp - 1) / 4;
     const int r = quarter * 32 + lane;
     const int row = r0 + r;
-    bool ok = true;
-    // ---- unpack: Kop[i][k] = -theta(i,k), Kop[k][i] = +theta(i,k), zero diagonal
-    {
-      const float4* th4 = reinterpret_cast<const float4*>(th);
-      constexpr int P4 = P / 4;
-      constexpr int BATCH = 8;
-      for (int q0 = 0; q0 < P4; q0 += kFwdWorkers * BATCH) {
-        float4 v[BATCH];
-#pragma unroll
-        for (int s = 0; s < BATCH; ++s) {
-          const int q = q0 + s * kFwdWorkers + wt;
-          if (q < P4) v[s] = __ldg(th4 + q);
-        }
-#pragma unroll
-        for (int s = 0; s < BATCH; ++s) {
-          const int q = q0 + s * kFwdWorkers + wt;
-          if (q < P4) {
-            int i, k;
-            skew_rowcol(4 * q, B, i, k);
-            const float e4[4] = {v[s].x, v[s].y, v[s].z, v[s].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              st_bf16(kop, sw128_offset(i, k, B), -e4[e]);
-              st_bf16(kop, sw128_offset(k, i, B), e4[e]);
-              if (++k == B) { ++i; k = i + 1; }
-            }
-          }
-        }
-      }
-      for (int c = wt; c < B; c += kFwdWorkers) st_bf16(kop, sw128_offset(c, c, B), 0.f);
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(kFwdWorkers) : "memory");   // Kop complete
     // ---- X_1 = K on the slab rows: A[r][k] = K[r0+r][k] = -Kop[r0+r][k]
     for (int u = wt; u < 128 * (B / 8); u += kFwdWorkers) {
       const int rr = u / (B / 8), k8 = (u % (B / 8)) * 8;
@@ -195,8 +220,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     fence_proxy_async_smem();
     mbar_arrive(afull);
-    // ---- X_{i+1} = X_i K + 2K (2K from the bf16 operand; X is rounded to bf16 anyway)
-    for (int i = 2; i <= n && ok; ++i) {
+    // ---- X_{i+1} = X_i K + 2K (as the next A operand), and finally Q = I + X_n K + 2K
+    for (int i = 2; i <= n + 1 && ok; ++i) {
       if (!(ok = mbar_wait(stepdone, (i - 2) & 1, err))) break;
       tc_fence_after();
       for (int c0 = half * (B / 2); c0 < (half + 1) * (B / 2); c0 += 32) {
@@ -209,44 +234,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         float x[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(rr[e]) - 2.f * kr[e];   // K = -Kop
+        if (i <= n) {
 #pragma unroll
-        for (int g = 0; g < 4; ++g)
-          *reinterpret_cast<uint4*>(amat + sw128_offset(r, c0 + 8 * g, 128)) = pack8(x + 8 * g);
-      }
-      tc_fence_before();
-      fence_proxy_async_smem();
-      mbar_arrive(afull);
-    }
-    // ---- epilogue: Q = I + X_n K + 2K, the last 2K exactly from the staged parameters
-    if (ok && mbar_wait(stepdone, (n - 1) & 1, err)) {
-      tc_fence_after();
-      {
-        const float4* th4 = reinterpret_cast<const float4*>(th);
-        float4* s4 = reinterpret_cast<float4*>(ths);
-        for (int q = wt; q < P / 4; q += kFwdWorkers) s4[q] = __ldg(th4 + q);
-      }
-      asm volatile("bar.sync 1, %0;" ::"n"(kFwdWorkers) : "memory");
-      for (int c0 = half * (B / 2); c0 < (half + 1) * (B / 2); c0 += 32) {
-        uint32_t rr[32];
-        tmem_ld32(tmem_base + (uint32_t)c0 + ((uint32_t)(quarter * 32) << 16), rr);
-        tmem_ld_wait();
-        float q[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int c = c0 + e;
-          const float kv = row < c ? ths[skew_index(row, c, B)]
-                                   : (row > c ? -ths[skew_index(c, row, B)] : 0.f);
-          q[e] = __uint_as_float(rr[e]) + 2.f * kv + (row == c ? 1.f : 0.f);
-        }
-        if (out_f32) {
-          float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + ((size_t)j * B + row) * B + c0);
-#pragma unroll
-          for (int g = 0; g < 8; ++g) o[g] = make_float4(q[4 * g], q[4 * g + 1], q[4 * g + 2], q[4 * g + 3]);
+          for (int g = 0; g < 4; ++g)
+            *reinterpret_cast<uint4*>(amat + sw128_offset(r, c0 + 8 * g, 128)) = pack8(x + 8 * g);
         } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (row == c0 + e) x[e] += 1.f;
           uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + ((size_t)j * B + row) * B + c0);
 #pragma unroll
-          for (int g = 0; g < 4; ++g) o[g] = pack8(q + 8 * g);
+          for (int g = 0; g < 4; ++g) o[g] = pack8(x + 8 * g);
         }
+      }
+      if (i <= n) {
+        tc_fence_before();
+        fence_proxy_async_smem();
+        mbar_arrive(afull);
       }
     }
   }
@@ -261,9 +265,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // ====================================================================== backward
 struct Side {
   const float* theta;
-  const float* dQ;
-  __nv_bfloat16* Kd;   // dense K, [nb, b, b] bf16
+  const float* dQ;     // dQ as n_part partial-sum slots [n_part][nb, b, b]; summed in slot order
+  int n_part;
+  __nv_bfloat16* Kd;   // K, [nb, b, b] bf16: the B operand of X -> X K^T
+  __nv_bfloat16* Td;   // K^T = -K, [nb, b, b] bf16: the first A operand X_1
   __nv_bfloat16* Gd;   // dQ in bf16, [nb, b, b]
+  float* dK;           // dK of every block, fp32 [nb, b, b] (read back when packing)
   float* dtheta;
   int nb;
 };
@@ -271,12 +278,12 @@ struct Side {
 constexpr int kPrepThreads = 256;
 constexpr int kPrepRows = 32;
 
-// Kd[j] = bf16(K_j), Gd[j] = bf16(dQ_j) for both sides; one CTA per 32-row
-// group of one block.  The group's rows of K are assembled in shared memory
-// (row pitch B + 2 halves, so the column writes fall in distinct banks):
-// entries right of the diagonal come from the packed rows of the group, the
-// ones left of it from the packed rows above, which hold the group's columns
-// contiguously; both are read with coalesced loads.
+// Kd[j] = bf16(K_j), Td[j] = -Kd[j], Gd[j] = bf16(dQ_j) for both sides; one
+// CTA per 32-row group of one block.  The group's rows of K are assembled in
+// shared memory (row pitch B + 2 halves, so the column writes fall in
+// distinct banks): entries right of the diagonal come from the packed rows of
+// the group, the ones left of it from the packed rows above, which hold the
+// group's columns contiguously; all loads are issued before their stores.
 template <int B>
 __global__ void __launch_bounds__(kPrepThreads)
     cnp_prep_kernel(Side s0, Side s1) {
@@ -289,51 +296,86 @@ __global__ void __launch_bounds__(kPrepThreads)
   const int c0 = blockIdx.x * kPrepRows;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const float* th = sd.theta + (size_t)j * P;
-  // right of the diagonal: K[c][k] = theta(c, k), packed row c
-  for (int rr = warp; rr < kPrepRows; rr += kPrepThreads / 32) {
-    const int c = c0 + rr;
+  constexpr int W = kPrepThreads / 32;
+#pragma unroll
+  for (int rr0 = 0; rr0 < kPrepRows; rr0 += W) {
+    const int rr = rr0 + warp, c = c0 + rr;
     const float* prow = th + skew_row_start(c, B) - (c + 1);   // prow[k] = theta(c, k)
-    for (int k = c + 1 + lane; k < B; k += 32) tile[rr * LD + k] = __float2bfloat16_rn(__ldg(prow + k));
-    if (lane == 0) tile[rr * LD + c] = __float2bfloat16_rn(0.f);
+    float v[B / 32];
+#pragma unroll
+    for (int q = 0; q < B / 32; ++q) {
+      const int k = q * 32 + lane;
+      v[q] = k > c ? __ldg(prow + k) : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < B / 32; ++q) {
+      const int k = q * 32 + lane;
+      if (k >= c) tile[rr * LD + k] = __float2bfloat16_rn(v[q]);
+    }
   }
-  // left of the diagonal: K[c][k] = -theta(k, c), packed row k holds columns c0.. contiguously
-  for (int k = warp; k < c0 + kPrepRows - 1; k += kPrepThreads / 32) {
+  {
     const int c = c0 + lane;
-    if (k < c) {
-      const float v = __ldg(th + skew_row_start(k, B) + (c - k - 1));
-      tile[lane * LD + k] = __float2bfloat16_rn(-v);
+    constexpr int U = 8;
+    for (int k0 = warp; k0 < c0 + kPrepRows - 1; k0 += W * U) {
+      float v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int k = k0 + u * W;
+        v[u] = k < c ? __ldg(th + skew_row_start(k, B) + (c - k - 1)) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int k = k0 + u * W;
+        if (k < c) tile[lane * LD + k] = __float2bfloat16_rn(-v[u]);
+      }
     }
   }
   // dQ rows of the group -> bf16
   const float4* g4 = reinterpret_cast<const float4*>(sd.dQ + ((size_t)j * B + c0) * B);
+  const size_t slot4 = (size_t)sd.nb * B * B / 4;
   uint4* gd = reinterpret_cast<uint4*>(sd.Gd + ((size_t)j * B + c0) * B);
   for (int u = threadIdx.x; u < kPrepRows * B / 8; u += kPrepThreads) {
-    const float4 a = __ldg(g4 + 2 * u), c = __ldg(g4 + 2 * u + 1);
+    float4 a = __ldg(g4 + 2 * u), c = __ldg(g4 + 2 * u + 1);
+    for (int p = 1; p < sd.n_part; ++p) {
+      const float4 a2 = __ldg(g4 + p * slot4 + 2 * u), c2 = __ldg(g4 + p * slot4 + 2 * u + 1);
+      a.x += a2.x; a.y += a2.y; a.z += a2.z; a.w += a2.w;
+      c.x += c2.x; c.y += c2.y; c.z += c2.z; c.w += c2.w;
+    }
     gd[u] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(c.x, c.y),
                        pack_bf16x2(c.z, c.w));
   }
   __syncthreads();
   uint32_t* kd = reinterpret_cast<uint32_t*>(sd.Kd + ((size_t)j * B + c0) * B);
+  uint32_t* td = reinterpret_cast<uint32_t*>(sd.Td + ((size_t)j * B + c0) * B);
   for (int u = threadIdx.x; u < kPrepRows * B / 2; u += kPrepThreads) {
     const int r = u / (B / 2), c2 = (u % (B / 2)) * 2;
-    kd[u] = *reinterpret_cast<const uint32_t*>(tile + r * LD + c2);
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(tile + r * LD + c2);
+    kd[u] = w;
+    td[u] = w ^ 0x80008000u;
   }
 }
 
 constexpr int kBwdThreads = 320;   // warp 0: TMEM + MMA; warp 1: TMA; warps 2..9: workers
 constexpr int kBwdWorkers = 256;
-
-// Bytes of the fp32 dK slab staged for the packing epilogue: 128 rows, stride B + 1.
-template <int B>
-constexpr int dk_stage_bytes() { return 128 * (B + 1) * 4; }
+constexpr int kPackPitch = 33;     // fp32 pitch of the 32 x 32 transpose tiles
 
 // One CTA = one 128-row slab of one block; for B = 256 the two slabs of a
-// block form a cluster of two CTAs, which exchange the off-diagonal quadrant
-// of dK through distributed shared memory when packing dtheta.
+// block form a cluster.  With A = K^T and G = dL/dQ the chain
+//   X_1 = A, Y_1 = G,  X_{i+1} = X_i A + 2A,  Y_{i+1} = X_i G + Y_i A + 2G,  dK = Y_{n+1}
+// runs as tcgen05.mma into TMEM.  X_1 and Y_1 arrive by TMA (prepared K^T and
+// G rows); the B operands K (for X A, Y A) and G^T stream through a TMA ring;
+// the terms 2A and 2G enter as extra MMAs whose A operand is 2I on the
+// slab's own rows (only the two 64-wide K chunks of the slab are non-zero), so
+// between steps the workers only convert TMEM to bf16 operands.  dK goes to
+// the workspace; after a cluster barrier both slabs pack
+//   dtheta(i,k) = dK[i][k] - dK[k][i]  (i < k)
+// from 32 x 32 tile pairs transposed through shared memory, each CTA taking
+// half of the tiles, every packed entry written exactly once.
 template <int B>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     cnp_bwd_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_constant__ CUtensorMap tg0,
-                   const __grid_constant__ CUtensorMap tk1, const __grid_constant__ CUtensorMap tg1,
+                   const __grid_constant__ CUtensorMap tt0, const __grid_constant__ CUtensorMap tk1,
+                   const __grid_constant__ CUtensorMap tg1, const __grid_constant__ CUtensorMap tt1,
                    Side s0, Side s1, int n, int stages, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -342,24 +384,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const Side& sd = second ? s1 : s0;
   const CUtensorMap* tk = second ? &tk1 : &tk0;
   const CUtensorMap* tg = second ? &tg1 : &tg0;
+  const CUtensorMap* tt = second ? &tt1 : &tt0;
   const int j = second ? (int)blockIdx.y - s0.nb : (int)blockIdx.y;
   const int slab = blockIdx.x;
   const int r0 = slab * 128;
   constexpr int a_bytes = 128 * B * 2;
+  constexpr int i_bytes = 128 * 128 * 2;
   constexpr int chunk_bytes = B * 64 * 2;
   constexpr int kchunks = B / 64;
   constexpr uint32_t ncols = 2 * B;
-  constexpr int LDS = B + 1;
   uint8_t* ax = smem;
   uint8_t* ay = smem + a_bytes;
-  uint8_t* ring = smem + 2 * a_bytes;
-  float* stage = reinterpret_cast<float*>(smem);   // epilogue: dK slab, reuses ax/ay/ring
+  uint8_t* itl = smem + 2 * a_bytes;   // 2I on the slab's K range, [128 rows][128 k], K-major
+  uint8_t* ring = itl + i_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(ring + stages * chunk_bytes);
   uint64_t* bfull = bars;
   uint64_t* bempty = bfull + kMaxStages;
   uint64_t* afull = bempty + kMaxStages;
   uint64_t* stepdone = afull + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stepdone + 1);
+  uint64_t* a0full = stepdone + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(a0full + 1);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
@@ -369,6 +413,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(afull, kBwdWorkers);
     mbar_init(stepdone, 1);
+    mbar_init(a0full, 1);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tmem_slot, ncols);
@@ -379,8 +424,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   bool ok = true;
 
   if (warp == 1) {
-    // ------------------------------------------------ TMA: per step, K chunks then G^T chunks
+    // ------------------------------------------------ TMA: X_1, Y_1, then per step K chunks and G^T chunks
     if (lane == 0) {
+      mbar_arrive_expect_tx(a0full, (uint32_t)(2 * a_bytes));
+      for (int q = 0; q < kchunks; ++q) {
+        tma_load_2d(ax + q * (128 * 128), tt, q * 64, j * B + r0, a0full);   // K^T rows
+        for (int h = 0; h < 2; ++h)                                         // G rows
+          tma_load_2d(ay + q * (128 * 128) + h * (64 * 128), tg, q * 64, j * B + r0 + 64 * h, a0full);
+      }
       int st = 0;
       uint32_t ph = 0;
       for (int i = 1; i <= n && ok; ++i)
@@ -404,9 +455,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t idk = idesc_bf16(128, B, false, false);
       const uint32_t idg = idesc_bf16(128, B, false, true);
       const uint32_t dx = tmem_base, dy = tmem_base + (uint32_t)B;
-      const uint32_t axb = smem_u32(ax), ayb = smem_u32(ay);
+      const uint32_t axb = smem_u32(ax), ayb = smem_u32(ay), itb = smem_u32(itl);
       int st = 0;
       uint32_t ph = 0;
+      ok = mbar_wait(a0full, 0, err);
       for (int i = 1; i <= n && ok; ++i) {
         if (!(ok = mbar_wait(afull, (i - 1) & 1, err))) break;
         tc_fence_after();
@@ -415,17 +467,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after();
           const uint32_t bb = smem_u32(ring + st * chunk_bytes);
           const int kc = c % kchunks;
+          const int ic = kc - r0 / 64;                 // chunk of the 2I tile, when 0 or 1
+          const bool in_slab = ic == 0 || ic == 1;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t xdesc = sw128_desc(axb + kc * 128 * 128 + kk * 32, 16, 1024);
+            const uint64_t idsc = sw128_desc(itb + (in_slab ? ic : 0) * 128 * 128 + kk * 32, 16, 1024);
             if (c < kchunks) {
               const uint64_t bdesc = sw128_desc(bb + kk * 32, 16, 1024);
               const uint32_t acc = (kc | kk) != 0;
-              if (i < n) mma_bf16(dx, xdesc, bdesc, idk, acc);                    // X K^T
+              if (i < n) mma_bf16(dx, xdesc, bdesc, idk, acc);                    // X A
               mma_bf16(dy, sw128_desc(ayb + kc * 128 * 128 + kk * 32, 16, 1024), bdesc, idk,
-                       acc);                                                    // Y K^T
+                       acc);                                                    // Y A
+              if (i < n && in_slab) mma_bf16(dx, idsc, bdesc, idk, 1);          // + 2A
             } else {
-              mma_bf16(dy, xdesc, sw128_desc(bb + kk * 2048, 8192, 1024), idg, 1);  // X G
+              const uint64_t bdesc = sw128_desc(bb + kk * 2048, 8192, 1024);
+              mma_bf16(dy, xdesc, bdesc, idg, 1);                              // X G
+              if (in_slab) mma_bf16(dy, idsc, bdesc, idg, 1);                   // + 2G
             }
           }
           mma_commit(bempty + st);
@@ -435,106 +493,89 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------ workers: A operands, then the dK slab
+    // ------------------------------------------------ workers: 2I tile, operands, dK rows
+    const int wt = threadIdx.x - 64;
     const int quarter = warp % 4;
     const int half = (warp - 2) / 4;
     const int r = quarter * 32 + lane;
     const int row = r0 + r;
-    const __nv_bfloat16* krow = sd.Kd + ((size_t)j * B + row) * B;   // K[row][.]
-    const __nv_bfloat16* gbrow = sd.Gd + ((size_t)j * B + row) * B;  // bf16 G[row][.]
-    const float* grow = sd.dQ + ((size_t)j * B + row) * B;           // G[row][.]
-    for (int i = 1; i <= n && ok; ++i) {
-      if (i > 1) {
-        if (!(ok = mbar_wait(stepdone, (i - 2) & 1, err))) break;
-        tc_fence_after();
-      }
+    for (int u = wt; u < i_bytes / 16; u += kBwdWorkers)
+      reinterpret_cast<uint4*>(itl)[u] = make_uint4(0u, 0u, 0u, 0u);
+    asm volatile("bar.sync 1, %0;" ::"n"(kBwdWorkers) : "memory");
+    if (wt < 128)   // 2.0 at (r, r) of the slab's K range
+      *reinterpret_cast<__nv_bfloat16*>(itl + sw128_offset(wt, wt, 128)) = __float2bfloat16_rn(2.f);
+    fence_proxy_async_smem();
+    mbar_arrive(afull);
+    for (int i = 2; i <= n && ok; ++i) {
+      if (!(ok = mbar_wait(stepdone, (i - 2) & 1, err))) break;
+      tc_fence_after();
       for (int c0 = half * (B / 2); c0 < (half + 1) * (B / 2); c0 += 32) {
-        float kv[32], gv[32];
+        uint32_t rx[32], ry[32];
+        tmem_ld32(tmem_base + (uint32_t)c0 + ((uint32_t)(quarter * 32) << 16), rx);
+        tmem_ld32(tmem_base + (uint32_t)(B + c0) + ((uint32_t)(quarter * 32) << 16), ry);
+        tmem_ld_wait();
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-          const uint4 uk = __ldg(reinterpret_cast<const uint4*>(krow + c0 + 8 * g));
-          const uint4 ug = __ldg(reinterpret_cast<const uint4*>(gbrow + c0 + 8 * g));
-          const uint32_t wk[4] = {uk.x, uk.y, uk.z, uk.w}, wg[4] = {ug.x, ug.y, ug.z, ug.w};
+          float x[8], y[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            kv[8 * g + 2 * e] = __uint_as_float(wk[e] << 16);
-            kv[8 * g + 2 * e + 1] = __uint_as_float(wk[e] & 0xFFFF0000u);
-            gv[8 * g + 2 * e] = __uint_as_float(wg[e] << 16);
-            gv[8 * g + 2 * e + 1] = __uint_as_float(wg[e] & 0xFFFF0000u);
+          for (int e = 0; e < 8; ++e) {
+            x[e] = __uint_as_float(rx[8 * g + e]);
+            y[e] = __uint_as_float(ry[8 * g + e]);
           }
-        }
-        float x[32], y[32];
-        if (i == 1) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            x[e] = -kv[e];   // K^T[row][c] = -K[row][c]
-            y[e] = gv[e];
-          }
-        } else {
-          uint32_t rx[32], ry[32];
-          tmem_ld32(tmem_base + (uint32_t)c0 + ((uint32_t)(quarter * 32) << 16), rx);
-          tmem_ld32(tmem_base + (uint32_t)(B + c0) + ((uint32_t)(quarter * 32) << 16), ry);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            x[e] = __uint_as_float(rx[e]) - 2.f * kv[e];
-            y[e] = __uint_as_float(ry[e]) + 2.f * gv[e];
-          }
-        }
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          *reinterpret_cast<uint4*>(ax + sw128_offset(r, c0 + 8 * g, 128)) = pack8(x + 8 * g);
-          *reinterpret_cast<uint4*>(ay + sw128_offset(r, c0 + 8 * g, 128)) = pack8(y + 8 * g);
+          *reinterpret_cast<uint4*>(ax + sw128_offset(r, c0 + 8 * g, 128)) = pack8(x);
+          *reinterpret_cast<uint4*>(ay + sw128_offset(r, c0 + 8 * g, 128)) = pack8(y);
         }
       }
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(afull);
     }
-    // dK = Y_{n+1} = (last Y product) + 2G, the 2G exactly in fp32; staged in shared memory
+    // dK = Y_{n+1}: the slab's rows to the workspace
     if (ok && (ok = mbar_wait(stepdone, (n - 1) & 1, err))) {
       tc_fence_after();
+      float* drow = sd.dK + ((size_t)j * B + row) * B;
       for (int c0 = half * (B / 2); c0 < (half + 1) * (B / 2); c0 += 32) {
         uint32_t ry[32];
         tmem_ld32(tmem_base + (uint32_t)(B + c0) + ((uint32_t)(quarter * 32) << 16), ry);
-        float g[32];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 v = __ldg(reinterpret_cast<const float4*>(grow + c0) + q);
-          g[4 * q] = v.x; g[4 * q + 1] = v.y; g[4 * q + 2] = v.z; g[4 * q + 3] = v.w;
-        }
         tmem_ld_wait();
+        float4* o = reinterpret_cast<float4*>(drow + c0);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) stage[r * LDS + c0 + e] = __uint_as_float(ry[e]) + 2.f * g[e];
+        for (int q = 0; q < 8; ++q)
+          o[q] = make_float4(__uint_as_float(ry[4 * q]), __uint_as_float(ry[4 * q + 1]),
+                             __uint_as_float(ry[4 * q + 2]), __uint_as_float(ry[4 * q + 3]));
       }
     }
   }
-  // ---- pack: dtheta(i,k) = dK[i][k] - dK[k][i], every packed entry written once.
-  // This slab writes the packed rows i of its own slab.  Partner entries
-  // dK[k][i] with k in the other slab of the block come from the partner CTA.
+  tc_fence_before();
   __syncthreads();
-  if constexpr (B == 256) cluster_sync();   // both slabs staged
-  if (warp >= 2 && ok) {
-    const int wt = threadIdx.x - 64;
-    const int w8 = wt / 32;
+  // every slab's dK rows are written (release/acquire at cluster scope)
+  if constexpr (B == 256) cluster_sync();
+  // ---- pack: 32 x 32 tile pairs (ti <= tk) shared round-robin by the CTAs and warps
+  {
+    constexpr int NT = B / 32;
+    constexpr int CT = B / 128;   // CTAs of the block
+    float* tA = reinterpret_cast<float*>(smem) + warp * (2 * 32 * kPackPitch);
+    float* tB = tA + 32 * kPackPitch;
+    const float* dKj = sd.dK + (size_t)j * B * B;
     float* dth = sd.dtheta + (size_t)j * (B * (B - 1) / 2);
-    uint32_t partner = 0;
-    if constexpr (B == 256) partner = mapa_shared(smem_u32(stage), cluster_ctarank() ^ 1u);
-    for (int i = r0 + w8; i < r0 + 128; i += 8) {
-      float* drow = dth + skew_index(i, i + 1, B) - (i + 1);   // drow[k] = dtheta(i, k)
-      const float* si = stage + (i - r0) * LDS;
-      for (int k = i + 1 + lane; k < B; k += 32) {
-        float other;
-        if (k < r0 + 128) {
-          other = stage[(k - r0) * LDS + i];
-        } else {
-          other = ld_dsmem_f32(partner + (uint32_t)(((k - 128) * LDS + i) * 4));
+    int t = 0;
+    for (int ti = 0; ti < NT; ++ti)
+      for (int tk = ti; tk < NT; ++tk, ++t) {
+        if (t % CT != slab || (t / CT) % (kBwdThreads / 32) != warp) continue;
+        // A[ii][kk] = dK[32ti+ii][32tk+kk],  Bt[kk][ii] = dK[32tk+kk][32ti+ii]
+        for (int ii = 0; ii < 32; ++ii) {
+          tA[ii * kPackPitch + lane] = dKj[(size_t)(32 * ti + ii) * B + 32 * tk + lane];
+          tB[ii * kPackPitch + lane] = dKj[(size_t)(32 * tk + ii) * B + 32 * ti + lane];
         }
-        drow[k] = si[k] - other;
+        __syncwarp();
+        for (int ii = 0; ii < 32; ++ii) {
+          const int i = 32 * ti + ii, k = 32 * tk + lane;
+          if (i < k)
+            dth[skew_row_start(i, B) + (k - i - 1)] = tA[ii * kPackPitch + lane] - tB[lane * kPackPitch + ii];
+        }
+        __syncwarp();
       }
-    }
   }
-  if constexpr (B == 256) cluster_sync();   // the partner has finished reading this slab
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -550,19 +591,49 @@ bool cnp_supported(int b) { return b == 128 || b == 256; }
 poetx_status cnp_fwd_pair_bf16ops(const float* theta0, int nb0, const float* theta1, int nb1,
                                   int b, int n, void* Q0, void* Q1, bool out_f32, cudaStream_t s) {
   if (nb0 + nb1 <= 0) return POETX_OK;
-  if (!cnp_supported(b) || n < 1 || nb0 + nb1 > 65535) return POETX_ERR_UNSUPPORTED;
-  const int smem = b * b * 2 + 128 * b * 2 + 1024 + 256;
-  dim3 grid(b / 128, nb0 + nb1);
+  if (out_f32 || !cnp_supported(b) || n < 1 || nb0 + nb1 > 65535) return POETX_ERR_UNSUPPORTED;
   FwdSide f0{theta0, Q0, nb0}, f1{theta1, Q1, nb1};
+  const FwdSide& t1 = nb1 > 0 ? f1 : f0;
+  const FwdSide& t0 = nb0 > 0 ? f0 : f1;
+  CUtensorMap tk0, tk1;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (!make_tmap_2d(&tk0, t0.Q, bf, 2, (uint64_t)t0.nb * b, (uint64_t)b, (uint32_t)b, 64, sw) ||
+      !make_tmap_2d(&tk1, t1.Q, bf, 2, (uint64_t)t1.nb * b, (uint64_t)b, (uint32_t)b, 64, sw))
+    return POETX_ERR_CUDA;
+  {
+    KernelScope ks_("tc_cnp_unpack", s);
+    if (b == 256)
+      cnp_unpack_kernel<256><<<dim3(256 / kUnpackRows, nb0 + nb1), kUnpackThreads, 0, s>>>(f0, f1);
+    else
+      cnp_unpack_kernel<128><<<dim3(128 / kUnpackRows, nb0 + nb1), kUnpackThreads, 0, s>>>(f0, f1);
+  }
+  poetx_status st = check_launch();
+  if (st != POETX_OK) return st;
+  const int smem = b * b * 2 + 128 * b * 2 + 1024 + 256;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(b / 128, nb0 + nb1);
+  cfg.blockDim = dim3(kFwdThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = b / 128;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   int* err = device_error_word();
   KernelScope ks_("tc_cnp_fwd", s);
+  cudaError_t e;
   if (b == 256) {
     cudaFuncSetAttribute(cnp_fwd_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cnp_fwd_kernel<256><<<grid, kFwdThreads, smem, s>>>(f0, f1, out_f32 ? 1 : 0, n, err);
+    e = cudaLaunchKernelEx(&cfg, cnp_fwd_kernel<256>, tk0, tk1, f0, f1, n, err);
   } else {
     cudaFuncSetAttribute(cnp_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cnp_fwd_kernel<128><<<grid, kFwdThreads, smem, s>>>(f0, f1, out_f32 ? 1 : 0, n, err);
+    e = cudaLaunchKernelEx(&cfg, cnp_fwd_kernel<128>, tk0, tk1, f0, f1, n, err);
   }
+  if (e != cudaSuccess) return check_launch();
   return check_launch();
 }
 
@@ -572,8 +643,8 @@ poetx_status cnp_fwd_bf16ops(const float* theta, int nb, int b, int n, void* Q, 
 }
 
 size_t cnp_bwd_workspace_bytes(int d_in, int b_in, int d_out, int b_out) {
-  // dense bf16 K and bf16 G for every block of both sides
-  return 2 * 2 * ((size_t)d_in * b_in + (size_t)d_out * b_out);
+  // bf16 K, K^T and G, and fp32 dK, for every block of both sides
+  return (2 + 2 + 2 + 4) * ((size_t)d_in * b_in + (size_t)d_out * b_out);
 }
 
 namespace {
@@ -587,20 +658,23 @@ poetx_status cnp_bwd_launch(const Side& s0, const Side& s1, int n, cudaStream_t 
   }
   poetx_status st = check_launch();
   if (st != POETX_OK) return st;
-  CUtensorMap tk0, tg0, tk1, tg1;
+  CUtensorMap tk0, tg0, tt0, tk1, tg1, tt1;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  const Side& t0 = s0.nb > 0 ? s0 : s1;
   const Side& t1 = s1.nb > 0 ? s1 : s0;
-  if (!make_tmap_2d(&tk0, s0.Kd, bf, 2, (uint64_t)s0.nb * B, B, B, 64, sw) ||
-      !make_tmap_2d(&tg0, s0.Gd, bf, 2, (uint64_t)s0.nb * B, B, 64, 64, sw) ||
+  if (!make_tmap_2d(&tk0, t0.Kd, bf, 2, (uint64_t)t0.nb * B, B, B, 64, sw) ||
+      !make_tmap_2d(&tg0, t0.Gd, bf, 2, (uint64_t)t0.nb * B, B, 64, 64, sw) ||
+      !make_tmap_2d(&tt0, t0.Td, bf, 2, (uint64_t)t0.nb * B, B, 128, 64, sw) ||
       !make_tmap_2d(&tk1, t1.Kd, bf, 2, (uint64_t)t1.nb * B, B, B, 64, sw) ||
-      !make_tmap_2d(&tg1, t1.Gd, bf, 2, (uint64_t)t1.nb * B, B, 64, 64, sw))
+      !make_tmap_2d(&tg1, t1.Gd, bf, 2, (uint64_t)t1.nb * B, B, 64, 64, sw) ||
+      !make_tmap_2d(&tt1, t1.Td, bf, 2, (uint64_t)t1.nb * B, B, 128, 64, sw))
     return POETX_ERR_CUDA;
-  constexpr int a_bytes = 128 * B * 2, chunk_bytes = B * 64 * 2;
-  int stages = (kSmemMax - 2 * a_bytes - 1024 - 256) / chunk_bytes;
+  constexpr int a_bytes = 128 * B * 2, i_bytes = 128 * 128 * 2, chunk_bytes = B * 64 * 2;
+  constexpr int fixed = 2 * a_bytes + i_bytes + 1024 + 256;
+  int stages = (kSmemMax - fixed) / chunk_bytes;
   if (stages > kMaxStages) stages = kMaxStages;
-  int smem = 2 * a_bytes + stages * chunk_bytes + 1024 + 256;
-  if (smem < dk_stage_bytes<B>() + 1024 + 256) smem = dk_stage_bytes<B>() + 1024 + 256;
+  const int smem = fixed + stages * chunk_bytes;
   auto kern = cnp_bwd_kernel<B>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   cudaLaunchConfig_t cfg = {};
@@ -618,7 +692,8 @@ poetx_status cnp_bwd_launch(const Side& s0, const Side& s1, int n, cudaStream_t 
   int* err = device_error_word();
   {
     KernelScope ks_("tc_cnp_bwd", s);
-    if (cudaLaunchKernelEx(&cfg, kern, tk0, tg0, tk1, tg1, s0, s1, n, stages, err) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, kern, tk0, tg0, tt0, tk1, tg1, tt1, s0, s1, n, stages, err) !=
+        cudaSuccess)
       return check_launch();
   }
   return check_launch();
@@ -635,17 +710,35 @@ poetx_status cnp_bwd_one(const Side& sd, int b, int n, cudaStream_t s) {
   return b == 256 ? cnp_bwd_launch<256>(sd, none, n, s) : cnp_bwd_launch<128>(sd, none, n, s);
 }
 
+// The side's part of the workspace: K, K^T, G (bf16) and dK (fp32) of nb blocks.
+Side carve(const float* theta, const float* dQ, int n_part, float* dtheta, int nb, int b,
+           uint8_t*& w) {
+  const size_t e = (size_t)nb * b * b;
+  Side sd;
+  sd.theta = theta;
+  sd.dQ = dQ;
+  sd.n_part = n_part;
+  sd.dtheta = dtheta;
+  sd.nb = nb;
+  sd.Kd = reinterpret_cast<__nv_bfloat16*>(w);
+  sd.Td = sd.Kd + e;
+  sd.Gd = sd.Td + e;
+  sd.dK = reinterpret_cast<float*>(sd.Gd + e);
+  w += 10 * e;
+  return sd;
+}
+
 }  // namespace
 
-poetx_status cnp_bwd_layer(const float* theta_P, const float* dQ_P, int nb_P, int b_P,
-                           const float* theta_R, const float* dQ_R, int nb_R, int b_R, int n,
-                           float* dtheta_P, float* dtheta_R, void* ws, cudaStream_t s) {
-  if (!cnp_supported(b_P) || !cnp_supported(b_R) || n < 1 || nb_P + nb_R > 65535)
+poetx_status cnp_bwd_layer(const float* theta_P, const float* dQ_P, int splits_P, int nb_P, int b_P,
+                           const float* theta_R, const float* dQ_R, int splits_R, int nb_R, int b_R,
+                           int n, float* dtheta_P, float* dtheta_R, void* ws, cudaStream_t s) {
+  if (!cnp_supported(b_P) || !cnp_supported(b_R) || n < 1 || nb_P + nb_R > 65535 ||
+      splits_P < 1 || splits_R < 1)
     return POETX_ERR_UNSUPPORTED;
-  __nv_bfloat16* w = static_cast<__nv_bfloat16*>(ws);
-  Side sp{theta_P, dQ_P, w, w + (size_t)nb_P * b_P * b_P, dtheta_P, nb_P};
-  __nv_bfloat16* w2 = w + 2 * (size_t)nb_P * b_P * b_P;
-  Side sr{theta_R, dQ_R, w2, w2 + (size_t)nb_R * b_R * b_R, dtheta_R, nb_R};
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const Side sp = carve(theta_P, dQ_P, splits_P, dtheta_P, nb_P, b_P, w);
+  const Side sr = carve(theta_R, dQ_R, splits_R, dtheta_R, nb_R, b_R, w);
   if (b_P == b_R)
     return b_P == 256 ? cnp_bwd_sides<256>(sp, sr, n, s) : cnp_bwd_sides<128>(sp, sr, n, s);
   const poetx_status st = cnp_bwd_one(sp, b_P, n, s);

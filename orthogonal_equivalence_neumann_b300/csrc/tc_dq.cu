@@ -14,8 +14,10 @@
 // columns k, K = 16 tokens, both operands MN-major tiles of [64 tokens x b
 // features] brought in by TMA (128-byte swizzle) through a multi-stage ring.
 // A CTA owns one block and a contiguous range of 64-token chunks; its fp32
-// accumulator lives in TMEM and is added to dQ (zeroed first) with vector
-// reductions at the end.  All waits are bounded.
+// accumulator lives in TMEM and is written, at the end, to the CTA's own slot
+// of a partial-sum buffer [splits][d][b]; the consumer adds the slots in a
+// fixed order, so the result does not depend on scheduling.  All waits are
+// bounded.
 #include "common.cuh"
 #include "profile.cuh"
 #include "tc.cuh"
@@ -33,16 +35,10 @@ constexpr int kSmemMax = 232448;
 constexpr int kMaxStages = 8;
 constexpr int kMaxSplit = 9;
 
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
-               "f"(d)
-               : "memory");
-}
-
 template <int B>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmV,
-              int nb, int n_chunks, int n_split, int stages, float* __restrict__ dQ, int* err) {
+              int nb, int n_chunks, int n_split, int stages, float* __restrict__ part, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -119,21 +115,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // epilogue warps 2..5 own TMEM lane quarters (warp % 4): rows i, columns k
-    if (c_end > c_begin && mbar_wait(dfull, 0, err)) {
-      tc_fence_after();
-      const int quarter = warp % 4;
-      for (int h = 0; h < halves; ++h) {
-        const int i = h * 128 + quarter * 32 + lane;
-        float* drow = dQ + ((size_t)j * B + i) * B;
-        for (int c0 = 0; c0 < B; c0 += 32) {
-          uint32_t r[32];
+    const int quarter = warp % 4;
+    const bool any = c_end > c_begin;
+    if (any && mbar_wait(dfull, 0, err)) tc_fence_after();
+    float* slot = part + (size_t)split * nb * B * B;
+    for (int h = 0; h < halves; ++h) {
+      const int i = h * 128 + quarter * 32 + lane;
+      float4* drow = reinterpret_cast<float4*>(slot + ((size_t)j * B + i) * B);
+      for (int c0 = 0; c0 < B; c0 += 32) {
+        uint32_t r[32];
+        if (any) {
           tmem_ld32(tmem_base + (uint32_t)(h * B + c0) + ((uint32_t)(quarter * 32) << 16), r);
           tmem_ld_wait();
+        } else {
 #pragma unroll
-          for (int v = 0; v < 32; v += 4)
-            red_add_v4(drow + c0 + v, __uint_as_float(r[v]), __uint_as_float(r[v + 1]),
-                       __uint_as_float(r[v + 2]), __uint_as_float(r[v + 3]));
+          for (int v = 0; v < 32; ++v) r[v] = 0u;   // an empty token range contributes zero
         }
+#pragma unroll
+        for (int v = 0; v < 32; v += 4)
+          drow[(c0 + v) / 4] = make_float4(__uint_as_float(r[v]), __uint_as_float(r[v + 1]),
+                                           __uint_as_float(r[v + 2]), __uint_as_float(r[v + 3]));
       }
     }
   }
@@ -149,29 +150,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 bool dq_supported(int d, int b) { return (b == 128 || b == 256) && d % b == 0; }
 
-// dQ_j[i][k] = sum_t G[t][jb+i] V[t][jb+k]; fp32 out [d/b, b, b], overwritten.
-poetx_status dq_bf16(const void* G, const void* V, int T, int d, int b, float* dQ, cudaStream_t s) {
-  if (cudaMemsetAsync(dQ, 0, sizeof(float) * (size_t)d * b, s) != cudaSuccess) return check_launch();
-  if (T <= 0) return POETX_OK;
-  if (!dq_supported(d, b)) return POETX_ERR_UNSUPPORTED;
+// Token splits per block: enough CTAs to keep HBM busy, few enough that the
+// partial sums (b x b fp32 per CTA) stay a small part of the traffic.
+int dq_splits(int T, int d, int b) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    cudaGetLastError();
+    sms = 148;
+  }
+  const int nb = d / b;
+  const int n_chunks = (T + KT - 1) / KT;
+  int n_split = sms / nb;
+  if (n_split > kMaxSplit) n_split = kMaxSplit;
+  if (n_split > n_chunks) n_split = n_chunks;
+  if (n_split < 1) n_split = 1;
+  return n_split;
+}
+
+// part[s][j][i][k] = sum over split s's tokens of G[t][jb+i] V[t][jb+k], s < n_split.
+poetx_status dq_bf16(const void* G, const void* V, int T, int d, int b, int n_split, float* part,
+                     cudaStream_t s) {
+  if (!dq_supported(d, b) || n_split < 1 || n_split > kMaxSplit) return POETX_ERR_UNSUPPORTED;
+  if (T <= 0) {
+    if (cudaMemsetAsync(part, 0, sizeof(float) * (size_t)n_split * d * b, s) != cudaSuccess)
+      return check_launch();
+    return POETX_OK;
+  }
   CUtensorMap tg, tv;
   if (!make_tmap_2d(&tg, G, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)T, (uint64_t)d, KT, 64,
                     CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap_2d(&tv, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)T, (uint64_t)d, KT, 64,
                     CU_TENSOR_MAP_SWIZZLE_128B))
     return POETX_ERR_CUDA;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int nb = d / b;
   const int n_chunks = (T + KT - 1) / KT;
-  // Token splits per block: enough CTAs to keep HBM busy, few enough that the
-  // fp32 partial sums (b x b per CTA, reduced into dQ with vector atomics at
-  // the end) stay a small fraction of the traffic.
-  int n_split = sms / nb;
-  if (n_split > kMaxSplit) n_split = kMaxSplit;
-  if (n_split < 1) n_split = 1;
-  if (n_split > n_chunks) n_split = n_chunks;
   const int tile_bytes = KT * b * 2;
   int stages = (kSmemMax - 1024 - 256) / (2 * tile_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
@@ -181,7 +194,7 @@ poetx_status dq_bf16(const void* G, const void* V, int T, int d, int b, float* d
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   {
     KernelScope ks_("tc_dq", s);
-    kern<<<nb * n_split, kThreads, smem, s>>>(tg, tv, nb, n_chunks, n_split, stages, dQ, err);
+    kern<<<nb * n_split, kThreads, smem, s>>>(tg, tv, nb, n_chunks, n_split, stages, part, err);
   }
   return check_launch();
 }

@@ -70,6 +70,10 @@ size_t tc_workspace_bytes(int T, int d_in, int d_out, int b_in, int b_out, poetx
   return bytes;
 }
 
+int tc_dq_slots(int T, int d, int b, poetx_dtype dt) {
+  return (dt == POETX_BF16 && dq_tc(d, b)) ? tc::dq_splits(T, d, b) : 1;
+}
+
 // Offset of the CNP backward's part of the tensor-core scratch.
 size_t tc_cnp_ws_offset(int T, int d_in, int d_out, int b_in, int b_out) {
   return shared_region_bytes(T, d_in, d_out, b_in, b_out, true);
@@ -91,15 +95,16 @@ static poetx_status block_apply(const void* in, void* out, const void* Q, int T,
 }
 
 // dQ token sums: gather once, then tensor cores, when the shape allows; CUDA cores otherwise.
+// `slots` partial sums on the tensor-core path (each written whole), one plain sum otherwise.
 static poetx_status dq(const void* G, const void* V, int T, int d, int b, const int32_t* gG,
-                       const int32_t* gV, float* out, void* gbuf, cudaStream_t s) {
+                       const int32_t* gV, float* out, int slots, void* gbuf, cudaStream_t s) {
   if (dq_tc(d, b)) {
     if (gG) {
       TC_TRY(tc::permute_cols_bf16(G, gbuf, gG, T, d, s));
-      return tc::dq_bf16(gbuf, V, T, d, b, out, s);
+      return tc::dq_bf16(gbuf, V, T, d, b, slots, out, s);
     }
     TC_TRY(tc::permute_cols_bf16(V, gbuf, gV, T, d, s));
-    return tc::dq_bf16(G, gbuf, T, d, b, out, s);
+    return tc::dq_bf16(G, gbuf, T, d, b, slots, out, s);
   }
   return launch_dq_simt(G, V, T, d, b, gG, gV, out, POETX_BF16, s);
 }
@@ -118,12 +123,13 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
                          const void* Q_R, const void* z, const int32_t* perm_in,
                          const int32_t* inv_in, const int32_t* perm_out, const int32_t* inv_out,
                          int T, int d_in, int d_out, int b_in, int b_out, void* dX, void* gz,
-                         void* gu, float* dqp, float* dqr, void* ws, cudaStream_t s) {
+                         void* gu, float* dqp, int slots_p, float* dqr, int slots_r, void* ws,
+                         cudaStream_t s) {
   TC_TRY(block_apply(dy, gz, Q_R, T, d_out, b_out, perm_out, inv_out, nullptr, true, ws, s));
-  TC_TRY(dq(dy, z, T, d_out, b_out, perm_out, nullptr, dqr, ws, s));
+  TC_TRY(dq(dy, z, T, d_out, b_out, perm_out, nullptr, dqr, slots_r, ws, s));
   TC_TRY(tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s));
   TC_TRY(block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, nullptr, perm_in, true, ws, s));
-  TC_TRY(dq(gu, x, T, d_in, b_in, nullptr, perm_in, dqp, ws, s));
+  TC_TRY(dq(gu, x, T, d_in, b_in, nullptr, perm_in, dqp, slots_p, ws, s));
   return POETX_OK;
 }
 
