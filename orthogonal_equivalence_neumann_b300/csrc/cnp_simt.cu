@@ -245,14 +245,13 @@ poetx_status launch_cnp_fwd_simt(const float* theta, int nb, int b, int n, void*
   dim3 grid(b / rows, nb);
   const size_t smem = cnp_fwd_simt_smem(b);
   if (out_dtype == POETX_F32) {
-    cudaFuncSetAttribute(cnp_fwd_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    set_max_dynamic_smem((const void*)cnp_fwd_kernel<float>, (int)smem);
     {
       KernelScope ks_("cnp_fwd_simt", s);
       cnp_fwd_kernel<float><<<grid, kThreads, smem, s>>>(theta, b, n, (float*)Q);
     }
   } else {
-    cudaFuncSetAttribute(cnp_fwd_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)smem);
+    set_max_dynamic_smem((const void*)cnp_fwd_kernel<__nv_bfloat16>, (int)smem);
     {
       KernelScope ks_("cnp_fwd_simt", s);
       cnp_fwd_kernel<__nv_bfloat16><<<grid, kThreads, smem, s>>>(theta, b, n, (__nv_bfloat16*)Q);
@@ -268,7 +267,7 @@ poetx_status launch_cnp_bwd_simt(const float* theta, const float* dQ, int nb, in
   const int cols = b < kColSlab ? b : kColSlab;
   dim3 grid(b / cols, nb);
   const size_t smem = cnp_bwd_simt_smem(b);
-  cudaFuncSetAttribute(cnp_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  set_max_dynamic_smem((const void*)cnp_bwd_kernel, (int)smem);
   {
     KernelScope ks_("cnp_bwd_simt", s);
     cnp_bwd_kernel<<<grid, kThreads, smem, s>>>(theta, dQ, b, n, dtheta);

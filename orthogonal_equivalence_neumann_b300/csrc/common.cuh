@@ -56,4 +56,13 @@ poetx_status check_launch();
 // Device address of the error word on the current device (nullptr on failure).
 int* device_error_word();
 
+// Launch set-up that does not change between calls, done once (launch.cu):
+// the multiprocessor count of the current device; the dynamic shared memory
+// limit of a kernel (set once per device, kernel and size); the number of
+// clusters of a kernel's launch configuration that fit on the device at once
+// (0 if none or on error).
+int device_sm_count();
+cudaError_t set_max_dynamic_smem(const void* kernel, int bytes);
+int max_active_clusters(const void* kernel, const cudaLaunchConfig_t& cfg);
+
 }  // namespace poetx

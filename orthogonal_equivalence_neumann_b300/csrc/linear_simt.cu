@@ -259,7 +259,7 @@ poetx_status launch_block_apply_simt(const void* in, void* out, const void* Qs, 
   const size_t smem = sizeof(float) * ((size_t)kTok * b + (size_t)b * (kc + 1));
   if (dt == POETX_F32) {
     auto k = block_apply_kernel<float, float, float>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    set_max_dynamic_smem((const void*)k, (int)smem);
     {
       KernelScope ks_("block_apply_simt", s);
       k<<<grid, kThreads, smem, s>>>((const float*)in, (float*)out, (const float*)Qs, T, d, b, gath,
@@ -267,7 +267,7 @@ poetx_status launch_block_apply_simt(const void* in, void* out, const void* Qs, 
     }
   } else {
     auto k = block_apply_kernel<__nv_bfloat16, __nv_bfloat16, __nv_bfloat16>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    set_max_dynamic_smem((const void*)k, (int)smem);
     {
       KernelScope ks_("block_apply_simt", s);
       k<<<grid, kThreads, smem, s>>>((const __nv_bfloat16*)in, (__nv_bfloat16*)out,

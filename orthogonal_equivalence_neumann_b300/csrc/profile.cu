@@ -5,7 +5,8 @@
 // of CUDA events recorded on the launch's own stream.  poetx_profile_report()
 // waits for those events and returns, per kernel name, the launch count and
 // the summed device time.  Off by default; events are recycled, no device
-// memory is allocated.
+// memory is allocated.  Launches captured into a CUDA graph carry their event
+// pair into the graph; a report after a replay gives that replay's times.
 #include <atomic>
 #include <map>
 #include <mutex>
@@ -44,6 +45,17 @@ cudaEvent_t take_event() {
   return e;
 }
 
+// Records `e` on `s`.  While `s` is being captured into a CUDA graph the
+// record becomes a node of the graph (an external event record), so every
+// replay re-records the pair around the kernel's node.
+void record(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, s);
+}
+
 }  // namespace
 
 KernelScope::KernelScope(const char* name, cudaStream_t s) : name_(name), stream_(s) {
@@ -52,12 +64,12 @@ KernelScope::KernelScope(const char* name, cudaStream_t s) : name_(name), stream
   std::lock_guard<std::mutex> lk(g_mu);
   begin_ = take_event();
   end_ = take_event();
-  if (begin_ && end_) cudaEventRecord(begin_, stream_);
+  if (begin_ && end_) record(begin_, stream_);
 }
 
 KernelScope::~KernelScope() {
   if (!begin_ || !end_) return;
-  cudaEventRecord(end_, stream_);
+  record(end_, stream_);
   std::lock_guard<std::mutex> lk(g_mu);
   g_pending.push_back(Pending{name_, begin_, end_});
 }

@@ -369,15 +369,13 @@ poetx_status blockapply_bf16(const void* in, void* out, const void* Q, const int
                   : make_tmap_2d(&tq, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)nb * b,
                                  (uint64_t)b, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!okq) return POETX_ERR_CUDA;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = device_sm_count();
   const int n_slabs = (T + g.TM - 1) / g.TM;
   const int grid = n_slabs < sms ? n_slabs : sms;
   int* err = device_error_word();
   const char* name = scatter ? "tc_blockapply_scatter" : "tc_blockapply_gather";
   auto launch = [&](auto kern) {
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem);
+    set_max_dynamic_smem((const void*)kern, g.smem);
     KernelScope ks_(name, s);
     kern<<<grid, kThreads, g.smem, s>>>(tin, tq, (__nv_bfloat16*)out, perm, T, d, b,
                                         transpose_q ? 1 : 0, g.stages, err);

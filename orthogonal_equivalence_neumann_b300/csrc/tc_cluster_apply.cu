@@ -681,16 +681,6 @@ bool ca_geometry(int d, int b, bool gather, CaGeo* out) {
   return false;
 }
 
-int device_sms() {
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
-    cudaGetLastError();
-    sms = 148;
-  }
-  return sms;
-}
-
 }  // namespace
 
 bool cluster_apply_supported(int d, int b, bool scatter) {
@@ -702,7 +692,7 @@ bool cluster_apply_supported(int d, int b, bool scatter) {
 size_t cluster_apply_workspace_bytes(int d, int b, bool scatter) {
   CaGeo g;
   if (!ca_geometry(d, b, !scatter, &g)) return 0;
-  const int clusters = device_sms() / g.C;
+  const int clusters = device_sm_count() / g.C;
   return (size_t)clusters * g.NX * g.C * g.r_bytes;
 }
 
@@ -728,8 +718,7 @@ poetx_status cluster_apply_bf16(const void* in, void* out, const void* Q, const 
     kern = b == 256 ? (const void*)ca_scatter_kernel<256> : (const void*)ca_scatter_kernel<128>;
   else
     kern = b == 256 ? (const void*)ca_gather_kernel<256> : (const void*)ca_gather_kernel<128>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem) != cudaSuccess)
-    return check_launch();
+  if (set_max_dynamic_smem(kern, g.smem) != cudaSuccess) return check_launch();
   if (g.C > 8 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
     return check_launch();
@@ -746,13 +735,10 @@ poetx_status cluster_apply_bf16(const void* in, void* out, const void* Q, const 
   cfg.numAttrs = 1;
   // as many clusters as can be resident at once (persistent), but no more than
   // tiles, nor than the exchange ring was sized for
-  const int sms = device_sms();
+  const int sms = device_sm_count();
   cfg.gridDim = dim3((sms / g.C) * g.C);
-  int active = 0;
-  if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess || active < 1) {
-    cudaGetLastError();
-    return POETX_ERR_UNSUPPORTED;
-  }
+  const int active = max_active_clusters(kern, cfg);
+  if (active < 1) return POETX_ERR_UNSUPPORTED;
   const int n_tiles = (T + TT - 1) / TT;
   int clusters = active < n_tiles ? active : n_tiles;
   if (clusters > sms / g.C) clusters = sms / g.C;

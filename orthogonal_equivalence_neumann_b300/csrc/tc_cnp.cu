@@ -530,19 +530,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(afull);
     }
-    // dK = Y_{n+1}: the slab's rows to the workspace
+    // dK = Y_{n+1}: the slab's rows to the workspace, 32 x 32 tiles turned
+    // through the warp's own shared-memory tile (the chain's operand buffers
+    // are free once the last step is done) so that each store is a full row
+    // segment of 128 bytes
     if (ok && (ok = mbar_wait(stepdone, (n - 1) & 1, err))) {
       tc_fence_after();
-      float* drow = sd.dK + ((size_t)j * B + row) * B;
+      float* tt = reinterpret_cast<float*>(smem) + warp * (2 * 32 * kPackPitch);
+      float* dtile = sd.dK + ((size_t)j * B + r0 + quarter * 32) * B;
       for (int c0 = half * (B / 2); c0 < (half + 1) * (B / 2); c0 += 32) {
         uint32_t ry[32];
         tmem_ld32(tmem_base + (uint32_t)(B + c0) + ((uint32_t)(quarter * 32) << 16), ry);
         tmem_ld_wait();
-        float4* o = reinterpret_cast<float4*>(drow + c0);
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          o[q] = make_float4(__uint_as_float(ry[4 * q]), __uint_as_float(ry[4 * q + 1]),
-                             __uint_as_float(ry[4 * q + 2]), __uint_as_float(ry[4 * q + 3]));
+        for (int e = 0; e < 32; ++e) tt[lane * kPackPitch + e] = __uint_as_float(ry[e]);
+        __syncwarp();
+#pragma unroll 8
+        for (int rr = 0; rr < 32; ++rr) dtile[(size_t)rr * B + c0 + lane] = tt[rr * kPackPitch + lane];
+        __syncwarp();
       }
     }
   }
@@ -562,10 +567,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int ti = 0; ti < NT; ++ti)
       for (int tk = ti; tk < NT; ++tk, ++t) {
         if (t % CT != slab || (t / CT) % (kBwdThreads / 32) != warp) continue;
-        // A[ii][kk] = dK[32ti+ii][32tk+kk],  Bt[kk][ii] = dK[32tk+kk][32ti+ii]
+        // A[ii][kk] = dK[32ti+ii][32tk+kk],  Bt[kk][ii] = dK[32tk+kk][32ti+ii]: all 64
+        // row segments are requested before any is stored (one round trip to L2;
+        // the partner slab's rows were written by another CTA: read at L2)
+        float va[32], vb[32];
+#pragma unroll
         for (int ii = 0; ii < 32; ++ii) {
-          tA[ii * kPackPitch + lane] = dKj[(size_t)(32 * ti + ii) * B + 32 * tk + lane];
-          tB[ii * kPackPitch + lane] = dKj[(size_t)(32 * tk + ii) * B + 32 * ti + lane];
+          va[ii] = __ldcg(dKj + (size_t)(32 * ti + ii) * B + 32 * tk + lane);
+          vb[ii] = __ldcg(dKj + (size_t)(32 * tk + ii) * B + 32 * ti + lane);
+        }
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) {
+          tA[ii * kPackPitch + lane] = va[ii];
+          tB[ii * kPackPitch + lane] = vb[ii];
         }
         __syncwarp();
         for (int ii = 0; ii < 32; ++ii) {
@@ -627,10 +641,10 @@ poetx_status cnp_fwd_pair_bf16ops(const float* theta0, int nb0, const float* the
   KernelScope ks_("tc_cnp_fwd", s);
   cudaError_t e;
   if (b == 256) {
-    cudaFuncSetAttribute(cnp_fwd_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    set_max_dynamic_smem((const void*)cnp_fwd_kernel<256>, smem);
     e = cudaLaunchKernelEx(&cfg, cnp_fwd_kernel<256>, tk0, tk1, f0, f1, n, err);
   } else {
-    cudaFuncSetAttribute(cnp_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    set_max_dynamic_smem((const void*)cnp_fwd_kernel<128>, smem);
     e = cudaLaunchKernelEx(&cfg, cnp_fwd_kernel<128>, tk0, tk1, f0, f1, n, err);
   }
   if (e != cudaSuccess) return check_launch();
@@ -676,7 +690,7 @@ poetx_status cnp_bwd_launch(const Side& s0, const Side& s1, int n, cudaStream_t 
   if (stages > kMaxStages) stages = kMaxStages;
   const int smem = fixed + stages * chunk_bytes;
   auto kern = cnp_bwd_kernel<B>;
-  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  set_max_dynamic_smem((const void*)kern, smem);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(B / 128, nb);
   cfg.blockDim = dim3(kBwdThreads);

@@ -153,12 +153,7 @@ bool dq_supported(int d, int b) { return (b == 128 || b == 256) && d % b == 0; }
 // Token splits per block: enough CTAs to keep HBM busy, few enough that the
 // partial sums (b x b fp32 per CTA) stay a small part of the traffic.
 int dq_splits(int T, int d, int b) {
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
-    cudaGetLastError();
-    sms = 148;
-  }
+  const int sms = device_sm_count();
   const int nb = d / b;
   const int n_chunks = (T + KT - 1) / KT;
   int n_split = sms / nb;
@@ -191,7 +186,7 @@ poetx_status dq_bf16(const void* G, const void* V, int T, int d, int b, int n_sp
   const int smem = stages * 2 * tile_bytes + 1024 + 256;
   int* err = device_error_word();
   auto kern = b == 256 ? dq_kernel<256> : dq_kernel<128>;
-  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  set_max_dynamic_smem((const void*)kern, smem);
   {
     KernelScope ks_("tc_dq", s);
     kern<<<nb * n_split, kThreads, smem, s>>>(tg, tv, nb, n_chunks, n_split, stages, part, err);

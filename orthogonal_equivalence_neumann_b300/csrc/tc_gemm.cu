@@ -171,17 +171,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-int sm_count() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
-
 }  // namespace
 
 bool gemm_supported(int N, int K) { return N % BN == 0 && K % BK == 0 && N > 0 && K > 0; }
@@ -202,8 +191,8 @@ poetx_status gemm_bf16(const void* A, const void* B, void* C, int M, int N, int 
                           BK, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!okb) return POETX_ERR_CUDA;
   const int tiles = ((M + BM - 1) / BM) * (N / BN);
-  const int grid = tiles < sm_count() ? tiles : sm_count();
-  cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
+  set_max_dynamic_smem((const void*)gemm_bf16_kernel, SMEM_BYTES);
   {
     KernelScope ks_(b_mn ? "tc_gemm_nn" : "tc_gemm_nt", s);
     gemm_bf16_kernel<<<grid, kThreads, SMEM_BYTES, s>>>(ta, tb, (__nv_bfloat16*)C, M, N, K,

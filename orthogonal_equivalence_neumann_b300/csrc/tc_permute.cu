@@ -125,13 +125,11 @@ poetx_status permute_cols_bf16(const void* in, void* out, const int32_t* perm, i
   if (!make_tmap_2d(&tin, in, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)T, (uint64_t)d,
                     (uint32_t)TM, 64, CU_TENSOR_MAP_SWIZZLE_128B))
     return POETX_ERR_CUDA;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = device_sm_count();
   const int n_slabs = (T + TM - 1) / TM;
   const int grid = n_slabs < sms ? n_slabs : sms;
   const int smem = 2 * TM * d * 2 + 1024 + 64;
-  cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  set_max_dynamic_smem((const void*)permute_kernel, smem);
   {
     KernelScope ks_("tc_permute_cols", s);
     permute_kernel<<<grid, kPermThreads, smem, s>>>(tin, static_cast<__nv_bfloat16*>(out), perm, T,

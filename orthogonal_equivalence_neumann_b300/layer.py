@@ -12,6 +12,8 @@ order of one training step:
 (source: "POET-X: Memory-efficient LLM Training by Scaling Orthogonal
 Transformation", gist.science summary, section 2).  PyTorch only allocates
 the buffers and supplies the stream; every step runs in the library's kernels.
+``capture_step`` records one step's launches into a CUDA graph, so that a
+training loop pays one host launch per step instead of one per kernel.
 """
 import torch
 
@@ -83,3 +85,22 @@ class TransformedLinear:
         y = self.forward(x, y)
         dX, dtp, dtr = self.backward(x, dy, dX)
         return y, dX, dtp, dtr
+
+    def capture_step(self, x, dy, y, dX, warm=True):
+        """Capture one step on fixed buffers into a CUDA graph and return it.
+
+        ``graph.replay()`` re-runs the whole step (the same kernels with the
+        same arguments) on whatever ``x``, ``dy`` and the parameters hold at
+        replay time, writing ``y``, ``dX`` and the skew gradients.  With
+        ``warm`` the step first runs once eagerly on a side stream, so every
+        launch's one-time set-up is done before capture."""
+        if warm:
+            side = torch.cuda.Stream(device=x.device)
+            side.wait_stream(torch.cuda.current_stream(x.device))
+            with torch.cuda.stream(side):
+                self.step(x, dy, y, dX)
+            torch.cuda.current_stream(x.device).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+            self.step(x, dy, y, dX)
+        return graph

@@ -268,6 +268,44 @@ def test_bf16_layer_is_run_to_run_deterministic(d, b, T):
         assert np.array_equal(c[k], a[k]), k
 
 
+@pytest.mark.parametrize("save_z", [True, False])
+def test_captured_step_replays_the_eager_step(save_z):
+    """A step captured into a CUDA graph and replayed on new inputs gives, bit
+    for bit, what the eager step gives on those inputs; the profiled capture's
+    per-kernel event pairs are readable after a replay."""
+    case = inputs.LinearCase("graph", 2048, 2048, 256, 256, 3, 4096, 0.005, "bf16", 804)
+    inp = inputs.make_linear_inputs(case)
+    dev = torch.device("cuda")
+    lay = TransformedLinear(inp["W0"].to(dev), inp["theta_P"], inp["theta_R"], inp["perm_in"],
+                            inp["perm_out"], case.b_in, case.b_out, case.n, T_max=case.T,
+                            save_z=save_z)
+    x, dy = inp["x"].to(dev), inp["dy"].to(dev)
+    y = torch.empty(case.T, case.d_out, dtype=torch.bfloat16, device=dev)
+    dX = torch.empty(case.T, case.d_in, dtype=torch.bfloat16, device=dev)
+    graph = lay.capture_step(x, dy, y, dX)
+    gen = torch.Generator(device=dev).manual_seed(5)
+    x2 = torch.randn(case.T, case.d_in, generator=gen, device=dev).to(torch.bfloat16)
+    dy2 = torch.randn(case.T, case.d_out, generator=gen, device=dev).to(torch.bfloat16)
+    ye, dXe, dtpe, dtre = [t.clone() for t in lay.step(x2, dy2)]
+    x.copy_(x2)
+    dy.copy_(dy2)
+    graph.replay()
+    _lib.poetx_stream_status()
+    torch.cuda.synchronize()
+    assert torch.equal(y, ye) and torch.equal(dX, dXe)
+    assert torch.equal(lay.dtheta_P, dtpe) and torch.equal(lay.dtheta_R, dtre)
+    _lib.poetx_profile_report()
+    _lib.poetx_profile_enable(True)
+    try:
+        pg = lay.capture_step(x, dy, y, dX, warm=False)
+    finally:
+        _lib.poetx_profile_enable(False)
+    pg.replay()
+    torch.cuda.synchronize()
+    rep = _lib.poetx_profile_report()
+    assert "tc_gemm_nt" in rep and all(v[1] > 0 for v in rep.values()), rep
+
+
 def test_zero_tokens_is_a_no_op_with_zero_gradients():
     case = inputs.LinearCase("empty", 256, 256, 32, 32, 3, 0, 0.01, "f32", 802)
     inp = inputs.make_linear_inputs(case, T=0)
