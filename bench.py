@@ -82,6 +82,7 @@ def kernel_work(case):
         "tc_cluster_gather": ("hbm", blk_flops, blk_bytes),
         "tc_cluster_scatter": ("hbm", blk_flops, blk_bytes),
         "tc_dq": ("hbm", dq_flops, dq_bytes),
+        "tc_cluster_dq": ("hbm", dq_flops, dq_bytes),
         "tc_permute_cols": ("hbm", 0.0, es * (T * di + T * do)),
         "tc_cnp_unpack": ("hbm", 0.0, 4 * npk + 2 * nbb),
         "tc_cnp_fwd": ("tensor", 2 * cnp_f, 2 * nbb + 2 * nbb),

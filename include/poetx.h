@@ -188,10 +188,11 @@ poetx_status poetx_backward(const void *x, const void *dy, const void *W0m, cons
  * device array of POETX_NOALLOC_WORKSPACE_BYTES inside the library.  The
  * caller still owns x, the weights, y and z_save.  This call allocates no
  * device memory.
- *   - Sizes for which poetx_workspace_bytes(T, d_in, d_out, b_in, b_out,
- *     act_dtype) exceeds POETX_NOALLOC_WORKSPACE_BYTES are rejected with
- *     POETX_ERR_SHAPE before anything is launched (e.g. T up to about 2300
- *     tokens for d_in = d_out = 2048 in bf16).
+ *   - Sizes whose forward scratch (the forward's part of
+ *     poetx_workspace_bytes(T, d_in, d_out, b_in, b_out, act_dtype)) exceeds
+ *     POETX_NOALLOC_WORKSPACE_BYTES are rejected with POETX_ERR_SHAPE before
+ *     anything is launched (e.g. T up to about 2600 tokens for
+ *     d_in = d_out = 2048 in bf16).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture.

@@ -59,12 +59,10 @@ bool tc_cnp_backward(int d_in, int d_out, int b_in, int b_out, poetx_dtype dt) {
          d_in / b_in + d_out / b_out <= 65535;
 }
 
-// dQ partial-sum slots of one side: several only when the tensor-core dQ feeds
-// the tensor-core block backward (which adds them in slot order), else one.
+// dQ partial-sum slots of one side: the tensor-core dQ writes several (the
+// block backward adds them in slot order), the CUDA-core dQ one.
 int dq_slots(int T, int d_in, int d_out, int b_in, int b_out, poetx_dtype dt, bool in_side) {
-  if (!tc_linear_supported(d_in, d_out, b_in, b_out, dt) ||
-      !tc_cnp_backward(d_in, d_out, b_in, b_out, dt))
-    return 1;
+  if (!tc_linear_supported(d_in, d_out, b_in, b_out, dt)) return 1;
   return in_side ? tc_dq_slots(T, d_in, b_in, dt) : tc_dq_slots(T, d_out, b_out, dt);
 }
 
@@ -207,6 +205,17 @@ size_t poetx_workspace_bytes(int T, int d_in, int d_out, int b_in, int b_out, po
   return w.fwd_bytes > w.bwd_bytes ? w.fwd_bytes : w.bwd_bytes;
 }
 
+}  // extern "C"
+
+namespace poetx {
+size_t forward_workspace_bytes(int T, int d_in, int d_out, int b_in, int b_out, poetx_dtype dtype) {
+  if (!valid_dtype(dtype) || !sizes_ok(T, d_in, d_out, b_in, b_out)) return 0;
+  return layout(T, d_in, d_out, b_in, b_out, dtype).fwd_bytes;
+}
+}  // namespace poetx
+
+extern "C" {
+
 // Forward chain into caller buffers; `u` and `z` may live in the workspace.
 static poetx_status forward_chain(const void* x, const void* W0m, const void* Q_P,
                                   const void* Q_R, const int32_t* perm_in, const int32_t* inv_in,
@@ -312,6 +321,8 @@ poetx_status poetx_backward(const void* x, const void* dy, const void* W0m, cons
                                     tc_cnp_ws_offset(T, d_in, d_out, b_in, b_out),
                                 stream));
   } else {
+    POETX_TRY(launch_sum_slots(dqp, w.slots_p, (size_t)d_in * b_in, stream));
+    POETX_TRY(launch_sum_slots(dqr, w.slots_r, (size_t)d_out * b_out, stream));
     POETX_TRY(launch_cnp_bwd_simt(theta_P, dqp, nb_in, b_in, n, dtheta_P, stream));
     POETX_TRY(launch_cnp_bwd_simt(theta_R, dqr, nb_out, b_out, n, dtheta_R, stream));
   }

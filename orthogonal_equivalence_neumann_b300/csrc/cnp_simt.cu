@@ -260,6 +260,26 @@ poetx_status launch_cnp_fwd_simt(const float* theta, int nb, int b, int n, void*
   return check_launch();
 }
 
+namespace {
+__global__ void sum_slots_kernel(float* __restrict__ part, int slots, size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    float acc = part[i];
+    for (int s = 1; s < slots; ++s) acc += part[(size_t)s * n + i];
+    part[i] = acc;
+  }
+}
+}  // namespace
+
+poetx_status launch_sum_slots(float* part, int slots, size_t n, cudaStream_t s) {
+  if (slots <= 1 || n == 0) return POETX_OK;
+  const size_t blocks = (n + 255) / 256;
+  {
+    KernelScope ks_("sum_slots", s);
+    sum_slots_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(part, slots, n);
+  }
+  return check_launch();
+}
+
 poetx_status launch_cnp_bwd_simt(const float* theta, const float* dQ, int nb, int b, int n,
                                  float* dtheta, cudaStream_t s) {
   if (cudaMemsetAsync(dtheta, 0, sizeof(float) * (size_t)nb * (b * (b - 1) / 2), s) != cudaSuccess)

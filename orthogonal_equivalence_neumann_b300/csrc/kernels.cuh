@@ -10,6 +10,8 @@ poetx_status launch_cnp_fwd_simt(const float* theta, int nb, int b, int n, void*
                                  poetx_dtype out_dtype, cudaStream_t s);
 poetx_status launch_cnp_bwd_simt(const float* theta, const float* dQ, int nb, int b, int n,
                                  float* dtheta, cudaStream_t s);
+// part[i] = sum over s < slots of part[s*n + i], added in slot order (dQ partial sums -> dQ).
+poetx_status launch_sum_slots(float* part, int slots, size_t n, cudaStream_t s);
 size_t cnp_fwd_simt_smem(int b);
 size_t cnp_bwd_simt_smem(int b);
 
@@ -20,6 +22,9 @@ poetx_status launch_gemm_simt(const void* A, const void* B, void* C, int M, int 
                               bool b_kmajor, poetx_dtype dt, cudaStream_t s);
 poetx_status launch_dq_simt(const void* G, const void* V, int T, int d, int b, const int32_t* gG,
                             const int32_t* gV, float* dQ, poetx_dtype dt, cudaStream_t s);
+
+// Scratch of poetx_forward alone (poetx_workspace_bytes covers the backward too).
+size_t forward_workspace_bytes(int T, int d_in, int d_out, int b_in, int b_out, poetx_dtype dtype);
 
 // ---- index maps ------------------------------------------------------------------
 poetx_status launch_invert_perm(const int32_t* perm, int32_t* inv, int d, cudaStream_t s);

@@ -19,6 +19,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "kernels.cuh"
 
 namespace {
 
@@ -56,7 +57,7 @@ extern "C" poetx_status poetx_forward_noalloc(const void* x, const void* W0m, co
                                               const int32_t* inv_out, int T, int d_in, int d_out,
                                               int b_in, int b_out, poetx_dtype act_dtype, void* y,
                                               void* z_save, cudaStream_t stream) {
-  const size_t need = poetx_workspace_bytes(T, d_in, d_out, b_in, b_out, act_dtype);
+  const size_t need = poetx::forward_workspace_bytes(T, d_in, d_out, b_in, b_out, act_dtype);
   if (need == 0)  // invalid sizes or dtype: let the forward name the error
     return poetx_forward(x, W0m, Q_P, Q_R, perm_in, inv_in, perm_out, inv_out, T, d_in, d_out,
                          b_in, b_out, act_dtype, y, z_save, nullptr, 0, stream);

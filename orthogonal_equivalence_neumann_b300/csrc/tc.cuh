@@ -48,7 +48,7 @@ poetx_status blockapply_bf16(const void* in, void* out, const void* Q, const int
 // Qop in tensor memory.  `inv` is the inverse of `perm` (gather form only).
 // Scratch: a small exchange ring in `ws` (cluster_apply_workspace_bytes).
 bool cluster_apply_supported(int d, int b, bool scatter);
-size_t cluster_apply_workspace_bytes(int d, int b, bool scatter);
+size_t cluster_apply_workspace_bytes(int T, int d, int b, bool scatter);
 poetx_status cluster_apply_bf16(const void* in, void* out, const void* Q, const int32_t* perm,
                                 const int32_t* inv, int T, int d, int b, bool transpose_q,
                                 bool scatter, void* ws, size_t ws_bytes, cudaStream_t s);
@@ -58,6 +58,16 @@ poetx_status cluster_apply_bf16(const void* in, void* out, const void* Q, const 
 // every slot written (the sum over slots is dQ).  dq_splits gives the count
 // that keeps the GPU busy.
 bool dq_supported(int d, int b);
+// The same sums with the permuted operand gathered in flight through a
+// thread-block cluster (no permuted copy in HBM): P is the activation to be
+// gathered (natural layout), inv the inverse of its gather permutation, Vc the
+// unpermuted operand; gather_a: P gives the rows i (dQ_R), else the columns k
+// (dQ_P).  part: cluster_dq_splits(T, d, b) slots, every one written; T > 0.
+bool cluster_dq_supported(int d, int b);
+int cluster_dq_splits(int T, int d, int b);
+size_t cluster_dq_workspace_bytes(int T, int d, int b);
+poetx_status cluster_dq_bf16(const void* P, const void* Vc, const int32_t* inv, int T, int d, int b,
+                             bool gather_a, float* part, void* ws, size_t ws_bytes, cudaStream_t s);
 int dq_splits(int T, int d, int b);
 poetx_status dq_bf16(const void* G, const void* V, int T, int d, int b, int n_split, float* part,
                      cudaStream_t s);

@@ -37,6 +37,7 @@
 #include "common.cuh"
 #include "profile.cuh"
 #include "tc.cuh"
+#include "tc_exchange.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.cuh"
 
@@ -45,11 +46,11 @@ namespace tc {
 
 namespace {
 
-constexpr int TT = 64;                 // tokens per tile (MMA N)
+using namespace xchg;
+
 constexpr int kCaThreads = 480;        // warp 0 TMA, 1 MMA, 2..9 movers, 10..13 epilogue, 14 loader
-constexpr int kMovers = 256;
 constexpr int kSmemLimit = 232448;
-constexpr int kMaxSlots = 4;           // exchange slots in the workspace ring
+constexpr int kOneCtaSmem = 120 * 1024;
 
 struct CaGeo {
   int C, G, F;        // cluster size, blocks per CTA, features per CTA
@@ -64,16 +65,8 @@ struct CaGeo {
   int smem;
 };
 
-__device__ __forceinline__ void movers_bar() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kMovers) : "memory");
-}
 __device__ __forceinline__ void epi_bar() {
   asm volatile("bar.sync 2, 128;" ::: "memory");
-}
-
-__device__ __forceinline__ uint4 pack8f(const float* v) {
-  return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                    pack_bf16x2(v[6], v[7]));
 }
 
 // Set-up shared by both forms: thread 0 brings the CTA's G blocks of Q into
@@ -131,84 +124,6 @@ __device__ void q_stage_to_tmem(const uint8_t* stage, int G, int transpose_q, ui
   tmem_st_wait();
 }
 
-// Barrier block (uint64 words) shared by both kernels.
-struct Bars {
-  uint64_t* s_full;     // [4] input tile landed (TMA)
-  uint64_t* s_empty;    // [4] input tile consumed
-  uint64_t* x_full;     // [4] every writer has written this CTA's part of an exchange slot
-  uint64_t* x_free;     // [4] every reader has fetched its part of an exchange slot
-  uint64_t* r_full;     // [2] fetched part landed in shared memory
-  uint64_t* r_empty;    // [2] fetched part consumed
-  uint64_t* a_full;     // [2] accumulators ready
-  uint64_t* a_empty;    // [2] accumulators drained
-  uint64_t* q_full;
-  uint32_t* tmem_slot;
-};
-
-__device__ __forceinline__ Bars bars_at(uint8_t* smem) {
-  uint64_t* b = reinterpret_cast<uint64_t*>(smem);
-  Bars r;
-  r.s_full = b;
-  r.s_empty = b + 4;
-  r.x_full = b + 8;
-  r.x_free = b + 12;
-  r.r_full = b + 16;
-  r.r_empty = b + 18;
-  r.a_full = b + 20;
-  r.a_empty = b + 22;
-  r.q_full = b + 24;
-  r.tmem_slot = reinterpret_cast<uint32_t*>(b + 25);
-  return r;
-}
-
-// s_empty arrivals: GATHER = the 256 movers, SCATTER = the MMA commit.
-// r_empty arrivals: GATHER = the MMA commit, SCATTER = one mover.
-__device__ __forceinline__ void init_bars(const Bars& br, int C, uint32_t s_empty_count) {
-  for (int i = 0; i < kMaxSlots; ++i) {
-    mbar_init(br.x_full + i, (uint32_t)C);
-    mbar_init(br.x_free + i, (uint32_t)C);
-    mbar_init(br.s_full + i, 1);
-    mbar_init(br.s_empty + i, s_empty_count);
-  }
-  for (int i = 0; i < 2; ++i) {
-    mbar_init(br.r_full + i, 1);
-    mbar_init(br.r_empty + i, 1);
-    mbar_init(br.a_full + i, 1);
-    mbar_init(br.a_empty + i, 128);
-  }
-  mbar_init(br.q_full, 1);
-  fence_mbar_init();
-}
-
-// The loader warp (one thread): fetches this CTA's part of every exchange
-// slot once all C writers have filled it.
-__device__ __forceinline__ void loader_loop(const Bars& br, const CaGeo& g, uint8_t* rbuf,
-                                            const uint8_t* part0, size_t slot_stride, int cluster_id,
-                                            int n_clusters, int n_tiles, bool& ok, int* err) {
-  for (int it = 0, tile = cluster_id; tile < n_tiles && ok; tile += n_clusters, ++it) {
-    const int r = it % g.NR, x = it % g.NX;
-    if (!(ok = mbar_wait(br.r_empty + r, ((it / g.NR) & 1) ^ 1, err))) break;   // buffer free
-    if (!(ok = mbar_wait_cluster(br.x_full + x, (it / g.NX) & 1, err))) break;  // slot written
-    fence_proxy_async_global();
-    mbar_arrive_expect_tx(br.r_full + r, (uint32_t)g.r_bytes);
-    bulk_load_g2s(rbuf + r * g.r_bytes, part0 + (size_t)x * slot_stride, (uint32_t)g.r_bytes,
-                  br.r_full + r);
-  }
-}
-
-// Remote arrives on barrier `bar` of every CTA of the cluster, one per
-// calling thread: thread `who` (0 <= who < C) signals CTA `who`, so the C
-// arrivals go out in parallel.  `release` orders the memory accesses the
-// caller has made or observed (e.g. through a CTA barrier) before the
-// arrival, cluster-wide; without it the arrival is a pure signal.
-__device__ __forceinline__ void arrive_one(uint64_t* bar, int who, int C, bool release) {
-  if (who < C) {
-    const uint32_t ra = mapa_shared(smem_u32(bar), (uint32_t)who);
-    if (release) mbar_arrive_remote(ra);
-    else mbar_arrive_remote_relaxed(ra);
-  }
-}
-
 // ======================================================================== GATHER_IN
 template <int B>
 __global__ void __launch_bounds__(kCaThreads, 1)
@@ -224,7 +139,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
   const int r_off = s_off + g.NS * g.s_bytes;
   const int o_off = r_off + g.NR * g.r_bytes;
   const Bars br = bars_at(smem);
-  uint32_t* table = reinterpret_cast<uint32_t*>(smem + 256);
+  uint32_t* table = reinterpret_cast<uint32_t*>(smem + kTableOff);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int c = (int)cluster_ctarank();
@@ -232,17 +147,13 @@ __global__ void __launch_bounds__(kCaThreads, 1)
   const int n_clusters = gridDim.x / C;
   const int n_tiles = (T + TT - 1) / TT;
   // exchange ring of this cluster: [slot r][reader CTA q][r_bytes]
+  const int n_it = cluster_iters(cluster_id, n_clusters, n_tiles);
   const size_t slot_stride = (size_t)C * g.r_bytes;
   uint8_t* ring = xchg + (size_t)cluster_id * g.NX * slot_stride;
 
-  if (threadIdx.x == 0) init_bars(br, C, kMovers);
+  if (threadIdx.x == 0) init_bars(br, C, kMovers, 1);
   if (warp == 1) tmem_alloc(br.tmem_slot, (uint32_t)g.tmem_cols);
-  // each owned feature's row: (reader CTA << 24) | byte offset of its row in that CTA's part
-  for (int f = threadIdx.x; f < F; f += blockDim.x) {
-    const int p = __ldg(inv + c * F + f);
-    const int j = p / B, k = p % B;
-    table[f] = ((uint32_t)(j / G) << 24) | (uint32_t)(((j % G) * B + k) * 128);
-  }
+  gather_table<B>(table, inv, c, F, G);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -287,8 +198,8 @@ __global__ void __launch_bounds__(kCaThreads, 1)
   } else if (warp == 14) {
     // ---------------------------------------------------------------- loader
     if (lane == 0)
-      loader_loop(br, g, smem + r_off, ring + (size_t)c * g.r_bytes, slot_stride, cluster_id,
-                  n_clusters, n_tiles, ok, err);
+      loader_loop(br, g.NR, g.NX, g.r_bytes, smem + r_off, ring + (size_t)c * g.r_bytes, slot_stride,
+                  cluster_iters(cluster_id, n_clusters, n_tiles), ok, err);
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
     // The whole warp follows the fetched parts; lanes 1..C tell the writers
@@ -297,7 +208,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
     for (int it = 0, tile = cluster_id; tile < n_tiles && ok; tile += n_clusters, ++it) {
       const int r = it % g.NR, a = it % g.NA;
       if (!(ok = mbar_wait(br.r_full + r, (it / g.NR) & 1, err))) break;
-      if (lane >= 1) arrive_one(br.x_free + it % g.NX, lane - 1, C, false);
+      if (lane >= 1) ack_fetch(br, it, g.NX, n_it, lane - 1, C);
       if (lane == 0) {
         if (!(ok = mbar_wait(br.a_empty + a, ((it / g.NA) & 1) ^ 1, err))) break;
         tc_fence_after();
@@ -327,26 +238,8 @@ __global__ void __launch_bounds__(kCaThreads, 1)
       if (!(ok = mbar_wait(br.s_full + s, (it / g.NS) & 1, err))) break;
       // every reader has fetched this slot's previous contents
       if (!(ok = mbar_wait_cluster(br.x_free + x, ((it / g.NX) & 1) ^ 1, err))) break;
-      const uint8_t* S = smem + s_off + s * g.s_bytes;
-      uint8_t* slot = ring + (size_t)x * slot_stride;
-      for (int f = pt; f < F; f += kMovers) {
-        const uint32_t ent = table[f];
-        const uint32_t roff = ent & 0xFFFFFFu;
-        const uint32_t k7 = (roff >> 7) & 7u;
-        uint8_t* row = slot + (size_t)(ent >> 24) * g.r_bytes + roff;
-#pragma unroll
-        for (int grp = 0; grp < TT / 8; ++grp) {
-          float v[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int tr = grp * 8 + e;
-            const uint32_t off = (uint32_t)((f >> 6) * (TT * 128) + tr * 128 +
-                                            ((((f >> 3) & 7) ^ (tr & 7)) << 4) + (f & 7) * 2);
-            v[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(S + off));
-          }
-          *reinterpret_cast<uint4*>(row + ((((uint32_t)grp) ^ k7) << 4)) = pack8f(v);
-        }
-      }
+      move_gather_rows(smem + s_off + s * g.s_bytes, ring + (size_t)x * slot_stride, table, F,
+                       g.r_bytes, pt);
       mbar_arrive(br.s_empty + s);
       movers_bar();
       // the movers' rows are visible before the hand-off (release, after the barrier)
@@ -407,7 +300,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();   // no CTA leaves while another may still arrive on its barriers
+  cluster_sync();   // no CTA leaves before its cluster is done with the exchange
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, (uint32_t)g.tmem_cols);
@@ -429,17 +322,18 @@ __global__ void __launch_bounds__(kCaThreads, 1)
   const int r_off = s_off + g.NS * g.s_bytes;
   const int st_off = r_off + g.NR * g.r_bytes;
   const Bars br = bars_at(smem);
-  uint32_t* table = reinterpret_cast<uint32_t*>(smem + 256);
+  uint32_t* table = reinterpret_cast<uint32_t*>(smem + kTableOff);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int c = (int)cluster_ctarank();
   const int cluster_id = blockIdx.x / C;
   const int n_clusters = gridDim.x / C;
   const int n_tiles = (T + TT - 1) / TT;
+  const int n_it = cluster_iters(cluster_id, n_clusters, n_tiles);
   const size_t slot_stride = (size_t)C * g.r_bytes;
   uint8_t* ring = xchg + (size_t)cluster_id * g.NX * slot_stride;
 
-  if (threadIdx.x == 0) init_bars(br, C, 1);
+  if (threadIdx.x == 0) init_bars(br, C, 1, 1);
   if (warp == 1) tmem_alloc(br.tmem_slot, (uint32_t)g.tmem_cols);
   // each output feature of the own blocks: (owner CTA << 24) | byte offset of its row there
   for (int e = threadIdx.x; e < G * B; e += blockDim.x) {
@@ -494,8 +388,8 @@ __global__ void __launch_bounds__(kCaThreads, 1)
   } else if (warp == 14) {
     // ---------------------------------------------------------------- loader
     if (lane == 0)
-      loader_loop(br, g, smem + r_off, ring + (size_t)c * g.r_bytes, slot_stride, cluster_id,
-                  n_clusters, n_tiles, ok, err);
+      loader_loop(br, g.NR, g.NX, g.r_bytes, smem + r_off, ring + (size_t)c * g.r_bytes, slot_stride,
+                  cluster_iters(cluster_id, n_clusters, n_tiles), ok, err);
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
@@ -574,7 +468,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
       const int r = it % g.NR;
       uint8_t* ST = smem + st_off + (it % g.NST) * g.st_bytes;
       if (!(ok = mbar_wait(br.r_full + r, (it / g.NR) & 1, err))) break;
-      arrive_one(br.x_free + it % g.NX, pt, C, false);   // this CTA's part has been fetched
+      ack_fetch(br, it, g.NX, n_it, pt, C);   // this CTA's part has been fetched
       if (pt == 0 && pending) {   // the store that last used this staging tile has read it
         if (g.NST > 1) bulk_wait_read1();
         else bulk_wait_read0();
@@ -607,7 +501,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();   // no CTA leaves while another may still arrive on its barriers
+  cluster_sync();   // no CTA leaves before its cluster is done with the exchange
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, (uint32_t)g.tmem_cols);
@@ -654,7 +548,7 @@ bool ca_geometry(int d, int b, bool gather, CaGeo* out) {
       g.st_bytes = TT * g.F * 2;           // token-row staging for the TMA store
     }
     const int table = 4 * (gather ? g.F : g.G * b);
-    g.hdr = (256 + table + 1023) / 1024 * 1024;
+    g.hdr = (kTableOff + table + 1023) / 1024 * 1024;
     const int qstage = g.G * b * b * 2;   // staged in the pipeline buffers before first use
     // deeper input rings first (they hide the HBM latency), then double
     // output staging (the TMA store of one tile overlaps the next)
@@ -669,7 +563,8 @@ bool ca_geometry(int d, int b, bool gather, CaGeo* out) {
         g.NS = NS;
         g.NR = NR;
         g.NST = NST;
-        g.smem = smem;
+        // at most one CTA per SM, so a CTA never waits for another's tensor memory
+        g.smem = smem > kOneCtaSmem ? smem : kOneCtaSmem;
         found = true;
       }
     }
@@ -681,6 +576,42 @@ bool ca_geometry(int d, int b, bool gather, CaGeo* out) {
   return false;
 }
 
+const void* ca_kernel_ptr(int b, bool scatter) {
+  if (scatter) return b == 256 ? (const void*)ca_scatter_kernel<256> : (const void*)ca_scatter_kernel<128>;
+  return b == 256 ? (const void*)ca_gather_kernel<256> : (const void*)ca_gather_kernel<128>;
+}
+
+// Clusters of one launch over T tokens (as many as fit at once, at most one per
+// tile) and the exchange slots of each; false if the kernel cannot be resident.
+bool ca_plan(int T, int b, bool scatter, CaGeo* g, int* clusters) {
+  const void* kern = ca_kernel_ptr(b, scatter);
+  if (set_max_dynamic_smem(kern, g->smem) != cudaSuccess ||
+      (g->C > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)) {
+    cudaGetLastError();
+    return false;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kCaThreads);
+  cfg.dynamicSmemBytes = g->smem;
+  const int sms = device_sm_count();
+  cfg.gridDim = dim3((sms / g->C) * g->C);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = g->C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = max_active_clusters(kern, cfg);
+  if (n > sms / g->C) n = sms / g->C;
+  const int n_tiles = (T + TT - 1) / TT;
+  if (n > n_tiles) n = n_tiles;
+  if (n < 1) return false;
+  *clusters = n;
+  g->NX = ring_slots(n_tiles, n);
+  return true;
+}
+
 }  // namespace
 
 bool cluster_apply_supported(int d, int b, bool scatter) {
@@ -688,11 +619,11 @@ bool cluster_apply_supported(int d, int b, bool scatter) {
   return ca_geometry(d, b, !scatter, &g);
 }
 
-// Exchange ring: at most one cluster per C SMs, NX slots of C parts each.
-size_t cluster_apply_workspace_bytes(int d, int b, bool scatter) {
+// Exchange ring: NX slots of C parts for each cluster of the launch.
+size_t cluster_apply_workspace_bytes(int T, int d, int b, bool scatter) {
   CaGeo g;
-  if (!ca_geometry(d, b, !scatter, &g)) return 0;
-  const int clusters = device_sm_count() / g.C;
+  int clusters = 0;
+  if (T <= 0 || !ca_geometry(d, b, !scatter, &g) || !ca_plan(T, b, scatter, &g, &clusters)) return 0;
   return (size_t)clusters * g.NX * g.C * g.r_bytes;
 }
 
@@ -702,7 +633,9 @@ poetx_status cluster_apply_bf16(const void* in, void* out, const void* Q, const 
   if (T <= 0) return POETX_OK;
   CaGeo g;
   if (!ca_geometry(d, b, !scatter, &g)) return POETX_ERR_UNSUPPORTED;
-  if (!ws || ws_bytes < cluster_apply_workspace_bytes(d, b, scatter) ||
+  int clusters = 0;
+  if (!ca_plan(T, b, scatter, &g, &clusters)) return POETX_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < (size_t)clusters * g.NX * g.C * g.r_bytes ||
       (reinterpret_cast<uintptr_t>(ws) & 255))
     return POETX_ERR_SHAPE;
   CUtensorMap tin, tout, tq;
@@ -713,16 +646,8 @@ poetx_status cluster_apply_bf16(const void* in, void* out, const void* Q, const 
       !make_tmap_2d(&tq, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d, (uint64_t)b, 64, 64,
                     CU_TENSOR_MAP_SWIZZLE_128B))
     return POETX_ERR_CUDA;
-  const void* kern;
-  if (scatter)
-    kern = b == 256 ? (const void*)ca_scatter_kernel<256> : (const void*)ca_scatter_kernel<128>;
-  else
-    kern = b == 256 ? (const void*)ca_gather_kernel<256> : (const void*)ca_gather_kernel<128>;
-  if (set_max_dynamic_smem(kern, g.smem) != cudaSuccess) return check_launch();
-  if (g.C > 8 &&
-      cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-    return check_launch();
   cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(clusters * g.C);
   cfg.blockDim = dim3(kCaThreads);
   cfg.dynamicSmemBytes = g.smem;
   cfg.stream = s;
@@ -733,16 +658,6 @@ poetx_status cluster_apply_bf16(const void* in, void* out, const void* Q, const 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // as many clusters as can be resident at once (persistent), but no more than
-  // tiles, nor than the exchange ring was sized for
-  const int sms = device_sm_count();
-  cfg.gridDim = dim3((sms / g.C) * g.C);
-  const int active = max_active_clusters(kern, cfg);
-  if (active < 1) return POETX_ERR_UNSUPPORTED;
-  const int n_tiles = (T + TT - 1) / TT;
-  int clusters = active < n_tiles ? active : n_tiles;
-  if (clusters > sms / g.C) clusters = sms / g.C;
-  cfg.gridDim = dim3(clusters * g.C);
   int* err = device_error_word();
   const int tqf = transpose_q ? 1 : 0;
   uint8_t* xchg = static_cast<uint8_t*>(ws);

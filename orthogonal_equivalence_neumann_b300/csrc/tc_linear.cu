@@ -5,8 +5,9 @@
 //   u = gather(x, perm_in) . B_P^T,  z = u . W0m^T,  y = scatter(z . B_R^T, perm_out)
 // and its backward.  The frozen-weight products run on tcgen05 (tc_gemm.cu),
 // so do the permuted block-diagonal applies (tc_blockapply.cu) for b in
-// {128, 256}, and so do the dQ token sums (tc_dq.cu); other block sizes use
-// the CUDA-core kernels.
+// {128, 256}, and so do the dQ token sums (tc_cluster_dq.cu, which gathers
+// the permuted operand in flight; tc_permute.cu + tc_dq.cu where the cluster
+// form does not fit); other block sizes use the CUDA-core kernels.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tc.cuh"
@@ -35,28 +36,40 @@ bool tc_linear_supported(int d_in, int d_out, int b_in, int b_out, poetx_dtype d
 }
 
 // Tensor-core scratch.  Forward: the exchange ring of the cluster block
-// applies.  Backward: one region that serves, in turn, the exchange ring of
-// the block applies and the gathered activation [T, max(d_in, d_out)] of the
-// dQ token sums (dy by perm_out, then x by perm_in); after it, the dense bf16
-// K and G of every block (CNP backward).
-static bool dq_tc(int d, int b) { return tc::dq_supported(d, b) && tc::permute_supported(d); }
+// applies.  Backward: one region that serves, in turn, the exchange rings of
+// the block applies and of the dQ token sums (or, where the cluster dQ does
+// not fit, a gathered activation [T, max(d_in, d_out)]); after it, the dense
+// bf16 K and G of every block (CNP backward).
+static bool dq_cluster(int T, int d, int b) {
+  return tc::cluster_dq_supported(d, b) && tc::cluster_dq_splits(T, d, b) > 0;
+}
+static bool dq_tc(int T, int d, int b) {
+  return dq_cluster(T, d, b) || (tc::dq_supported(d, b) && tc::permute_supported(d));
+}
 
-static size_t ring_bytes(int d, int b, bool scatter) {
-  return tc::cluster_apply_supported(d, b, scatter) ? tc::cluster_apply_workspace_bytes(d, b, scatter)
+static size_t ring_bytes(int T, int d, int b, bool scatter) {
+  return tc::cluster_apply_supported(d, b, scatter) ? tc::cluster_apply_workspace_bytes(T, d, b, scatter)
                                                     : 0;
 }
 
 static size_t shared_region_bytes(int T, int d_in, int d_out, int b_in, int b_out, bool backward) {
   // the backward may also run the forward applies (z recomputed without a saved copy)
   size_t bytes = 0;
-  const size_t rings[4] = {ring_bytes(d_in, b_in, false), ring_bytes(d_out, b_out, true),
-                           backward ? ring_bytes(d_out, b_out, false) : 0,
-                           backward ? ring_bytes(d_in, b_in, true) : 0};
+  const size_t rings[4] = {ring_bytes(T, d_in, b_in, false), ring_bytes(T, d_out, b_out, true),
+                           backward ? ring_bytes(T, d_out, b_out, false) : 0,
+                           backward ? ring_bytes(T, d_in, b_in, true) : 0};
   for (size_t r : rings)
     if (r > bytes) bytes = r;
-  if (backward && (dq_tc(d_in, b_in) || dq_tc(d_out, b_out))) {
-    const size_t g = (size_t)T * (d_in > d_out ? d_in : d_out) * 2;
-    if (g > bytes) bytes = g;
+  if (backward) {
+    const int ds[2] = {d_in, d_out}, bs[2] = {b_in, b_out};
+    for (int i = 0; i < 2; ++i) {
+      size_t need = 0;
+      if (dq_cluster(T, ds[i], bs[i]))
+        need = tc::cluster_dq_workspace_bytes(T, ds[i], bs[i]);
+      else if (dq_tc(T, ds[i], bs[i]))
+        need = (size_t)T * ds[i] * 2;
+      if (need > bytes) bytes = need;
+    }
   }
   return round_up(bytes, 256);
 }
@@ -71,7 +84,8 @@ size_t tc_workspace_bytes(int T, int d_in, int d_out, int b_in, int b_out, poetx
 }
 
 int tc_dq_slots(int T, int d, int b, poetx_dtype dt) {
-  return (dt == POETX_BF16 && dq_tc(d, b)) ? tc::dq_splits(T, d, b) : 1;
+  if (dt != POETX_BF16 || !dq_tc(T, d, b)) return 1;
+  return dq_cluster(T, d, b) ? tc::cluster_dq_splits(T, d, b) : tc::dq_splits(T, d, b);
 }
 
 // Offset of the CNP backward's part of the tensor-core scratch.
@@ -88,23 +102,30 @@ static poetx_status block_apply(const void* in, void* out, const void* Q, int T,
   const bool scatter = scat != nullptr;
   if (tc::cluster_apply_supported(d, b, scatter))
     return tc::cluster_apply_bf16(in, out, Q, scatter ? scat : gath, inv, T, d, b, transpose_q,
-                                  scatter, ws, tc::cluster_apply_workspace_bytes(d, b, scatter), s);
+                                  scatter, ws, tc::cluster_apply_workspace_bytes(T, d, b, scatter), s);
   if (tc::blockapply_supported(d, b))
     return tc::blockapply_bf16(in, out, Q, gath ? gath : scat, T, d, b, transpose_q, scatter, s);
   return launch_block_apply_simt(in, out, Q, T, d, b, gath, scat, transpose_q, POETX_BF16, s);
 }
 
-// dQ token sums: gather once, then tensor cores, when the shape allows; CUDA cores otherwise.
-// `slots` partial sums on the tensor-core path (each written whole), one plain sum otherwise.
+// dQ token sums as `slots` partial sums on the tensor cores (the permuted
+// operand gathered through the cluster exchange, or gathered once into the
+// scratch where that does not fit); one plain sum on the CUDA cores otherwise.
+// gG / gV: the gather permutation of G or V (one of them), iG / iV its inverse.
 static poetx_status dq(const void* G, const void* V, int T, int d, int b, const int32_t* gG,
-                       const int32_t* gV, float* out, int slots, void* gbuf, cudaStream_t s) {
-  if (dq_tc(d, b)) {
+                       const int32_t* iG, const int32_t* gV, const int32_t* iV, float* out,
+                       int slots, void* ws, size_t ws_bytes, cudaStream_t s) {
+  if (dq_cluster(T, d, b)) {
+    if (gG) return tc::cluster_dq_bf16(G, V, iG, T, d, b, true, out, ws, ws_bytes, s);
+    return tc::cluster_dq_bf16(V, G, iV, T, d, b, false, out, ws, ws_bytes, s);
+  }
+  if (dq_tc(T, d, b)) {
     if (gG) {
-      TC_TRY(tc::permute_cols_bf16(G, gbuf, gG, T, d, s));
-      return tc::dq_bf16(gbuf, V, T, d, b, slots, out, s);
+      TC_TRY(tc::permute_cols_bf16(G, ws, gG, T, d, s));
+      return tc::dq_bf16(ws, V, T, d, b, slots, out, s);
     }
-    TC_TRY(tc::permute_cols_bf16(V, gbuf, gV, T, d, s));
-    return tc::dq_bf16(G, gbuf, T, d, b, slots, out, s);
+    TC_TRY(tc::permute_cols_bf16(V, ws, gV, T, d, s));
+    return tc::dq_bf16(G, ws, T, d, b, slots, out, s);
   }
   return launch_dq_simt(G, V, T, d, b, gG, gV, out, POETX_BF16, s);
 }
@@ -126,10 +147,11 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
                          void* gu, float* dqp, int slots_p, float* dqr, int slots_r, void* ws,
                          cudaStream_t s) {
   TC_TRY(block_apply(dy, gz, Q_R, T, d_out, b_out, perm_out, inv_out, nullptr, true, ws, s));
-  TC_TRY(dq(dy, z, T, d_out, b_out, perm_out, nullptr, dqr, slots_r, ws, s));
+  const size_t shared = shared_region_bytes(T, d_in, d_out, b_in, b_out, true);
+  TC_TRY(dq(dy, z, T, d_out, b_out, perm_out, inv_out, nullptr, nullptr, dqr, slots_r, ws, shared, s));
   TC_TRY(tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s));
   TC_TRY(block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, nullptr, perm_in, true, ws, s));
-  TC_TRY(dq(gu, x, T, d_in, b_in, nullptr, perm_in, dqp, slots_p, ws, s));
+  TC_TRY(dq(gu, x, T, d_in, b_in, nullptr, nullptr, perm_in, inv_in, dqp, slots_p, ws, shared, s));
   return POETX_OK;
 }
 

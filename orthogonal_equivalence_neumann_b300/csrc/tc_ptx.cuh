@@ -115,11 +115,14 @@ __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t remote_bar) 
                : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+// Non-blocking test of a barrier that other CTAs of the cluster arrive on.
+// (A blocking try_wait may stay suspended for a while after a remote arrive
+// completes the phase; polling sees the completion at once.)
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.b32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
@@ -130,7 +133,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
 // As mbar_wait, for barriers that other CTAs of the cluster arrive on.
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int* err) {
   for (uint32_t i = 0; i < kWaitLimit; ++i)
-    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (mbar_test_wait_cluster(bar, parity)) return true;
   raise_device_error(err, POETX_ERR_TIMEOUT);
   return false;
 }

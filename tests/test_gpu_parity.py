@@ -219,9 +219,10 @@ def test_layer_bf16_tiles_and_ragged_tail(b_in, b_out, T):
 @pytest.mark.parametrize("b", [256, 128])
 def test_bf16_step_runs_on_the_tensor_core_kernels(b):
     """The 2048-wide bf16 layer takes the sm_103a paths: cluster block applies,
-    tcgen05 GEMMs, TMA-fed dQ sums and the tensor-core Cayley-Neumann kernels
-    (a silent fall-back to the slab or CUDA-core kernels would still pass the
-    parity tests, so the launched kernels are checked by name)."""
+    tcgen05 GEMMs, cluster dQ sums (the permuted operand gathered in flight, no
+    permuted copy written) and the tensor-core Cayley-Neumann kernels (a silent
+    fall-back to the slab, permute-then-sum or CUDA-core kernels would still
+    pass the parity tests, so the launched kernels are checked by name)."""
     case = inputs.LinearCase("paths_%d" % b, 2048, 2048, b, b, 3, 256, 0.005, "bf16", 990 + b)
     inp = inputs.make_linear_inputs(case)
     lay = TransformedLinear(inp["W0"].cuda(), inp["theta_P"], inp["theta_R"], inp["perm_in"],
@@ -237,10 +238,11 @@ def test_bf16_step_runs_on_the_tensor_core_kernels(b):
     finally:
         _lib.poetx_profile_enable(False)
     names = set(_lib.poetx_profile_report())
-    for k in ("tc_cluster_gather", "tc_cluster_scatter", "tc_gemm_nt", "tc_gemm_nn", "tc_dq",
-              "tc_cnp_fwd", "tc_cnp_bwd"):
+    for k in ("tc_cluster_gather", "tc_cluster_scatter", "tc_gemm_nt", "tc_gemm_nn",
+              "tc_cluster_dq", "tc_cnp_fwd", "tc_cnp_bwd"):
         assert k in names, (k, sorted(names))
     assert not any(n.endswith("_simt") for n in names), sorted(names)
+    assert "tc_permute_cols" not in names and "tc_dq" not in names, sorted(names)
 
 
 def test_xfast_and_xmem_give_the_same_gradients():
