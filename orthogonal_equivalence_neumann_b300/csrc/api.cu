@@ -294,10 +294,17 @@ poetx_status poetx_backward(const void* x, const void* dy, const void* W0m, cons
     z = zr;
   }
   const poetx_dtype dt = act_dtype;
+  // [§2.D] backward of the Cayley-Neumann blocks: on the bf16 tensor-core path
+  // it runs inside tc_backward (bf16 operands; the R side overlapping the g_u
+  // GEMM); the fp32 layer uses the exact CUDA-core kernel per side
+  const bool tc_cnp = tc_cnp_backward(d_in, d_out, b_in, b_out, dt);
   if (tc_linear_supported(d_in, d_out, b_in, b_out, dt)) {
+    TcCnpBwd cnp{theta_P, theta_R, n, dtheta_P, dtheta_R,
+                     static_cast<char*>(tc_ws) + tc_cnp_ws_offset(T, d_in, d_out, b_in, b_out)};
     POETX_TRY(tc_backward(x, dy, W0m, Q_P, Q_R, z, perm_in, inv_in, perm_out, inv_out, T, d_in,
                           d_out, b_in, b_out, dX, gz, gu, dqp, w.slots_p, dqr, w.slots_r, tc_ws,
-                          stream));
+                          tc_cnp ? &cnp : nullptr, stream));
+    if (tc_cnp) return POETX_OK;
   } else {
     // g_z = gather(dy, perm_out) . B_R
     POETX_TRY(launch_block_apply_simt(dy, gz, Q_R, T, d_out, b_out, perm_out, nullptr, true, dt, stream));
@@ -310,13 +317,9 @@ poetx_status poetx_backward(const void* x, const void* dy, const void* W0m, cons
     // dQ_P,j = sum_t g_u,j^T gather(x)_j
     POETX_TRY(launch_dq_simt(gu, x, T, d_in, b_in, nullptr, perm_in, dqp, dt, stream));
   }
-  // [§2.D] backward of the Cayley-Neumann blocks: the bf16 layer runs both sides
-  // in one tensor-core launch (bf16 operands), the fp32 layer the exact
-  // CUDA-core kernel per side
-  if (tc_cnp_backward(d_in, d_out, b_in, b_out, dt)) {
+  if (tc_cnp) {
     POETX_TRY(tc::cnp_bwd_layer(theta_P, dqp, w.slots_p, nb_in, b_in, theta_R, dqr, w.slots_r,
-                                nb_out, b_out, n,
-                                dtheta_P, dtheta_R,
+                                nb_out, b_out, n, dtheta_P, dtheta_R,
                                 static_cast<char*>(tc_ws) +
                                     tc_cnp_ws_offset(T, d_in, d_out, b_in, b_out),
                                 stream));

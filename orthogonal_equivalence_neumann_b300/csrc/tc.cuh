@@ -21,19 +21,31 @@ poetx_status tc_forward(const void* x, const void* W0m, const void* Q_P, const v
                         const int32_t* perm_in, const int32_t* inv_in, const int32_t* perm_out,
                         const int32_t* inv_out, int T, int d_in, int d_out, int b_in, int b_out,
                         void* u, void* z, void* y, void* ws, cudaStream_t s);
+// The Cayley-Neumann backward of both sides, when tc_backward runs it too.
+struct TcCnpBwd {
+  const float* theta_P;
+  const float* theta_R;
+  int n;
+  float* dtheta_P;
+  float* dtheta_R;
+  void* ws;   // cnp_bwd_workspace_bytes(d_in, b_in, d_out, b_out)
+};
+// With `cnp`, the R side's block backward runs on a library stream as soon as
+// dQ_R is summed, next to the g_u GEMM, and joins `s` before the call returns.
 poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const void* Q_P,
                          const void* Q_R, const void* z, const int32_t* perm_in,
                          const int32_t* inv_in, const int32_t* perm_out, const int32_t* inv_out,
                          int T, int d_in, int d_out, int b_in, int b_out, void* dX, void* gz,
                          void* gu, float* dqp, int slots_p, float* dqr, int slots_r, void* ws,
-                         cudaStream_t s);
+                         const TcCnpBwd* cnp, cudaStream_t s);
 
 namespace tc {
 // C[M,N] (bf16) = A[M,K] . B^T with A [M,K] and B [N,K] (b_mn == false) or
 // B [K,N] (b_mn == true), all bf16 row-major, fp32 accumulation (tcgen05).
 bool gemm_supported(int N, int K);
+// reserve_sms: SMs to leave to kernels on another stream.
 poetx_status gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, bool b_mn,
-                       cudaStream_t s);
+                       cudaStream_t s, int reserve_sms = 0);
 
 // Permuted block-diagonal apply, bf16 in/out, fp32 accumulation (tcgen05):
 //   scatter == false: out[t][jb+i] = sum_k Qop_j[i][k] in[t][perm[jb+k]]
@@ -88,6 +100,12 @@ poetx_status cnp_fwd_pair_bf16ops(const float* theta0, int nb0, const float* the
 // Backward of both sides of a layer in one launch (after a prep kernel that
 // writes dense bf16 K and G into `ws`, cnp_bwd_workspace_bytes of it).
 size_t cnp_bwd_workspace_bytes(int d_in, int b_in, int d_out, int b_out);
+// One side alone (its workspace part: 10 * nb * b * b bytes, the P side's at
+// the start of the CNP backward workspace, the R side's after it); the chain
+// kernel takes cnp_bwd_ctas(nb, b) CTAs.
+poetx_status cnp_bwd_side(const float* theta, const float* dQ, int splits, int nb, int b, int n,
+                          float* dtheta, void* ws, cudaStream_t s);
+int cnp_bwd_ctas(int nb, int b);
 // dQ_P / dQ_R come as `splits_P` / `splits_R` partial-sum slots [splits][nb, b, b].
 poetx_status cnp_bwd_layer(const float* theta_P, const float* dQ_P, int splits_P, int nb_P, int b_P,
                            const float* theta_R, const float* dQ_R, int splits_R, int nb_R, int b_R,

@@ -48,7 +48,7 @@ namespace {
 
 using namespace xchg;
 
-constexpr int kCaThreads = 480;        // warp 0 TMA, 1 MMA, 2..9 movers, 10..13 epilogue, 14 loader
+constexpr int kCaThreads = 512;        // warp 0 TMA, 1 MMA, 2..9 movers, 10..13 epilogue, 14 loader, 15 signals
 constexpr int kSmemLimit = 232448;
 constexpr int kOneCtaSmem = 120 * 1024;
 
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
   const size_t slot_stride = (size_t)C * g.r_bytes;
   uint8_t* ring = xchg + (size_t)cluster_id * g.NX * slot_stride;
 
-  if (threadIdx.x == 0) init_bars(br, C, kMovers, 1);
+  if (threadIdx.x == 0) init_bars(br, C, kMovers, 1, kMovers);
   if (warp == 1) tmem_alloc(br.tmem_slot, (uint32_t)g.tmem_cols);
   gather_table<B>(table, inv, c, F, G);
   tc_fence_before();
@@ -200,6 +200,9 @@ __global__ void __launch_bounds__(kCaThreads, 1)
     if (lane == 0)
       loader_loop(br, g.NR, g.NX, g.r_bytes, smem + r_off, ring + (size_t)c * g.r_bytes, slot_stride,
                   cluster_iters(cluster_id, n_clusters, n_tiles), ok, err);
+  } else if (warp == 15) {
+    // ---------------------------------------------------------------- signals to the readers
+    signal_loop(br, g.NX, cluster_iters(cluster_id, n_clusters, n_tiles), C, lane, ok, err);
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
     // The whole warp follows the fetched parts; lanes 1..C tell the writers
@@ -241,9 +244,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
       move_gather_rows(smem + s_off + s * g.s_bytes, ring + (size_t)x * slot_stride, table, F,
                        g.r_bytes, pt);
       mbar_arrive(br.s_empty + s);
-      movers_bar();
-      // the movers' rows are visible before the hand-off (release, after the barrier)
-      arrive_one(br.x_full + x, pt, C, true);
+      mbar_arrive(br.moved + x);   // the loader warp signals the readers
     }
   } else {
     // ---------------------------------------------------------------- epilogue
@@ -272,18 +273,17 @@ __global__ void __launch_bounds__(kCaThreads, 1)
           const uint32_t fu = (uint32_t)((f & 63) >> 3);
           const uint32_t tacc = acc0 + (uint32_t)(((a * G + jj) * halves + h) * TT) +
                                 ((uint32_t)(quarter * 32) << 16);
+          // both 32-token halves in flight before one wait
+          uint32_t rr[2][32];
+          tmem_ld32(tacc, rr[0]);
+          tmem_ld32(tacc + 32u, rr[1]);
+          tmem_ld_wait();
+          tmem_regs_ready(rr[0]);
+          tmem_regs_ready(rr[1]);
 #pragma unroll
-          for (int cc = 0; cc < TT; cc += 32) {
-            uint32_t rr[32];
-            tmem_ld32(tacc + (uint32_t)cc, rr);
-            tmem_ld_wait();
-#pragma unroll
-            for (int t = 0; t < 32; ++t) {
-              const int tr = cc + t;
-              *reinterpret_cast<__nv_bfloat16*>(col + tr * 128 + ((fu ^ (uint32_t)(tr & 7)) << 4)) =
-                  __float2bfloat16_rn(__uint_as_float(rr[t]));
-            }
-          }
+          for (int tr = 0; tr < TT; ++tr)
+            *reinterpret_cast<__nv_bfloat16*>(col + tr * 128 + ((fu ^ (uint32_t)(tr & 7)) << 4)) =
+                __float2bfloat16_rn(__uint_as_float(rr[tr >> 5][tr & 31]));
         }
       tc_fence_before();
       mbar_arrive(br.a_empty + a);   // the accumulators may be refilled
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
   const size_t slot_stride = (size_t)C * g.r_bytes;
   uint8_t* ring = xchg + (size_t)cluster_id * g.NX * slot_stride;
 
-  if (threadIdx.x == 0) init_bars(br, C, 1, 1);
+  if (threadIdx.x == 0) init_bars(br, C, 1, 1, 128);
   if (warp == 1) tmem_alloc(br.tmem_slot, (uint32_t)g.tmem_cols);
   // each output feature of the own blocks: (owner CTA << 24) | byte offset of its row there
   for (int e = threadIdx.x; e < G * B; e += blockDim.x) {
@@ -390,6 +390,9 @@ __global__ void __launch_bounds__(kCaThreads, 1)
     if (lane == 0)
       loader_loop(br, g.NR, g.NX, g.r_bytes, smem + r_off, ring + (size_t)c * g.r_bytes, slot_stride,
                   cluster_iters(cluster_id, n_clusters, n_tiles), ok, err);
+  } else if (warp == 15) {
+    // ---------------------------------------------------------------- signals to the readers
+    signal_loop(br, g.NX, cluster_iters(cluster_id, n_clusters, n_tiles), C, lane, ok, err);
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
@@ -437,28 +440,26 @@ __global__ void __launch_bounds__(kCaThreads, 1)
           uint8_t* row = slot + (size_t)(ent >> 24) * g.r_bytes + roff;
           const uint32_t tacc = acc0 + (uint32_t)(((a * G + jj) * halves + h) * TT) +
                                 ((uint32_t)(quarter * 32) << 16);
+          // both 32-token halves in flight before one wait
+          uint32_t rr[2][32];
+          tmem_ld32(tacc, rr[0]);
+          tmem_ld32(tacc + 32u, rr[1]);
+          tmem_ld_wait();
+          tmem_regs_ready(rr[0]);
+          tmem_regs_ready(rr[1]);
 #pragma unroll
-          for (int cc = 0; cc < TT; cc += 32) {
-            uint32_t rr[32];
-            tmem_ld32(tacc + (uint32_t)cc, rr);
-            tmem_ld_wait();
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const uint32_t grp = (uint32_t)(cc / 8 + u);
-              const uint4 v = make_uint4(
-                  pack_bf16x2(__uint_as_float(rr[8 * u + 0]), __uint_as_float(rr[8 * u + 1])),
-                  pack_bf16x2(__uint_as_float(rr[8 * u + 2]), __uint_as_float(rr[8 * u + 3])),
-                  pack_bf16x2(__uint_as_float(rr[8 * u + 4]), __uint_as_float(rr[8 * u + 5])),
-                  pack_bf16x2(__uint_as_float(rr[8 * u + 6]), __uint_as_float(rr[8 * u + 7])));
-              *reinterpret_cast<uint4*>(row + ((grp ^ f7) << 4)) = v;
-            }
+          for (int grp = 0; grp < TT / 8; ++grp) {
+            const uint32_t* q = &rr[grp >> 2][(grp & 3) * 8];
+            const uint4 v = make_uint4(pack_bf16x2(__uint_as_float(q[0]), __uint_as_float(q[1])),
+                                       pack_bf16x2(__uint_as_float(q[2]), __uint_as_float(q[3])),
+                                       pack_bf16x2(__uint_as_float(q[4]), __uint_as_float(q[5])),
+                                       pack_bf16x2(__uint_as_float(q[6]), __uint_as_float(q[7])));
+            *reinterpret_cast<uint4*>(row + ((((uint32_t)grp) ^ f7) << 4)) = v;
           }
         }
       tc_fence_before();
       mbar_arrive(br.a_empty + a);
-      epi_bar();
-      // the epilogue's rows are visible before the hand-off (release, after the barrier)
-      arrive_one(br.x_full + x, et, C, true);
+      mbar_arrive(br.moved + x);   // the loader warp signals the readers
     }
   } else {
     // ---------------------------------------------------------------- movers: fetched features -> token rows

@@ -28,6 +28,7 @@
 //   warps 2-9   movers: feature rows into the exchange ring
 //   warps 10-13 epilogue: TMEM -> partial slot, 128-byte rows via shared memory
 //   warp 14     loader: fetches this CTA's part of each exchange slot
+//   warp 15     signals the readers when this CTA's rows of a slot are stored
 #include "common.cuh"
 #include "profile.cuh"
 #include "tc.cuh"
@@ -42,7 +43,7 @@ namespace {
 
 using namespace xchg;
 
-constexpr int kDqThreads = 480;
+constexpr int kDqThreads = 512;
 constexpr int kSmemLimit = 232448;
 constexpr int kPitch = 33;   // fp32 pitch of the 32 x 32 transpose tiles
 constexpr int kOneCtaSmem = 120 * 1024;
@@ -83,7 +84,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   const size_t slot_stride = (size_t)C * g.r_bytes;
   uint8_t* ring = xring + (size_t)cluster_id * g.NX * slot_stride;
 
-  if (threadIdx.x == 0) init_bars(br, C, kMovers, 1);
+  if (threadIdx.x == 0) init_bars(br, C, kMovers, 1, kMovers);
   if (warp == 1) tmem_alloc(br.tmem_slot, (uint32_t)g.tmem_cols);
   gather_table<B>(table, inv, c, F, G);
   tc_fence_before();
@@ -118,6 +119,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     if (lane == 0)
       loader_loop(br, g.NR, g.NX, g.r_bytes, smem + r_off, ring + (size_t)c * g.r_bytes, slot_stride,
                   n_it, ok, err);
+  } else if (warp == 15) {
+    // ---------------------------------------------------------------- signals to the readers
+    signal_loop(br, g.NX, n_it, C, lane, ok, err);
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
     const uint32_t idesc = idesc_bf16(128, B, !GATHER_A, GATHER_A);
@@ -164,9 +168,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       move_gather_rows(smem + s_off + s * g.s_bytes, ring + (size_t)x * slot_stride, table, F,
                        g.r_bytes, pt);
       mbar_arrive(br.s_empty + s);
-      movers_bar();
-      // the movers' rows are visible before the hand-off (release, after the barrier)
-      arrive_one(br.x_full + x, pt, C, true);
+      mbar_arrive(br.moved + x);   // the loader warp signals the readers
     }
   } else {
     // ---------------------------------------------------------------- epilogue

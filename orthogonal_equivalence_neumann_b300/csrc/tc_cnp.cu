@@ -335,11 +335,22 @@ __global__ void __launch_bounds__(kPrepThreads)
   const size_t slot4 = (size_t)sd.nb * B * B / 4;
   uint4* gd = reinterpret_cast<uint4*>(sd.Gd + ((size_t)j * B + c0) * B);
   for (int u = threadIdx.x; u < kPrepRows * B / 8; u += kPrepThreads) {
-    float4 a = __ldg(g4 + 2 * u), c = __ldg(g4 + 2 * u + 1);
-    for (int p = 1; p < sd.n_part; ++p) {
-      const float4 a2 = __ldg(g4 + p * slot4 + 2 * u), c2 = __ldg(g4 + p * slot4 + 2 * u + 1);
-      a.x += a2.x; a.y += a2.y; a.z += a2.z; a.w += a2.w;
-      c.x += c2.x; c.y += c2.y; c.z += c2.z; c.w += c2.w;
+    // slots added in order 0, 1, ...; up to 8 slots' loads in flight at a time
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), c = a;
+    for (int p0 = 0; p0 < sd.n_part; p0 += 8) {
+      float4 va[8], vc[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (p0 + q < sd.n_part) {
+          va[q] = __ldg(g4 + (p0 + q) * slot4 + 2 * u);
+          vc[q] = __ldg(g4 + (p0 + q) * slot4 + 2 * u + 1);
+        }
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (p0 + q < sd.n_part) {
+          a.x += va[q].x; a.y += va[q].y; a.z += va[q].z; a.w += va[q].w;
+          c.x += vc[q].x; c.y += vc[q].y; c.z += vc[q].z; c.w += vc[q].w;
+        }
     }
     gd[u] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(c.x, c.y),
                        pack_bf16x2(c.z, c.w));
@@ -743,6 +754,16 @@ Side carve(const float* theta, const float* dQ, int n_part, float* dtheta, int n
 }
 
 }  // namespace
+
+poetx_status cnp_bwd_side(const float* theta, const float* dQ, int splits, int nb, int b, int n,
+                          float* dtheta, void* ws, cudaStream_t s) {
+  if (!cnp_supported(b) || n < 1 || nb > 65535 || splits < 1) return POETX_ERR_UNSUPPORTED;
+  if (nb <= 0) return POETX_OK;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  return cnp_bwd_one(carve(theta, dQ, splits, dtheta, nb, b, w), b, n, s);
+}
+
+int cnp_bwd_ctas(int nb, int b) { return nb * (b / 128); }
 
 poetx_status cnp_bwd_layer(const float* theta_P, const float* dQ_P, int splits_P, int nb_P, int b_P,
                            const float* theta_R, const float* dQ_R, int splits_R, int nb_R, int b_R,

@@ -11,8 +11,11 @@
 // the workspace (a few MB, rewritten every few microseconds, so it stays in
 // L2), and the CTA that needs it fetches its whole part of the slot with one
 // bulk copy.  Hand-offs are cluster mbarriers (waited on by polling):
-//   x_full[slot] of the reader: C remote arrivals, one per writer, released
-//                               after the writer's rows are stored;
+//   x_full[slot] of the reader: C remote arrivals, one per writer CTA,
+//                               released by its loader warp once the CTA's
+//                               writers have stored their rows (a local
+//                               barrier, so the writers never wait on the
+//                               release);
 //   x_free[slot] of the writer: C remote arrivals, one per reader, after the
 //                               reader's bulk copy of its part has landed --
 //                               sent only for slots that will be written
@@ -28,7 +31,7 @@ namespace poetx {
 namespace tc {
 namespace xchg {
 
-constexpr int TT = 64;          // tokens per tile
+constexpr int TT = 64;          // tokens per tile (the epilogues hold a tile row in two 32-wide TMEM loads)
 constexpr int kMovers = 256;    // threads that write feature rows (warps 2..9)
 constexpr int kMaxSlots = 8;    // exchange slots in the workspace ring (at most)
 constexpr int kTableOff = 512;  // routing table, after the barrier block
@@ -55,6 +58,7 @@ struct Bars {
   uint64_t* q_full;     // [1] one-time operand staged (Q blocks; the dQ sums)
   uint64_t* v_full;     // [2] second, unpermuted operand landed (TMA)
   uint64_t* v_empty;    // [2] second operand consumed
+  uint64_t* moved;      // [8] this CTA's writers have stored their rows of an exchange slot
   uint32_t* tmem_slot;
 };
 
@@ -72,17 +76,19 @@ __device__ __forceinline__ Bars bars_at(uint8_t* smem) {
   r.q_full = b + 32;
   r.v_full = b + 33;
   r.v_empty = b + 35;
-  r.tmem_slot = reinterpret_cast<uint32_t*>(b + 37);
+  r.moved = b + 37;
+  r.tmem_slot = reinterpret_cast<uint32_t*>(b + 45);
   return r;
 }
 
 // s_empty arrivals: the movers (GATHER side) or an MMA commit (SCATTER side);
-// r_empty: an MMA commit or one mover.
+// r_empty: an MMA commit or one mover; moved: every thread that writes rows.
 __device__ __forceinline__ void init_bars(const Bars& br, int C, uint32_t s_empty_count,
-                                          uint32_t r_empty_count) {
+                                          uint32_t r_empty_count, uint32_t writers) {
   for (int i = 0; i < kMaxSlots; ++i) {
     mbar_init(br.x_full + i, (uint32_t)C);
     mbar_init(br.x_free + i, (uint32_t)C);
+    mbar_init(br.moved + i, writers);
   }
   for (int i = 0; i < 4; ++i) {
     mbar_init(br.s_full + i, 1);
@@ -119,7 +125,7 @@ __device__ __forceinline__ int cluster_iters(int cluster_id, int n_clusters, int
 }
 
 // The loader (one thread): fetches this CTA's part of every exchange slot
-// once all C writers have filled it.
+// once all C writers have signalled it.
 __device__ __forceinline__ void loader_loop(const Bars& br, int NR, int NX, int r_bytes, uint8_t* rbuf,
                                             const uint8_t* part0, size_t slot_stride, int n_it,
                                             bool& ok, int* err) {
@@ -131,6 +137,22 @@ __device__ __forceinline__ void loader_loop(const Bars& br, int NR, int NX, int 
     mbar_arrive_expect_tx(br.r_full + r, (uint32_t)r_bytes);
     bulk_load_g2s(rbuf + r * r_bytes, part0 + (size_t)x * slot_stride, (uint32_t)r_bytes,
                   br.r_full + r);
+  }
+}
+
+// The signalling warp (all 32 lanes call this): for every iteration, lanes
+// 0..C-1 wait until this CTA's writers have stored their rows of the slot
+// (local barrier `moved`) and then signal the C readers with a remote arrive
+// on x_full, released at cluster scope (which carries the writers' stores the
+// lane has observed).  The writers never wait for the release themselves.
+__device__ __forceinline__ void signal_loop(const Bars& br, int NX, int n_it, int C, int lane,
+                                            bool& ok, int* err) {
+  for (int it = 0; it < n_it && ok; ++it) {
+    const int x = it % NX;
+    bool lok = true;
+    if (lane < C && (lok = mbar_wait(br.moved + x, (it / NX) & 1, err)))
+      arrive_one(br.x_full + x, lane, C, true);
+    ok = __all_sync(0xffffffffu, lok);   // the lanes leave together
   }
 }
 

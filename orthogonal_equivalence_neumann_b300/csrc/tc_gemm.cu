@@ -177,7 +177,7 @@ bool gemm_supported(int N, int K) { return N % BN == 0 && K % BK == 0 && N > 0 &
 
 // C[M,N] = A[M,K] . B^T; B is [N,K] (b_mn == false) or [K,N] (b_mn == true), all bf16 row-major.
 poetx_status gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, bool b_mn,
-                       cudaStream_t s) {
+                       cudaStream_t s, int reserve_sms) {
   if (M <= 0) return POETX_OK;
   if (!gemm_supported(N, K)) return POETX_ERR_UNSUPPORTED;
   CUtensorMap ta, tb;
@@ -190,8 +190,13 @@ poetx_status gemm_bf16(const void* A, const void* B, void* C, int M, int N, int 
            : make_tmap_2d(&tb, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)N, (uint64_t)K, BN,
                           BK, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!okb) return POETX_ERR_CUDA;
+  // as few CTAs as give the fewest rounds of tiles (the SMs left over stay free
+  // for work on another stream), never more than the SMs not reserved
   const int tiles = ((M + BM - 1) / BM) * (N / BN);
-  const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
+  int avail = device_sm_count() - (reserve_sms > 0 ? reserve_sms : 0);
+  if (avail < 1) avail = 1;
+  const int rounds = (tiles + avail - 1) / avail;
+  const int grid = (tiles + rounds - 1) / rounds;
   set_max_dynamic_smem((const void*)gemm_bf16_kernel, SMEM_BYTES);
   {
     KernelScope ks_(b_mn ? "tc_gemm_nn" : "tc_gemm_nt", s);

@@ -8,6 +8,8 @@
 // {128, 256}, and so do the dQ token sums (tc_cluster_dq.cu, which gathers
 // the permuted operand in flight; tc_permute.cu + tc_dq.cu where the cluster
 // form does not fit); other block sizes use the CUDA-core kernels.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tc.cuh"
@@ -140,19 +142,83 @@ poetx_status tc_forward(const void* x, const void* W0m, const void* Q_P, const v
   return POETX_OK;
 }
 
+// A second stream per device for work that overlaps the main chain, with the
+// two events of a fork and a join; calls that use it hold the mutex while they
+// enqueue, so forks and joins of concurrent callers do not interleave.
+namespace {
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxSideDevices = 64;
+std::mutex g_side_mu;
+SideStream g_side[kMaxSideDevices];
+
+SideStream* side_stream() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxSideDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  SideStream& ss = g_side[dev];
+  if (!ss.stream) {
+    if (cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      ss = SideStream{};
+      return nullptr;
+    }
+  }
+  return &ss;
+}
+}  // namespace
+
 poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const void* Q_P,
                          const void* Q_R, const void* z, const int32_t* perm_in,
                          const int32_t* inv_in, const int32_t* perm_out, const int32_t* inv_out,
                          int T, int d_in, int d_out, int b_in, int b_out, void* dX, void* gz,
                          void* gu, float* dqp, int slots_p, float* dqr, int slots_r, void* ws,
-                         cudaStream_t s) {
-  TC_TRY(block_apply(dy, gz, Q_R, T, d_out, b_out, perm_out, inv_out, nullptr, true, ws, s));
+                         const TcCnpBwd* cnp, cudaStream_t s) {
   const size_t shared = shared_region_bytes(T, d_in, d_out, b_in, b_out, true);
+  const int nb_in = d_in / b_in, nb_out = d_out / b_out;
+  TC_TRY(block_apply(dy, gz, Q_R, T, d_out, b_out, perm_out, inv_out, nullptr, true, ws, s));
   TC_TRY(dq(dy, z, T, d_out, b_out, perm_out, inv_out, nullptr, nullptr, dqr, slots_r, ws, shared, s));
-  TC_TRY(tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s));
-  TC_TRY(block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, nullptr, perm_in, true, ws, s));
-  TC_TRY(dq(gu, x, T, d_in, b_in, nullptr, nullptr, perm_in, inv_in, dqp, slots_p, ws, shared, s));
-  return POETX_OK;
+  std::unique_lock<std::mutex> lk(g_side_mu, std::defer_lock);
+  SideStream* side = nullptr;
+  int reserve = 0;
+  uint8_t* cnp_ws = cnp ? static_cast<uint8_t*>(cnp->ws) : nullptr;
+  uint8_t* cnp_ws_r = cnp_ws ? cnp_ws + 10 * (size_t)d_in * b_in : nullptr;
+  if (cnp) {
+    lk.lock();
+    side = side_stream();
+    const int ctas = tc::cnp_bwd_ctas(nb_out, b_out);
+    if (side && 2 * ctas <= device_sm_count()) {
+      // dQ_R is complete: its block backward overlaps the g_u GEMM
+      if (cudaEventRecord(side->fork, s) != cudaSuccess ||
+          cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
+        return check_launch();
+      TC_TRY(tc::cnp_bwd_side(cnp->theta_R, dqr, slots_r, nb_out, b_out, cnp->n, cnp->dtheta_R,
+                              cnp_ws_r, side->stream));
+      if (cudaEventRecord(side->join, side->stream) != cudaSuccess) return check_launch();
+      reserve = ctas;
+    } else {
+      side = nullptr;
+      lk.unlock();
+      TC_TRY(tc::cnp_bwd_side(cnp->theta_R, dqr, slots_r, nb_out, b_out, cnp->n, cnp->dtheta_R,
+                              cnp_ws_r, s));
+    }
+  }
+  poetx_status st = tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s, reserve);
+  if (st == POETX_OK)
+    st = block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, nullptr, perm_in, true, ws, s);
+  if (st == POETX_OK)
+    st = dq(gu, x, T, d_in, b_in, nullptr, nullptr, perm_in, inv_in, dqp, slots_p, ws, shared, s);
+  if (st == POETX_OK && cnp)
+    st = tc::cnp_bwd_side(cnp->theta_P, dqp, slots_p, nb_in, b_in, cnp->n, cnp->dtheta_P, cnp_ws, s);
+  if (side && cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess && st == POETX_OK)
+    st = check_launch();
+  return st;
 }
 
 }  // namespace poetx
