@@ -96,22 +96,40 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA
+    // The two input streams advance independently: whichever ring has a free
+    // stage gets its next tile (bounded: no progress for kWaitLimit polls is
+    // recorded as a timeout).
     if (lane == 0) {
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int tile = cluster_id + it * n_clusters;
-        const int s = it % g.NS, v = it % g.NV;
-        if (!(ok = mbar_wait(br.s_empty + s, ((it / g.NS) & 1) ^ 1, err))) break;
-        mbar_arrive_expect_tx(br.s_full + s, (uint32_t)g.s_bytes);
-        uint8_t* sd = smem + s_off + s * g.s_bytes;
-        for (int q = 0; q < F / 64; ++q)
-          tma_load_2d(sd + q * (TT * 128), &tmP, c * F + q * 64, tile * TT, br.s_full + s);
-        if (!(ok = mbar_wait(br.v_empty + v, ((it / g.NV) & 1) ^ 1, err))) break;
-        mbar_arrive_expect_tx(br.v_full + v, (uint32_t)g.v_bytes);
-        uint8_t* vd = smem + v_off + v * g.v_bytes;
-        for (int jj = 0; jj < G; ++jj)
-          for (int q = 0; q < B / 64; ++q)
-            tma_load_2d(vd + jj * (B * TT * 2) + q * (TT * 128), &tmV, (c * G + jj) * B + q * 64,
-                        tile * TT, br.v_full + v);
+      int is = 0, iv = 0;
+      uint32_t idle = 0;
+      while (ok && (is < n_it || iv < n_it)) {
+        bool moved_on = false;
+        if (is < n_it && mbar_test_wait(br.s_empty + is % g.NS, ((is / g.NS) & 1) ^ 1)) {
+          const int s = is % g.NS, tile = cluster_id + is * n_clusters;
+          mbar_arrive_expect_tx(br.s_full + s, (uint32_t)g.s_bytes);
+          uint8_t* sd = smem + s_off + s * g.s_bytes;
+          for (int q = 0; q < F / 64; ++q)
+            tma_load_2d(sd + q * (TT * 128), &tmP, c * F + q * 64, tile * TT, br.s_full + s);
+          ++is;
+          moved_on = true;
+        }
+        if (iv < n_it && mbar_test_wait(br.v_empty + iv % g.NV, ((iv / g.NV) & 1) ^ 1)) {
+          const int v = iv % g.NV, tile = cluster_id + iv * n_clusters;
+          mbar_arrive_expect_tx(br.v_full + v, (uint32_t)g.v_bytes);
+          uint8_t* vd = smem + v_off + v * g.v_bytes;
+          for (int jj = 0; jj < G; ++jj)
+            for (int q = 0; q < B / 64; ++q)
+              tma_load_2d(vd + jj * (B * TT * 2) + q * (TT * 128), &tmV, (c * G + jj) * B + q * 64,
+                          tile * TT, br.v_full + v);
+          ++iv;
+          moved_on = true;
+        }
+        if (moved_on) {
+          idle = 0;
+        } else if (++idle > kWaitLimit) {
+          raise_device_error(err, POETX_ERR_TIMEOUT);
+          ok = false;
+        }
       }
     }
   } else if (warp == 14) {

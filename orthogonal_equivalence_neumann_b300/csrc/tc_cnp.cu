@@ -278,12 +278,16 @@ struct Side {
 constexpr int kPrepThreads = 256;
 constexpr int kPrepRows = 32;
 
-// Kd[j] = bf16(K_j), Td[j] = -Kd[j], Gd[j] = bf16(dQ_j) for both sides; one
-// CTA per 32-row group of one block.  The group's rows of K are assembled in
-// shared memory (row pitch B + 2 halves, so the column writes fall in
-// distinct banks): entries right of the diagonal come from the packed rows of
-// the group, the ones left of it from the packed rows above, which hold the
-// group's columns contiguously; all loads are issued before their stores.
+// Kd[j] = bf16(K_j), Td[j] = -Kd[j], Gd[j] = bf16(dQ_j) for both sides; CTA
+// (x, y, z) takes the 32-row group x of block y: the z-th quarter of the
+// group's dQ columns (the partial-sum slots added in order), and for z = 0
+// also the group's rows of K, assembled in shared memory (row pitch B + 2
+// halves, so the column writes fall in distinct banks): entries right of the
+// diagonal come from the packed rows of the group, the ones left of it from
+// the packed rows above, which hold the group's columns contiguously.  All
+// loads are issued before their stores.
+constexpr int kPrepZ = 4;
+
 template <int B>
 __global__ void __launch_bounds__(kPrepThreads)
     cnp_prep_kernel(Side s0, Side s1) {
@@ -295,6 +299,37 @@ __global__ void __launch_bounds__(kPrepThreads)
   const int j = second ? (int)blockIdx.y - s0.nb : (int)blockIdx.y;
   const int c0 = blockIdx.x * kPrepRows;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // ---- dQ: rows [c0, c0 + 32), columns of quarter z -> bf16
+  {
+    constexpr int QC = B / kPrepZ;   // columns of the quarter
+    const float4* g4 = reinterpret_cast<const float4*>(sd.dQ + ((size_t)j * B + c0) * B);
+    const size_t slot4 = (size_t)sd.nb * B * B / 4;
+    uint4* gd = reinterpret_cast<uint4*>(sd.Gd + ((size_t)j * B + c0) * B);
+    for (int u = threadIdx.x; u < kPrepRows * QC / 8; u += kPrepThreads) {
+      const int e8 = ((u / (QC / 8)) * B + (int)blockIdx.z * QC + (u % (QC / 8)) * 8) / 8;
+      // slots added in order 0, 1, ...; up to 8 slots' loads in flight at a time
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), c = a;
+      for (int p0 = 0; p0 < sd.n_part; p0 += 8) {
+        float4 va[8], vc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (p0 + q < sd.n_part) {
+            va[q] = __ldg(g4 + (p0 + q) * slot4 + 2 * e8);
+            vc[q] = __ldg(g4 + (p0 + q) * slot4 + 2 * e8 + 1);
+          }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (p0 + q < sd.n_part) {
+            a.x += va[q].x; a.y += va[q].y; a.z += va[q].z; a.w += va[q].w;
+            c.x += vc[q].x; c.y += vc[q].y; c.z += vc[q].z; c.w += vc[q].w;
+          }
+      }
+      gd[e8] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(c.x, c.y),
+                          pack_bf16x2(c.z, c.w));
+    }
+  }
+  if (blockIdx.z != 0) return;
+  // ---- K and K^T rows of the group
   const float* th = sd.theta + (size_t)j * P;
   constexpr int W = kPrepThreads / 32;
 #pragma unroll
@@ -329,31 +364,6 @@ __global__ void __launch_bounds__(kPrepThreads)
         if (k < c) tile[lane * LD + k] = __float2bfloat16_rn(-v[u]);
       }
     }
-  }
-  // dQ rows of the group -> bf16
-  const float4* g4 = reinterpret_cast<const float4*>(sd.dQ + ((size_t)j * B + c0) * B);
-  const size_t slot4 = (size_t)sd.nb * B * B / 4;
-  uint4* gd = reinterpret_cast<uint4*>(sd.Gd + ((size_t)j * B + c0) * B);
-  for (int u = threadIdx.x; u < kPrepRows * B / 8; u += kPrepThreads) {
-    // slots added in order 0, 1, ...; up to 8 slots' loads in flight at a time
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), c = a;
-    for (int p0 = 0; p0 < sd.n_part; p0 += 8) {
-      float4 va[8], vc[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (p0 + q < sd.n_part) {
-          va[q] = __ldg(g4 + (p0 + q) * slot4 + 2 * u);
-          vc[q] = __ldg(g4 + (p0 + q) * slot4 + 2 * u + 1);
-        }
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (p0 + q < sd.n_part) {
-          a.x += va[q].x; a.y += va[q].y; a.z += va[q].z; a.w += va[q].w;
-          c.x += vc[q].x; c.y += vc[q].y; c.z += vc[q].z; c.w += vc[q].w;
-        }
-    }
-    gd[u] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(c.x, c.y),
-                       pack_bf16x2(c.z, c.w));
   }
   __syncthreads();
   uint32_t* kd = reinterpret_cast<uint32_t*>(sd.Kd + ((size_t)j * B + c0) * B);
@@ -679,7 +689,7 @@ poetx_status cnp_bwd_launch(const Side& s0, const Side& s1, int n, cudaStream_t 
   const int nb = s0.nb + s1.nb;
   {
     KernelScope ks_("tc_cnp_bwd_prep", s);
-    cnp_prep_kernel<B><<<dim3(B / kPrepRows, nb), kPrepThreads, 0, s>>>(s0, s1);
+    cnp_prep_kernel<B><<<dim3(B / kPrepRows, nb, kPrepZ), kPrepThreads, 0, s>>>(s0, s1);
   }
   poetx_status st = check_launch();
   if (st != POETX_OK) return st;
