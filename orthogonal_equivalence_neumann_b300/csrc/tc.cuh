@@ -61,9 +61,10 @@ poetx_status blockapply_bf16(const void* in, void* out, const void* Q, const int
 // Scratch: a small exchange ring in `ws` (cluster_apply_workspace_bytes).
 bool cluster_apply_supported(int d, int b, bool scatter);
 size_t cluster_apply_workspace_bytes(int T, int d, int b, bool scatter);
+// max_clusters > 0 caps the clusters of the launch (SMs left to another stream).
 poetx_status cluster_apply_bf16(const void* in, void* out, const void* Q, const int32_t* perm,
                                 const int32_t* inv, int T, int d, int b, bool transpose_q,
-                                bool scatter, void* ws, size_t ws_bytes, cudaStream_t s);
+                                bool scatter, void* ws, size_t ws_bytes, cudaStream_t s, int max_clusters = 0);
 
 // dQ_j[i][k] = sum_t G[t][jb+i] V[t][jb+k] (both operands already gathered),
 // as n_split partial sums over token ranges: part [n_split][d/b, b, b] fp32,
@@ -102,9 +103,10 @@ poetx_status cnp_fwd_pair_bf16ops(const float* theta0, int nb0, const float* the
 size_t cnp_bwd_workspace_bytes(int d_in, int b_in, int d_out, int b_out);
 // One side alone (its workspace part: 10 * nb * b * b bytes, the P side's at
 // the start of the CNP backward workspace, the R side's after it); the chain
-// kernel takes cnp_bwd_ctas(nb, b) CTAs.
+// kernel takes cnp_bwd_ctas(nb, b) CTAs.  parts: 1 = the prep kernel (K, K^T and the
+// summed dQ in bf16), 2 = the chain kernel (after the prep), 3 = both.
 poetx_status cnp_bwd_side(const float* theta, const float* dQ, int splits, int nb, int b, int n,
-                          float* dtheta, void* ws, cudaStream_t s);
+                          float* dtheta, void* ws, cudaStream_t s, int parts = 3);
 int cnp_bwd_ctas(int nb, int b);
 // dQ_P / dQ_R come as `splits_P` / `splits_R` partial-sum slots [splits][nb, b, b].
 poetx_status cnp_bwd_layer(const float* theta_P, const float* dQ_P, int splits_P, int nb_P, int b_P,

@@ -630,12 +630,13 @@ size_t cluster_apply_workspace_bytes(int T, int d, int b, bool scatter) {
 
 poetx_status cluster_apply_bf16(const void* in, void* out, const void* Q, const int32_t* perm,
                                 const int32_t* inv, int T, int d, int b, bool transpose_q,
-                                bool scatter, void* ws, size_t ws_bytes, cudaStream_t s) {
+                                bool scatter, void* ws, size_t ws_bytes, cudaStream_t s, int max_clusters) {
   if (T <= 0) return POETX_OK;
   CaGeo g;
   if (!ca_geometry(d, b, !scatter, &g)) return POETX_ERR_UNSUPPORTED;
   int clusters = 0;
   if (!ca_plan(T, b, scatter, &g, &clusters)) return POETX_ERR_UNSUPPORTED;
+  if (max_clusters > 0 && clusters > max_clusters) clusters = max_clusters;
   if (!ws || ws_bytes < (size_t)clusters * g.NX * g.C * g.r_bytes ||
       (reinterpret_cast<uintptr_t>(ws) & 255))
     return POETX_ERR_SHAPE;

@@ -685,14 +685,16 @@ size_t cnp_bwd_workspace_bytes(int d_in, int b_in, int d_out, int b_out) {
 namespace {
 
 template <int B>
-poetx_status cnp_bwd_launch(const Side& s0, const Side& s1, int n, cudaStream_t s) {
+poetx_status cnp_bwd_launch(const Side& s0, const Side& s1, int n, cudaStream_t s, int parts = 3) {
   const int nb = s0.nb + s1.nb;
-  {
-    KernelScope ks_("tc_cnp_bwd_prep", s);
-    cnp_prep_kernel<B><<<dim3(B / kPrepRows, nb, kPrepZ), kPrepThreads, 0, s>>>(s0, s1);
+  if (parts & 1) {
+    {
+      KernelScope ks_("tc_cnp_bwd_prep", s);
+      cnp_prep_kernel<B><<<dim3(B / kPrepRows, nb, kPrepZ), kPrepThreads, 0, s>>>(s0, s1);
+    }
+    const poetx_status st = check_launch();
+    if (st != POETX_OK || !(parts & 2)) return st;
   }
-  poetx_status st = check_launch();
-  if (st != POETX_OK) return st;
   CUtensorMap tk0, tg0, tt0, tk1, tg1, tt1;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
@@ -739,10 +741,11 @@ poetx_status cnp_bwd_sides(const Side& s0, const Side& s1, int n, cudaStream_t s
   return cnp_bwd_launch<B>(s0, s1, n, s);
 }
 
-poetx_status cnp_bwd_one(const Side& sd, int b, int n, cudaStream_t s) {
+poetx_status cnp_bwd_one(const Side& sd, int b, int n, cudaStream_t s, int parts = 3) {
   Side none = sd;
   none.nb = 0;
-  return b == 256 ? cnp_bwd_launch<256>(sd, none, n, s) : cnp_bwd_launch<128>(sd, none, n, s);
+  return b == 256 ? cnp_bwd_launch<256>(sd, none, n, s, parts)
+                  : cnp_bwd_launch<128>(sd, none, n, s, parts);
 }
 
 // The side's part of the workspace: K, K^T, G (bf16) and dK (fp32) of nb blocks.
@@ -766,11 +769,12 @@ Side carve(const float* theta, const float* dQ, int n_part, float* dtheta, int n
 }  // namespace
 
 poetx_status cnp_bwd_side(const float* theta, const float* dQ, int splits, int nb, int b, int n,
-                          float* dtheta, void* ws, cudaStream_t s) {
-  if (!cnp_supported(b) || n < 1 || nb > 65535 || splits < 1) return POETX_ERR_UNSUPPORTED;
+                          float* dtheta, void* ws, cudaStream_t s, int parts) {
+  if (!cnp_supported(b) || n < 1 || nb > 65535 || splits < 1 || parts < 1 || parts > 3)
+    return POETX_ERR_UNSUPPORTED;
   if (nb <= 0) return POETX_OK;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  return cnp_bwd_one(carve(theta, dQ, splits, dtheta, nb, b, w), b, n, s);
+  return cnp_bwd_one(carve(theta, dQ, splits, dtheta, nb, b, w), b, n, s, parts);
 }
 
 int cnp_bwd_ctas(int nb, int b) { return nb * (b / 128); }

@@ -10,10 +10,7 @@
 //
 // Persistent kernel, one CTA per SM, 128 x 256 output tiles, 64-deep k steps:
 //   warp 0  one thread issues TMA loads of A and B tiles (128-byte swizzle)
-//           into two shared-memory rings that advance independently: 6 stages
-//           of A (the streamed activations, 16 KB each) and 4 of B (the
-//           weight, 32 KB each, mostly L2 hits), so more of the activation
-//           stream is in flight than one joint ring of the same size allows;
+//           into a 4-stage shared-memory ring;
 //   warp 1  allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
 //           and one thread issues tcgen05.mma (M=128, N=256, K=16), freeing
 //           each stage with tcgen05.commit;
@@ -32,10 +29,11 @@ namespace tc {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, SA = 6, SB = 4;
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
-constexpr int SMEM_BYTES = SA * A_BYTES + SB * B_BYTES + 1024 + 256;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 
@@ -46,12 +44,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + SA * A_BYTES;
-  uint64_t* afull = reinterpret_cast<uint64_t*>(sB + SB * B_BYTES);
-  uint64_t* aempty = afull + SA;
-  uint64_t* bfull = aempty + SA;
-  uint64_t* bempty = bfull + SB;
-  uint64_t* tfull = bempty + SB;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
 
@@ -61,13 +57,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int k_iters = K / BK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < SA; ++s) {
-      mbar_init(afull + s, 1);
-      mbar_init(aempty + s, 1);
-    }
-    for (int s = 0; s < SB; ++s) {
-      mbar_init(bfull + s, 1);
-      mbar_init(bempty + s, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull + a, 1);
@@ -80,69 +72,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // the k-blocks this CTA loads, in order: tile t = blockIdx.x + (q / k_iters) * gridDim.x,
-  // k-block q % k_iters
-  const int my_tiles = blockIdx.x < num_tiles ? (num_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-  const int n_loads = my_tiles * k_iters;
 
   if (warp == 0) {
     if (lane == 0) {
-      // A and B advance independently: whichever ring has a free stage gets
-      // its next k-block (no progress for kWaitLimit polls = timeout)
-      int qa = 0, qb = 0;
-      uint32_t idle = 0;
+      int stage = 0;
+      uint32_t phase = 0;
       bool ok = true;
-      while (ok && (qa < n_loads || qb < n_loads)) {
-        bool moved_on = false;
-        if (qa < n_loads && mbar_test_wait(aempty + qa % SA, ((qa / SA) & 1) ^ 1)) {
-          const int tile = blockIdx.x + (qa / k_iters) * gridDim.x, kb = qa % k_iters;
-          const int st = qa % SA;
-          mbar_arrive_expect_tx(afull + st, A_BYTES);
-          tma_load_2d(sA + st * A_BYTES, &tmA, kb * BK, (tile % m_tiles) * BM, afull + st);
-          ++qa;
-          moved_on = true;
-        }
-        if (qb < n_loads && mbar_test_wait(bempty + qb % SB, ((qb / SB) & 1) ^ 1)) {
-          const int tile = blockIdx.x + (qb / k_iters) * gridDim.x, kb = qb % k_iters;
-          const int st = qb % SB, n_blk = tile / m_tiles;
-          mbar_arrive_expect_tx(bfull + st, B_BYTES);
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int m_blk = tile % m_tiles, n_blk = tile / m_tiles;
+        for (int kb = 0; kb < k_iters; ++kb) {
+          if (!(ok = mbar_wait(empty + stage, phase ^ 1, err))) break;
+          mbar_arrive_expect_tx(full + stage, STAGE_BYTES);
+          tma_load_2d(sA + stage * A_BYTES, &tmA, kb * BK, m_blk * BM, full + stage);
           if (!b_mn) {
-            tma_load_2d(sB + st * B_BYTES, &tmB, kb * BK, n_blk * BN, bfull + st);
+            tma_load_2d(sB + stage * B_BYTES, &tmB, kb * BK, n_blk * BN, full + stage);
           } else {
 #pragma unroll
             for (int q = 0; q < BN / 64; ++q)
-              tma_load_2d(sB + st * B_BYTES + q * (BK * 128), &tmB, n_blk * BN + q * 64, kb * BK,
-                          bfull + st);
+              tma_load_2d(sB + stage * B_BYTES + q * (BK * 128), &tmB, n_blk * BN + q * 64,
+                          kb * BK, full + stage);
           }
-          ++qb;
-          moved_on = true;
-        }
-        if (moved_on) {
-          idle = 0;
-        } else if (++idle > kWaitLimit) {
-          raise_device_error(err, POETX_ERR_TIMEOUT);
-          ok = false;
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(BM, BN, false, b_mn != 0);
+      int stage = 0;
+      uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      int q = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
         if (!(ok = mbar_wait(tempty + acc, acc_phase ^ 1, err))) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < k_iters; ++kb, ++q) {
-          const int sa = q % SA, sb = q % SB;
-          if (!(ok = mbar_wait(afull + sa, (q / SA) & 1, err))) break;
-          if (!(ok = mbar_wait(bfull + sb, (q / SB) & 1, err))) break;
+        for (int kb = 0; kb < k_iters; ++kb) {
+          if (!(ok = mbar_wait(full + stage, phase, err))) break;
           tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + sa * A_BYTES);
-          const uint32_t b_base = smem_u32(sB + sb * B_BYTES);
+          const uint32_t a_base = smem_u32(sA + stage * A_BYTES);
+          const uint32_t b_base = smem_u32(sB + stage * B_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t adesc = sw128_desc(a_base + k * 32, 16, 1024);
@@ -150,8 +120,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         : sw128_desc(b_base + k * 32, 16, 1024);
             mma_bf16(d_tmem, adesc, bdesc, idesc, (kb | k) != 0);
           }
-          mma_commit(aempty + sa);
-          mma_commit(bempty + sb);
+          mma_commit(empty + stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         mma_commit(tfull + acc);
         if (++acc == 2) { acc = 0; acc_phase ^= 1; }

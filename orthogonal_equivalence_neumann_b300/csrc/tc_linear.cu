@@ -100,11 +100,12 @@ size_t tc_cnp_ws_offset(int T, int d_in, int d_out, int b_in, int b_out) {
 // inverse of the gather permutation.
 static poetx_status block_apply(const void* in, void* out, const void* Q, int T, int d, int b,
                                 const int32_t* gath, const int32_t* inv, const int32_t* scat,
-                                bool transpose_q, void* ws, cudaStream_t s) {
+                                bool transpose_q, void* ws, cudaStream_t s, int max_clusters = 0) {
   const bool scatter = scat != nullptr;
   if (tc::cluster_apply_supported(d, b, scatter))
     return tc::cluster_apply_bf16(in, out, Q, scatter ? scat : gath, inv, T, d, b, transpose_q,
-                                  scatter, ws, tc::cluster_apply_workspace_bytes(T, d, b, scatter), s);
+                                  scatter, ws, tc::cluster_apply_workspace_bytes(T, d, b, scatter), s,
+                                  max_clusters);
   if (tc::blockapply_supported(d, b))
     return tc::blockapply_bf16(in, out, Q, gath ? gath : scat, T, d, b, transpose_q, scatter, s);
   return launch_block_apply_simt(in, out, Q, T, d, b, gath, scat, transpose_q, POETX_BF16, s);
@@ -184,40 +185,60 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
   const int nb_in = d_in / b_in, nb_out = d_out / b_out;
   TC_TRY(block_apply(dy, gz, Q_R, T, d_out, b_out, perm_out, inv_out, nullptr, true, ws, s));
   TC_TRY(dq(dy, z, T, d_out, b_out, perm_out, inv_out, nullptr, nullptr, dqr, slots_r, ws, shared, s));
-  std::unique_lock<std::mutex> lk(g_side_mu, std::defer_lock);
-  SideStream* side = nullptr;
-  int reserve = 0;
-  uint8_t* cnp_ws = cnp ? static_cast<uint8_t*>(cnp->ws) : nullptr;
-  uint8_t* cnp_ws_r = cnp_ws ? cnp_ws + 10 * (size_t)d_in * b_in : nullptr;
-  if (cnp) {
-    lk.lock();
-    side = side_stream();
-    const int ctas = tc::cnp_bwd_ctas(nb_out, b_out);
-    if (side && 2 * ctas <= device_sm_count()) {
-      // dQ_R is complete: its block backward overlaps the g_u GEMM
-      if (cudaEventRecord(side->fork, s) != cudaSuccess ||
-          cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
-        return check_launch();
-      TC_TRY(tc::cnp_bwd_side(cnp->theta_R, dqr, slots_r, nb_out, b_out, cnp->n, cnp->dtheta_R,
-                              cnp_ws_r, side->stream));
-      if (cudaEventRecord(side->join, side->stream) != cudaSuccess) return check_launch();
-      reserve = ctas;
-    } else {
-      side = nullptr;
-      lk.unlock();
-      TC_TRY(tc::cnp_bwd_side(cnp->theta_R, dqr, slots_r, nb_out, b_out, cnp->n, cnp->dtheta_R,
-                              cnp_ws_r, s));
-    }
+  if (!cnp) {
+    TC_TRY(tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s));
+    TC_TRY(block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, nullptr, perm_in, true, ws, s));
+    return dq(gu, x, T, d_in, b_in, nullptr, nullptr, perm_in, inv_in, dqp, slots_p, ws, shared, s);
   }
-  poetx_status st = tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s, reserve);
-  if (st == POETX_OK)
-    st = block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, nullptr, perm_in, true, ws, s);
+  // With the Cayley-Neumann backward: each side's chain kernel runs on a
+  // library stream next to the main chain -- the R side's beside the g_u GEMM
+  // (which leaves it SMs: it takes only the CTAs its tile rounds need), the P
+  // side's beside the dX scatter (which then takes fewer clusters).  The dQ_P
+  // sums come before the dX scatter so that the P side can start early.
+  uint8_t* cnp_ws = static_cast<uint8_t*>(cnp->ws);
+  uint8_t* cnp_ws_r = cnp_ws + 10 * (size_t)d_in * b_in;
+  const int ctas_r = tc::cnp_bwd_ctas(nb_out, b_out), ctas_p = tc::cnp_bwd_ctas(nb_in, b_in);
+  std::unique_lock<std::mutex> lk(g_side_mu);
+  SideStream* side = side_stream();
+  const int sms = device_sm_count();
+  if (!side || 2 * ctas_r > sms || 2 * ctas_p > sms) {
+    // no second stream: everything in order on `s`
+    lk.unlock();
+    TC_TRY(tc::cnp_bwd_side(cnp->theta_R, dqr, slots_r, nb_out, b_out, cnp->n, cnp->dtheta_R,
+                            cnp_ws_r, s));
+    TC_TRY(tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s));
+    TC_TRY(block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, nullptr, perm_in, true, ws, s));
+    TC_TRY(dq(gu, x, T, d_in, b_in, nullptr, nullptr, perm_in, inv_in, dqp, slots_p, ws, shared, s));
+    return tc::cnp_bwd_side(cnp->theta_P, dqp, slots_p, nb_in, b_in, cnp->n, cnp->dtheta_P, cnp_ws, s);
+  }
+  auto fork = [&]() -> poetx_status {
+    if (cudaEventRecord(side->fork, s) != cudaSuccess ||
+        cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
+      return check_launch();
+    return POETX_OK;
+  };
+  // R side: dQ_R is complete
+  TC_TRY(fork());
+  TC_TRY(tc::cnp_bwd_side(cnp->theta_R, dqr, slots_r, nb_out, b_out, cnp->n, cnp->dtheta_R, cnp_ws_r,
+                          side->stream));
+  poetx_status st = tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s, ctas_r);
   if (st == POETX_OK)
     st = dq(gu, x, T, d_in, b_in, nullptr, nullptr, perm_in, inv_in, dqp, slots_p, ws, shared, s);
-  if (st == POETX_OK && cnp)
-    st = tc::cnp_bwd_side(cnp->theta_P, dqp, slots_p, nb_in, b_in, cnp->n, cnp->dtheta_P, cnp_ws, s);
-  if (side && cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess && st == POETX_OK)
-    st = check_launch();
+  // P side: its prep on `s`, its chain next to the dX scatter
+  if (st == POETX_OK)
+    st = tc::cnp_bwd_side(cnp->theta_P, dqp, slots_p, nb_in, b_in, cnp->n, cnp->dtheta_P, cnp_ws, s, 1);
+  if (st == POETX_OK) st = fork();
+  if (st == POETX_OK)
+    st = tc::cnp_bwd_side(cnp->theta_P, dqp, slots_p, nb_in, b_in, cnp->n, cnp->dtheta_P, cnp_ws,
+                          side->stream, 2);
+  if (st == POETX_OK && cudaEventRecord(side->join, side->stream) != cudaSuccess) st = check_launch();
+  if (st == POETX_OK) {
+    // clusters of 8 CTAs that still fit beside the chain kernel's CTAs
+    const int max_clusters = (sms - ctas_p - 16) / 8;
+    st = block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, nullptr, perm_in, true, ws, s,
+                     max_clusters > 1 ? max_clusters : 1);
+  }
+  if (cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess && st == POETX_OK) st = check_launch();
   return st;
 }
 
