@@ -61,6 +61,7 @@ poetx_status blockapply_bf16(const void* in, void* out, const void* Q, const int
 // Scratch: a small exchange ring in `ws` (cluster_apply_workspace_bytes).
 bool cluster_apply_supported(int d, int b, bool scatter);
 size_t cluster_apply_workspace_bytes(int T, int d, int b, bool scatter);
+int cluster_apply_clusters(int T, int d, int b, bool scatter);
 // max_clusters > 0 caps the clusters of the launch (SMs left to another stream).
 poetx_status cluster_apply_bf16(const void* in, void* out, const void* Q, const int32_t* perm,
                                 const int32_t* inv, int T, int d, int b, bool transpose_q,
@@ -75,12 +76,14 @@ bool dq_supported(int d, int b);
 // thread-block cluster (no permuted copy in HBM): P is the activation to be
 // gathered (natural layout), inv the inverse of its gather permutation, Vc the
 // unpermuted operand; gather_a: P gives the rows i (dQ_R), else the columns k
-// (dQ_P).  part: cluster_dq_splits(T, d, b) slots, every one written; T > 0.
+// (dQ_P).  part: cluster_dq_splits(T, d, b) slots (min(that, max_clusters) when
+// max_clusters > 0), every one written; T > 0.
 bool cluster_dq_supported(int d, int b);
 int cluster_dq_splits(int T, int d, int b);
 size_t cluster_dq_workspace_bytes(int T, int d, int b);
 poetx_status cluster_dq_bf16(const void* P, const void* Vc, const int32_t* inv, int T, int d, int b,
-                             bool gather_a, float* part, void* ws, size_t ws_bytes, cudaStream_t s);
+                             bool gather_a, float* part, void* ws, size_t ws_bytes, cudaStream_t s,
+                             int max_clusters = 0);
 int dq_splits(int T, int d, int b);
 poetx_status dq_bf16(const void* G, const void* V, int T, int d, int b, int n_split, float* part,
                      cudaStream_t s);

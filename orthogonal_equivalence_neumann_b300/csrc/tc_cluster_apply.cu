@@ -620,6 +620,14 @@ bool cluster_apply_supported(int d, int b, bool scatter) {
   return ca_geometry(d, b, !scatter, &g);
 }
 
+// Clusters of a launch over T tokens (0 if the cluster form does not apply).
+int cluster_apply_clusters(int T, int d, int b, bool scatter) {
+  CaGeo g;
+  int clusters = 0;
+  if (T <= 0 || !ca_geometry(d, b, !scatter, &g) || !ca_plan(T, b, scatter, &g, &clusters)) return 0;
+  return clusters;
+}
+
 // Exchange ring: NX slots of C parts for each cluster of the launch.
 size_t cluster_apply_workspace_bytes(int T, int d, int b, bool scatter) {
   CaGeo g;

@@ -333,11 +333,12 @@ size_t cluster_dq_workspace_bytes(int T, int d, int b) {
 }
 
 poetx_status cluster_dq_bf16(const void* Pm, const void* Vc, const int32_t* inv, int T, int d, int b,
-                             bool gather_a, float* part, void* ws, size_t ws_bytes, cudaStream_t s) {
+                             bool gather_a, float* part, void* ws, size_t ws_bytes, cudaStream_t s, int max_clusters) {
   DqGeo g;
   if (T <= 0 || !dq_geometry(d, b, &g)) return POETX_ERR_UNSUPPORTED;
-  const int clusters = dq_plan(T, b, &g);
+  int clusters = dq_plan(T, b, &g);
   if (clusters < 1) return POETX_ERR_UNSUPPORTED;
+  if (max_clusters > 0 && clusters > max_clusters) clusters = max_clusters;
   const int nb = d / b;
   if (!ws || ws_bytes < (size_t)clusters * g.NX * g.C * g.r_bytes || (reinterpret_cast<uintptr_t>(ws) & 255))
     return POETX_ERR_SHAPE;

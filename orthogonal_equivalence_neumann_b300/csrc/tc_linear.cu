@@ -54,7 +54,8 @@ static size_t ring_bytes(int T, int d, int b, bool scatter) {
                                                     : 0;
 }
 
-static size_t shared_region_bytes(int T, int d_in, int d_out, int b_in, int b_out, bool backward) {
+// Exchange rings of the block applies (forward, and the backward's g_z and dX).
+static size_t apply_region_bytes(int T, int d_in, int d_out, int b_in, int b_out, bool backward) {
   // the backward may also run the forward applies (z recomputed without a saved copy)
   size_t bytes = 0;
   const size_t rings[4] = {ring_bytes(T, d_in, b_in, false), ring_bytes(T, d_out, b_out, true),
@@ -62,18 +63,28 @@ static size_t shared_region_bytes(int T, int d_in, int d_out, int b_in, int b_ou
                            backward ? ring_bytes(T, d_in, b_in, true) : 0};
   for (size_t r : rings)
     if (r > bytes) bytes = r;
-  if (backward) {
-    const int ds[2] = {d_in, d_out}, bs[2] = {b_in, b_out};
-    for (int i = 0; i < 2; ++i) {
-      size_t need = 0;
-      if (dq_cluster(T, ds[i], bs[i]))
-        need = tc::cluster_dq_workspace_bytes(T, ds[i], bs[i]);
-      else if (dq_tc(T, ds[i], bs[i]))
-        need = (size_t)T * ds[i] * 2;
-      if (need > bytes) bytes = need;
-    }
+  return round_up(bytes, 256);
+}
+
+// The dQ sums' scratch (their exchange ring, or a gathered activation), apart
+// from the applies' so that a dQ sum can run beside an apply.
+static size_t dq_region_bytes(int T, int d_in, int d_out, int b_in, int b_out) {
+  size_t bytes = 0;
+  const int ds[2] = {d_in, d_out}, bs[2] = {b_in, b_out};
+  for (int i = 0; i < 2; ++i) {
+    size_t need = 0;
+    if (dq_cluster(T, ds[i], bs[i]))
+      need = tc::cluster_dq_workspace_bytes(T, ds[i], bs[i]);
+    else if (dq_tc(T, ds[i], bs[i]))
+      need = (size_t)T * ds[i] * 2;
+    if (need > bytes) bytes = need;
   }
   return round_up(bytes, 256);
+}
+
+static size_t shared_region_bytes(int T, int d_in, int d_out, int b_in, int b_out, bool backward) {
+  return apply_region_bytes(T, d_in, d_out, b_in, b_out, backward) +
+         (backward ? dq_region_bytes(T, d_in, d_out, b_in, b_out) : 0);
 }
 
 size_t tc_workspace_bytes(int T, int d_in, int d_out, int b_in, int b_out, poetx_dtype dt,
@@ -115,12 +126,13 @@ static poetx_status block_apply(const void* in, void* out, const void* Q, int T,
 // operand gathered through the cluster exchange, or gathered once into the
 // scratch where that does not fit); one plain sum on the CUDA cores otherwise.
 // gG / gV: the gather permutation of G or V (one of them), iG / iV its inverse.
+// max_clusters > 0 caps the cluster form's clusters, and with them its slots.
 static poetx_status dq(const void* G, const void* V, int T, int d, int b, const int32_t* gG,
                        const int32_t* iG, const int32_t* gV, const int32_t* iV, float* out,
-                       int slots, void* ws, size_t ws_bytes, cudaStream_t s) {
+                       int slots, void* ws, size_t ws_bytes, cudaStream_t s, int max_clusters = 0) {
   if (dq_cluster(T, d, b)) {
-    if (gG) return tc::cluster_dq_bf16(G, V, iG, T, d, b, true, out, ws, ws_bytes, s);
-    return tc::cluster_dq_bf16(V, G, iV, T, d, b, false, out, ws, ws_bytes, s);
+    if (gG) return tc::cluster_dq_bf16(G, V, iG, T, d, b, true, out, ws, ws_bytes, s, max_clusters);
+    return tc::cluster_dq_bf16(V, G, iV, T, d, b, false, out, ws, ws_bytes, s, max_clusters);
   }
   if (dq_tc(T, d, b)) {
     if (gG) {
@@ -181,63 +193,74 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
                          int T, int d_in, int d_out, int b_in, int b_out, void* dX, void* gz,
                          void* gu, float* dqp, int slots_p, float* dqr, int slots_r, void* ws,
                          const TcCnpBwd* cnp, cudaStream_t s) {
-  const size_t shared = shared_region_bytes(T, d_in, d_out, b_in, b_out, true);
+  // the applies' exchange rings first, the dQ sums' scratch after them
+  const size_t apply_bytes = apply_region_bytes(T, d_in, d_out, b_in, b_out, true);
+  const size_t dq_bytes = dq_region_bytes(T, d_in, d_out, b_in, b_out);
+  void* ws_dq = static_cast<uint8_t*>(ws) + apply_bytes;
   const int nb_in = d_in / b_in, nb_out = d_out / b_out;
-  TC_TRY(block_apply(dy, gz, Q_R, T, d_out, b_out, perm_out, inv_out, nullptr, true, ws, s));
-  TC_TRY(dq(dy, z, T, d_out, b_out, perm_out, inv_out, nullptr, nullptr, dqr, slots_r, ws, shared, s));
-  if (!cnp) {
-    TC_TRY(tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s));
-    TC_TRY(block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, nullptr, perm_in, true, ws, s));
-    return dq(gu, x, T, d_in, b_in, nullptr, nullptr, perm_in, inv_in, dqp, slots_p, ws, shared, s);
-  }
-  // With the Cayley-Neumann backward: each side's chain kernel runs on a
-  // library stream next to the main chain -- the R side's beside the g_u GEMM
-  // (which leaves it SMs: it takes only the CTAs its tile rounds need), the P
-  // side's beside the dX scatter (which then takes fewer clusters).  The dQ_P
-  // sums come before the dX scatter so that the P side can start early.
+  auto sequential = [&](cudaStream_t st) -> poetx_status {
+    TC_TRY(block_apply(dy, gz, Q_R, T, d_out, b_out, perm_out, inv_out, nullptr, true, ws, st));
+    TC_TRY(dq(dy, z, T, d_out, b_out, perm_out, inv_out, nullptr, nullptr, dqr, slots_r, ws_dq,
+              dq_bytes, st));
+    TC_TRY(tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, st));
+    TC_TRY(block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, nullptr, perm_in, true, ws, st));
+    return dq(gu, x, T, d_in, b_in, nullptr, nullptr, perm_in, inv_in, dqp, slots_p, ws_dq, dq_bytes, st);
+  };
+  if (!cnp) return sequential(s);
   uint8_t* cnp_ws = static_cast<uint8_t*>(cnp->ws);
   uint8_t* cnp_ws_r = cnp_ws + 10 * (size_t)d_in * b_in;
   const int ctas_r = tc::cnp_bwd_ctas(nb_out, b_out), ctas_p = tc::cnp_bwd_ctas(nb_in, b_in);
+  const int sms = device_sm_count();
+  // Clusters of the two concurrent pairs (g_z beside dQ_R, dX beside dQ_P):
+  // the applies' clusters split between the two kernels of a pair.
+  const int cl_r = tc::cluster_apply_clusters(T, d_out, b_out, false);
+  const int cl_p = tc::cluster_apply_clusters(T, d_in, b_in, true);
+  const bool dq_r = dq_cluster(T, d_out, b_out), dq_p = dq_cluster(T, d_in, b_in);
   std::unique_lock<std::mutex> lk(g_side_mu);
   SideStream* side = side_stream();
-  const int sms = device_sm_count();
-  if (!side || 2 * ctas_r > sms || 2 * ctas_p > sms) {
-    // no second stream: everything in order on `s`
+  if (!side || 2 * ctas_r > sms || 2 * ctas_p > sms || cl_r < 2 || cl_p < 2 || !dq_r || !dq_p) {
+    // no overlap: everything in order on `s`
     lk.unlock();
+    TC_TRY(sequential(s));
     TC_TRY(tc::cnp_bwd_side(cnp->theta_R, dqr, slots_r, nb_out, b_out, cnp->n, cnp->dtheta_R,
                             cnp_ws_r, s));
-    TC_TRY(tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s));
-    TC_TRY(block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, nullptr, perm_in, true, ws, s));
-    TC_TRY(dq(gu, x, T, d_in, b_in, nullptr, nullptr, perm_in, inv_in, dqp, slots_p, ws, shared, s));
     return tc::cnp_bwd_side(cnp->theta_P, dqp, slots_p, nb_in, b_in, cnp->n, cnp->dtheta_P, cnp_ws, s);
   }
+  // Schedule (main = `s`, side = the library stream):
+  //   main: g_z apply      | g_u GEMM (leaves the chain's SMs) | dX apply
+  //   side: dQ_R, R prep + chain                               | dQ_P, P prep + chain
+  // The side stream's dQ sums take the clusters the concurrent apply leaves;
+  // their partial slots are as many as their clusters.
+  const int main_r = (cl_r + 1) / 2, main_p = (cl_p + 1) / 2;
+  const int side_r = cl_r - main_r, side_p = cl_p - main_p;
+  const int used_r = tc::cluster_dq_splits(T, d_out, b_out) < side_r ? tc::cluster_dq_splits(T, d_out, b_out) : side_r;
+  const int used_p = tc::cluster_dq_splits(T, d_in, b_in) < side_p ? tc::cluster_dq_splits(T, d_in, b_in) : side_p;
   auto fork = [&]() -> poetx_status {
     if (cudaEventRecord(side->fork, s) != cudaSuccess ||
         cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
       return check_launch();
     return POETX_OK;
   };
-  // R side: dQ_R is complete
-  TC_TRY(fork());
-  TC_TRY(tc::cnp_bwd_side(cnp->theta_R, dqr, slots_r, nb_out, b_out, cnp->n, cnp->dtheta_R, cnp_ws_r,
-                          side->stream));
-  poetx_status st = tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s, ctas_r);
+  poetx_status st = fork();
   if (st == POETX_OK)
-    st = dq(gu, x, T, d_in, b_in, nullptr, nullptr, perm_in, inv_in, dqp, slots_p, ws, shared, s);
-  // P side: its prep on `s`, its chain next to the dX scatter
+    st = dq(dy, z, T, d_out, b_out, perm_out, inv_out, nullptr, nullptr, dqr, slots_r, ws_dq, dq_bytes,
+            side->stream, side_r);
   if (st == POETX_OK)
-    st = tc::cnp_bwd_side(cnp->theta_P, dqp, slots_p, nb_in, b_in, cnp->n, cnp->dtheta_P, cnp_ws, s, 1);
+    st = tc::cnp_bwd_side(cnp->theta_R, dqr, used_r, nb_out, b_out, cnp->n, cnp->dtheta_R, cnp_ws_r,
+                          side->stream);
+  if (st == POETX_OK)
+    st = block_apply(dy, gz, Q_R, T, d_out, b_out, perm_out, inv_out, nullptr, true, ws, s, main_r);
+  if (st == POETX_OK) st = tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s, ctas_r);
   if (st == POETX_OK) st = fork();
   if (st == POETX_OK)
-    st = tc::cnp_bwd_side(cnp->theta_P, dqp, slots_p, nb_in, b_in, cnp->n, cnp->dtheta_P, cnp_ws,
-                          side->stream, 2);
+    st = dq(gu, x, T, d_in, b_in, nullptr, nullptr, perm_in, inv_in, dqp, slots_p, ws_dq, dq_bytes,
+            side->stream, side_p);
+  if (st == POETX_OK)
+    st = tc::cnp_bwd_side(cnp->theta_P, dqp, used_p, nb_in, b_in, cnp->n, cnp->dtheta_P, cnp_ws,
+                          side->stream);
   if (st == POETX_OK && cudaEventRecord(side->join, side->stream) != cudaSuccess) st = check_launch();
-  if (st == POETX_OK) {
-    // clusters of 8 CTAs that still fit beside the chain kernel's CTAs
-    const int max_clusters = (sms - ctas_p - 16) / 8;
-    st = block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, nullptr, perm_in, true, ws, s,
-                     max_clusters > 1 ? max_clusters : 1);
-  }
+  if (st == POETX_OK)
+    st = block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, nullptr, perm_in, true, ws, s, main_p);
   if (cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess && st == POETX_OK) st = check_launch();
   return st;
 }
