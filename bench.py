@@ -114,6 +114,53 @@ def read_traffic(kernel):
     return None
 
 
+class _CtypesNvml:
+    """The few read-only NVML queries the clock sampler makes, bound with
+    ctypes to the driver's libnvidia-ml when the pynvml module is absent."""
+    NVML_CLOCK_SM = 1
+
+    def __init__(self):
+        import ctypes
+        self._c = ctypes
+        self._lib = ctypes.CDLL("libnvidia-ml.so.1")
+
+    def _check(self, rc, what):
+        if rc != 0:
+            raise RuntimeError("%s returned %d" % (what, rc))
+
+    def nvmlInit(self):
+        self._check(self._lib.nvmlInit_v2(), "nvmlInit_v2")
+
+    def _handle(self, fn, arg):
+        h = self._c.c_void_p()
+        self._check(fn(arg, self._c.byref(h)), fn.__name__)
+        return h
+
+    def nvmlDeviceGetHandleByPciBusId(self, bus):
+        return self._handle(self._lib.nvmlDeviceGetHandleByPciBusId_v2, self._c.c_char_p(bus))
+
+    def nvmlDeviceGetHandleByIndex(self, i):
+        return self._handle(self._lib.nvmlDeviceGetHandleByIndex_v2, self._c.c_uint(i))
+
+    def _clock(self, fn, h, kind):
+        v = self._c.c_uint()
+        self._check(fn(h, self._c.c_int(kind), self._c.byref(v)), fn.__name__)
+        return v.value
+
+    def nvmlDeviceGetClockInfo(self, h, kind):
+        return self._clock(self._lib.nvmlDeviceGetClockInfo, h, kind)
+
+    def nvmlDeviceGetMaxClockInfo(self, h, kind):
+        return self._clock(self._lib.nvmlDeviceGetMaxClockInfo, h, kind)
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h):
+        v = self._c.c_ulonglong()
+        fn = getattr(self._lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self._lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self._check(fn(h, self._c.byref(v)), "clock event reasons")
+        return v.value
+
+
 class ClockSampler:
     """SM clock and clock-event reasons sampled during the timed region.
 
@@ -147,7 +194,10 @@ class ClockSampler:
     def __enter__(self):
         import threading
         try:
-            import pynvml as nv
+            try:
+                import pynvml as nv
+            except ImportError:
+                nv = _CtypesNvml()
             nv.nvmlInit()
             h = None
             try:   # the NVML device of this CUDA device, by PCI address
@@ -481,41 +531,80 @@ def run_poetx(args, world, rank, local):
                             for k, v in prof.items()}}
 
     # ---------------- end to end through host buffers
+    # Every step's inputs come from pinned host memory and every step's results
+    # (y, dX, both skew gradients) go back to it, inside the timed region; as a
+    # training loop would, the copies run on their own streams with two device
+    # buffer sets, so step k's upload and step k-1's download overlap step k's
+    # compute (the compute calls are the public API's, eager).
+    NB = 2
     h_x = [t.cpu().pin_memory() for t in xs[:2]]
     h_dy = [t.cpu().pin_memory() for t in dys[:2]]
-    d_x = torch.empty_like(xs[0])
-    d_dy = torch.empty_like(dys[0])
-    h_y = torch.empty(y.shape, dtype=y.dtype).pin_memory()
-    h_dX = torch.empty(dX.shape, dtype=dX.dtype).pin_memory()
-    h_tp = torch.empty(lay.dtheta_P.shape, dtype=torch.float32).pin_memory()
-    h_tr = torch.empty(lay.dtheta_R.shape, dtype=torch.float32).pin_memory()
+    d_x = [torch.empty_like(xs[0]) for _ in range(NB)]
+    d_dy = [torch.empty_like(dys[0]) for _ in range(NB)]
+    d_y = [torch.empty_like(y) for _ in range(NB)]
+    d_dX = [torch.empty_like(dX) for _ in range(NB)]
+    d_tp = [torch.empty_like(lay.dtheta_P) for _ in range(NB)]
+    d_tr = [torch.empty_like(lay.dtheta_R) for _ in range(NB)]
+    h_y = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _ in range(NB)]
+    h_dX = [torch.empty(dX.shape, dtype=dX.dtype).pin_memory() for _ in range(NB)]
+    h_tp = [torch.empty(lay.dtheta_P.shape, dtype=torch.float32).pin_memory() for _ in range(NB)]
+    h_tr = [torch.empty(lay.dtheta_R.shape, dtype=torch.float32).pin_memory() for _ in range(NB)]
+    copy_in = torch.cuda.Stream(device=dev)
+    copy_out = torch.cuda.Stream(device=dev)
+    in_ready = [torch.cuda.Event() for _ in range(NB)]
+    computed = [torch.cuda.Event() for _ in range(NB)]
+    out_done = [torch.cuda.Event() for _ in range(NB)]
+
+    def upload(k):
+        b = k % NB
+        with torch.cuda.stream(copy_in):
+            copy_in.wait_event(computed[b])       # step k - NB is done with these buffers
+            d_x[b].copy_(h_x[k % 2], non_blocking=True)
+            d_dy[b].copy_(h_dy[k % 2], non_blocking=True)
+            in_ready[b].record(copy_in)
 
     def e2e_step(k):
-        d_x.copy_(h_x[k % 2], non_blocking=True)
-        d_dy.copy_(h_dy[k % 2], non_blocking=True)
-        lay.step(d_x, d_dy, y, dX)
+        b = k % NB
+        stream.wait_event(in_ready[b])
+        stream.wait_event(out_done[b])            # step k - NB's results have left
+        lay.step(d_x[b], d_dy[b], d_y[b], d_dX[b])
         allreduce_grads(lay, world)
-        h_y.copy_(y, non_blocking=True)
-        h_dX.copy_(dX, non_blocking=True)
-        h_tp.copy_(lay.dtheta_P, non_blocking=True)
-        h_tr.copy_(lay.dtheta_R, non_blocking=True)
+        d_tp[b].copy_(lay.dtheta_P, non_blocking=True)
+        d_tr[b].copy_(lay.dtheta_R, non_blocking=True)
+        computed[b].record(stream)
+        with torch.cuda.stream(copy_out):
+            copy_out.wait_event(computed[b])
+            h_y[b].copy_(d_y[b], non_blocking=True)
+            h_dX[b].copy_(d_dX[b], non_blocking=True)
+            h_tp[b].copy_(d_tp[b], non_blocking=True)
+            h_tr[b].copy_(d_tr[b], non_blocking=True)
+            out_done[b].record(copy_out)
 
-    for k in range(2):
-        e2e_step(k)
+    def e2e_run(n):
+        copy_in.wait_stream(stream)
+        upload(0)
+        for k in range(n):
+            if k + 1 < n:
+                upload(k + 1)
+            e2e_step(k)
+        stream.wait_stream(copy_out)
+        stream.wait_stream(copy_in)
+
+    e2e_run(2)
     torch.cuda.synchronize()
     barrier(world)
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
-    for k in range(args.steps):
-        e2e_step(k)
+    e2e_run(args.steps)
     f1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), world)
-    h2d = (d_x.numel() + d_dy.numel()) * 2
-    d2h = (y.numel() + dX.numel()) * 2 + 4 * (h_tp.numel() + h_tr.numel())
+    h2d = (d_x[0].numel() + d_dy[0].numel()) * 2
+    d2h = (y.numel() + dX.numel()) * 2 + 4 * (h_tp[0].numel() + h_tr[0].numel())
     e2e = {"value": world * case.T * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "copies": "pinned host buffers; uploads and downloads on their own streams, double-buffered"}
 
     cnp = cnp_points(dev) if rank == 0 else None
 
