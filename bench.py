@@ -426,6 +426,39 @@ def cnp_points(dev):
     return out
 
 
+def fold_point(lay, dev, peaks):
+    """End-of-inner-loop fold W0_new = R W0 P (poetx_fold_w0) at the layer's
+    shape, into a scratch matrix (the layer is left as it is)."""
+    need = _lib.poetx_fold_workspace_bytes(lay.d_out, lay.d_in, lay.b_in, lay.b_out, lay.dtype)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    out = torch.empty_like(lay.W0m)
+    lay.cayley_neumann()
+
+    def fold():
+        _lib.poetx_fold_w0(lay.W0m, lay.Q_P, lay.Q_R, lay.perm_in, lay.perm_out, lay.b_in,
+                           lay.b_out, out, ws)
+
+    for _ in range(3):
+        fold()
+    reps = 10
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(reps):
+        fold()
+    e1.record()
+    torch.cuda.synchronize()
+    us = 1e3 * e0.elapsed_time(e1) / reps
+    es = lay.W0m.element_size()
+    alg = es * (2 * lay.d_out * lay.d_in + lay.d_in * lay.b_in + lay.d_out * lay.b_out)
+    gbs = alg / (us * 1e-6) / 1e9
+    del ws, out
+    return {"us": round(us, 2), "algorithmic_bytes": alg, "achieved_gbs": round(gbs, 1),
+            "frac": round(gbs / peaks["hbm_gbs"], 4),
+            "passes": "two scattered block applies and two transposes",
+            "note": "the weight and the intermediate fit in L2 at this shape"}
+
+
 def run_poetx(args, world, rank, local):
     dev = torch.device("cuda", local)
     peaks = load_peaks()
@@ -607,6 +640,7 @@ def run_poetx(args, world, rank, local):
            "copies": "pinned host buffers; uploads and downloads on their own streams, double-buffered"}
 
     cnp = cnp_points(dev) if rank == 0 else None
+    fold = fold_point(lay, dev, peaks) if rank == 0 else None
 
     # ---------------- CPU oracle baseline (rank 0, N = 1 only)
     cpu = None
@@ -631,7 +665,7 @@ def run_poetx(args, world, rank, local):
             "data": "synthetic", "config": workload_config(world),
             "step_tflops": round(flops / (ms_per_step * 1e-3) / 1e12 / 1, 2),
             "step_frac_of_bf16_peak": round(flops / (ms_per_step * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-            "cnp_blocks_per_s": cnp, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "cnp_blocks_per_s": cnp, "fold_w0": fold, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(launches), "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)

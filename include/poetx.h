@@ -123,6 +123,29 @@ poetx_status poetx_merge_w0(const void *W0, void *W0m, int d_out, int d_in, poet
                             const int32_t *perm_out, const int32_t *perm_in,
                             cudaStream_t stream);
 
+/* End of an inner loop [§2.B: the permutations are fixed for an inner loop
+ * and merged into the weight; the learned rotations are then folded into the
+ * frozen weight before new permutations are drawn]: the effective weight in
+ * the original coordinates,
+ *   W0_new = R W0 P = Pi_R^T B_R W0m B_P Pi_P,
+ * from the merged W0m = Pi_R W0 Pi_P^T of poetx_merge_w0 and the current
+ * blocks Q_P, Q_R (poetx_cayley_neumann of the current theta).  The caller
+ * then resets theta (to zero: Q = I), draws new permutations and merges
+ * W0_new with them (poetx_merge_w0).
+ * Arguments (device, `dtype` unless stated): W0m [d_out, d_in],
+ *   Q_P [d_in/b_in, b_in, b_in], Q_R [d_out/b_out, b_out, b_out],
+ *   perm_in int32 [d_in], perm_out int32 [d_out] (the permutations W0m was
+ *   merged with), W0_new [d_out, d_in] written (may be W0m itself: the fold
+ *   can run in place), workspace of ws_bytes >= poetx_fold_workspace_bytes.
+ * Two scattered block applies (on the rows of W0m, then on the rows of its
+ * transpose) and two transposes; bf16 runs the applies on the tensor cores
+ * with fp32 accumulation and one bf16 rounding of the intermediate. */
+size_t poetx_fold_workspace_bytes(int d_out, int d_in, int b_in, int b_out, poetx_dtype dtype);
+poetx_status poetx_fold_w0(const void *W0m, const void *Q_P, const void *Q_R,
+                           const int32_t *perm_in, const int32_t *perm_out, int d_out, int d_in,
+                           int b_in, int b_out, poetx_dtype dtype, void *W0_new, void *workspace,
+                           size_t ws_bytes, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* The transformed linear [POET-X §2.A-§2.C, §2.E]                          */
 /* ------------------------------------------------------------------------ */

@@ -167,6 +167,20 @@ def merge_w0(W0, perm_out, perm_in):
     return out
 
 
+def fold_w0(W0, QP, QR, perm_in, perm_out):
+    """[POET-X §2.B] the effective weight R W0 P, written out densely.
+
+    P = Pi_P^T blockdiag(QP) Pi_P and R = Pi_R^T blockdiag(QR) Pi_R, each built
+    from the dense permutation matrix and the dense block-diagonal above; two
+    numpy matmuls in double.  This is what the weight becomes when an inner
+    loop ends and the learned rotations are folded into it."""
+    W0 = _d(W0)
+    Pi_P, Pi_R = perm_matrix(perm_in), perm_matrix(perm_out)
+    P = Pi_P.T @ blockdiag(QP) @ Pi_P
+    R = Pi_R.T @ blockdiag(QR) @ Pi_R
+    return R @ W0 @ P
+
+
 def forward(x, W0, QP, QR, perm_in, perm_out, return_z=False):
     """[POET-X §2.A-§2.C] y = Pi_R^T B_R Pi_R W0 Pi_P^T B_P Pi_P x, token by token.
 

@@ -25,7 +25,8 @@ EXPORTS = ["poetx_status_string", "poetx_version", "poetx_cayley_neumann",
            "poetx_cayley_neumann_backward", "poetx_invert_perm", "poetx_check_perm",
            "poetx_merge_w0", "poetx_workspace_bytes", "poetx_forward", "poetx_backward",
            "poetx_stream_status", "poetx_launch_count", "poetx_profile_enable",
-           "poetx_profile_report", "poetx_forward_noalloc"]
+           "poetx_profile_report", "poetx_forward_noalloc", "poetx_fold_workspace_bytes",
+           "poetx_fold_w0"]
 
 
 class PoetxError(RuntimeError):
@@ -65,6 +66,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "poetx_launch_count": (ctypes.c_ulonglong, []),
         "poetx_profile_enable": (I, [I]),
         "poetx_profile_report": (I, [ctypes.c_char_p, Z]),
+        "poetx_fold_workspace_bytes": (Z, [I, I, I, I, I]),
+        "poetx_fold_w0": (I, [P, P, P, P, P, I, I, I, I, I, P, P, Z, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -153,6 +156,18 @@ def poetx_merge_w0(W0, W0m, perm_out, perm_in, stream=None):
     _check("poetx_merge_w0", load().poetx_merge_w0(
         _ptr(W0), _ptr(W0m), d_out, d_in, dtype_code(W0.dtype), _ptr(perm_out), _ptr(perm_in),
         _stream(stream)))
+
+
+def poetx_fold_workspace_bytes(d_out, d_in, b_in, b_out, dtype) -> int:
+    return int(load().poetx_fold_workspace_bytes(d_out, d_in, b_in, b_out, dtype_code(dtype)))
+
+
+def poetx_fold_w0(W0m, Q_P, Q_R, perm_in, perm_out, b_in, b_out, W0_new, workspace, stream=None):
+    d_out, d_in = W0m.shape
+    _check("poetx_fold_w0", load().poetx_fold_w0(
+        _ptr(W0m), _ptr(Q_P), _ptr(Q_R), _ptr(perm_in), _ptr(perm_out), d_out, d_in, b_in, b_out,
+        dtype_code(W0m.dtype), _ptr(W0_new), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def poetx_workspace_bytes(T, d_in, d_out, b_in, b_out, dtype) -> int:

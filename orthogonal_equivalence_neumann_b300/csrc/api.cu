@@ -199,6 +199,49 @@ poetx_status poetx_merge_w0(const void* W0, void* W0m, int d_out, int d_in, poet
   return launch_merge_w0(W0, W0m, d_out, d_in, dtype, perm_out, perm_in, stream);
 }
 
+// [§2.B] fold at the end of an inner loop: W0_new = Pi_R^T B_R W0m B_P Pi_P.
+// Workspace: one [d_out, d_in] matrix, then (bf16) the exchange ring of the
+// larger of the two scattered applies.
+static size_t fold_ring_bytes(int d_out, int d_in, int b_in, int b_out, poetx_dtype dtype) {
+  if (dtype != POETX_BF16) return 0;
+  const size_t a = tc_scatter_apply_bytes(d_out, d_in, b_in);
+  const size_t b = tc_scatter_apply_bytes(d_in, d_out, b_out);
+  return a > b ? a : b;
+}
+
+size_t poetx_fold_workspace_bytes(int d_out, int d_in, int b_in, int b_out, poetx_dtype dtype) {
+  if (!valid_dtype(dtype) || !sizes_ok(0, d_in, d_out, b_in, b_out)) return 0;
+  return round_up((size_t)d_out * d_in * dtype_size(dtype), 256) +
+         round_up(fold_ring_bytes(d_out, d_in, b_in, b_out, dtype), 256);
+}
+
+poetx_status poetx_fold_w0(const void* W0m, const void* Q_P, const void* Q_R,
+                           const int32_t* perm_in, const int32_t* perm_out, int d_out, int d_in,
+                           int b_in, int b_out, poetx_dtype dtype, void* W0_new, void* workspace,
+                           size_t ws_bytes, cudaStream_t stream) {
+  POETX_TRY(check_linear_args(0, d_in, d_out, b_in, b_out, dtype,
+                              {W0m, Q_P, Q_R, perm_in, perm_out, W0_new, workspace}));
+  if (ws_bytes < poetx_fold_workspace_bytes(d_out, d_in, b_in, b_out, dtype))
+    return POETX_ERR_SHAPE;
+  char* ws = static_cast<char*>(workspace);
+  void* M = ws;   // [d_out, d_in], then [d_in, d_out]
+  void* ring = ws + round_up((size_t)d_out * d_in * dtype_size(dtype), 256);
+  auto scatter_apply = [&](const void* in, void* out, const void* Q, int T, int d, int b,
+                           const int32_t* scat, bool transpose_q) {
+    if (dtype == POETX_BF16)
+      return tc_scatter_apply(in, out, Q, T, d, b, scat, transpose_q, ring, stream);
+    return launch_block_apply_simt(in, out, Q, T, d, b, nullptr, scat, transpose_q, dtype, stream);
+  };
+  // rows of W0m times B_P, columns scattered by perm_in:  M = W0m B_P Pi_P
+  POETX_TRY(scatter_apply(W0m, M, Q_P, d_out, d_in, b_in, perm_in, true));
+  // M^T [d_in, d_out] into W0_new's storage (W0m is no longer read)
+  POETX_TRY(launch_transpose(M, W0_new, d_out, d_in, dtype, stream));
+  // rows of M^T times B_R^T, scattered by perm_out:  (Pi_R^T B_R M)^T = M^T B_R^T Pi_R
+  POETX_TRY(scatter_apply(W0_new, M, Q_R, d_in, d_out, b_out, perm_out, false));
+  // back to [d_out, d_in]
+  return launch_transpose(M, W0_new, d_in, d_out, dtype, stream);
+}
+
 size_t poetx_workspace_bytes(int T, int d_in, int d_out, int b_in, int b_out, poetx_dtype dtype) {
   if (!valid_dtype(dtype) || !sizes_ok(T, d_in, d_out, b_in, b_out)) return 0;
   const Workspace w = layout(T, d_in, d_out, b_in, b_out, dtype);

@@ -30,6 +30,9 @@ size_t forward_workspace_bytes(int T, int d_in, int d_out, int b_in, int b_out, 
 poetx_status launch_invert_perm(const int32_t* perm, int32_t* inv, int d, cudaStream_t s);
 poetx_status launch_check_perm(const int32_t* perm, const int32_t* inv, int d, int32_t* scratch,
                                int32_t* flag_host, cudaStream_t s);
+// out [cols][rows] = in [rows][cols]^T (activation dtype).
+poetx_status launch_transpose(const void* in, void* out, int rows, int cols, poetx_dtype dt,
+                              cudaStream_t s);
 poetx_status launch_merge_w0(const void* W0, void* W0m, int d_out, int d_in, poetx_dtype dt,
                              const int32_t* po, const int32_t* pi, cudaStream_t s);
 

@@ -246,6 +246,29 @@ __global__ void merge_w0_kernel(const T* __restrict__ W0, T* __restrict__ W0m, i
   if (k < d_in) W0m[(size_t)i * d_in + k] = W0[(size_t)__ldg(po + i) * d_in + __ldg(pi + k)];
 }
 
+// ---------------------------------------------------------------- transpose
+// out[c][r] = in[r][c] for in [rows][cols]: one 32 x 32 tile per CTA of
+// 32 x 8 threads, read and written along rows (coalesced) through shared
+// memory (a padded column removes bank conflicts).
+constexpr int kTr = 32;
+
+template <typename T>
+__global__ void __launch_bounds__(kTr * 8) transpose_kernel(const T* __restrict__ in,
+                                                            T* __restrict__ out, int rows,
+                                                            int cols) {
+  __shared__ T tile[kTr][kTr + 1];
+  const int c0 = blockIdx.x * kTr, r0 = blockIdx.y * kTr;
+  for (int k = threadIdx.y; k < kTr; k += 8) {
+    const int r = r0 + k, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) tile[k][threadIdx.x] = in[(size_t)r * cols + c];
+  }
+  __syncthreads();
+  for (int k = threadIdx.y; k < kTr; k += 8) {
+    const int c = c0 + k, r = r0 + threadIdx.x;
+    if (c < cols && r < rows) out[(size_t)c * rows + r] = tile[threadIdx.x][k];
+  }
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- launchers
@@ -381,6 +404,22 @@ poetx_status launch_merge_w0(const void* W0, void* W0m, int d_out, int d_in, poe
       merge_w0_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)W0,
                                                           (__nv_bfloat16*)W0m, d_out, d_in, po, pi);
     }
+  return check_launch();
+}
+
+poetx_status launch_transpose(const void* in, void* out, int rows, int cols, poetx_dtype dt,
+                              cudaStream_t s) {
+  if (rows <= 0 || cols <= 0) return POETX_OK;
+  const dim3 grid((cols + kTr - 1) / kTr, (rows + kTr - 1) / kTr), block(kTr, 8);
+  if (grid.y > 65535) return POETX_ERR_SHAPE;
+  {
+    KernelScope ks_("transpose", s);
+    if (dt == POETX_F32)
+      transpose_kernel<float><<<grid, block, 0, s>>>((const float*)in, (float*)out, rows, cols);
+    else
+      transpose_kernel<__nv_bfloat16><<<grid, block, 0, s>>>((const __nv_bfloat16*)in,
+                                                             (__nv_bfloat16*)out, rows, cols);
+  }
   return check_launch();
 }
 

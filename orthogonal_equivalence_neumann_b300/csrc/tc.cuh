@@ -21,6 +21,12 @@ poetx_status tc_forward(const void* x, const void* W0m, const void* Q_P, const v
                         const int32_t* perm_in, const int32_t* inv_in, const int32_t* perm_out,
                         const int32_t* inv_out, int T, int d_in, int d_out, int b_in, int b_out,
                         void* u, void* z, void* y, void* ws, cudaStream_t s);
+// One scattered block apply of bf16 rows on the fastest kernel that takes the
+// shape: out[t][scat(jb + i)] = sum_k Qop_j[i][k] in[t][jb + k], Qop = Q or
+// (transpose_q) Q^T.  `ws` holds tc_scatter_apply_bytes(T, d, b).
+size_t tc_scatter_apply_bytes(int T, int d, int b);
+poetx_status tc_scatter_apply(const void* in, void* out, const void* Q, int T, int d, int b,
+                              const int32_t* scat, bool transpose_q, void* ws, cudaStream_t s);
 // The Cayley-Neumann backward of both sides, when tc_backward runs it too.
 struct TcCnpBwd {
   const float* theta_P;

@@ -155,6 +155,13 @@ poetx_status tc_forward(const void* x, const void* W0m, const void* Q_P, const v
   return POETX_OK;
 }
 
+size_t tc_scatter_apply_bytes(int T, int d, int b) { return ring_bytes(T, d, b, true); }
+
+poetx_status tc_scatter_apply(const void* in, void* out, const void* Q, int T, int d, int b,
+                              const int32_t* scat, bool transpose_q, void* ws, cudaStream_t s) {
+  return block_apply(in, out, Q, T, d, b, nullptr, nullptr, scat, transpose_q, ws, s);
+}
+
 // A second stream per device for work that overlaps the main chain, with the
 // two events of a fork and a join; calls that use it hold the mutex while they
 // enqueue, so forks and joins of concurrent callers do not interleave.

@@ -9,6 +9,9 @@ order of one training step:
   2. poetx_forward   y = R (W0 (P x))      [POET-X §2.A-§2.C]
   3. poetx_backward  dX, dtheta_P, dtheta_R
 
+and, when an inner loop ends, ``merge_and_resample`` (poetx_fold_w0, then
+fresh permutations merged by poetx_merge_w0) [POET-X §2.B]
+
 (source: "POET-X: Memory-efficient LLM Training by Scaling Orthogonal
 Transformation", gist.science summary, section 2).  PyTorch only allocates
 the buffers and supplies the stream; every step runs in the library's kernels.
@@ -85,6 +88,30 @@ class TransformedLinear:
         y = self.forward(x, y)
         dX, dtp, dtr = self.backward(x, dy, dX)
         return y, dX, dtp, dtr
+
+    def merge_and_resample(self, perm_in, perm_out):
+        """End of an inner loop [§2.B]: fold the current rotations into the
+        frozen weight (W0 <- R W0 P, poetx_fold_w0), reset theta to zero (so
+        Q = I), take the new permutations and merge them into the weight
+        (poetx_merge_w0).  The layer then computes the same function as
+        before, up to the fold's rounding, with fresh permutations."""
+        self.cayley_neumann()                       # Q of the current theta
+        need = _lib.poetx_fold_workspace_bytes(self.d_out, self.d_in, self.b_in, self.b_out,
+                                               self.dtype)
+        if need == 0:
+            raise ValueError("invalid layer sizes")
+        ws = (self.workspace if self.workspace.numel() >= need else
+              torch.empty(need, dtype=torch.uint8, device=self.W0.device))
+        _lib.poetx_fold_w0(self.W0m, self.Q_P, self.Q_R, self.perm_in, self.perm_out, self.b_in,
+                           self.b_out, self.W0, ws)
+        self.theta_P.zero_()
+        self.theta_R.zero_()
+        self.perm_in.copy_(perm_in.to(torch.int32))
+        self.perm_out.copy_(perm_out.to(torch.int32))
+        _lib.poetx_invert_perm(self.perm_in, self.inv_in)
+        _lib.poetx_invert_perm(self.perm_out, self.inv_out)
+        _lib.poetx_merge_w0(self.W0, self.W0m, self.perm_out, self.perm_in)
+        self.cayley_neumann()
 
     def capture_step(self, x, dy, y, dX, warm=True):
         """Capture one step on fixed buffers into a CUDA graph and return it.

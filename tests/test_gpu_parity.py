@@ -194,6 +194,81 @@ def test_merge_w0_bit_exact(dt):
     np.testing.assert_array_equal(to64(W0m), oracle.merge_w0(to64(W0), po.numpy(), pi.numpy()))
 
 
+# ------------------------------------------------------------------ end of an inner loop
+
+@pytest.mark.parametrize("dt,d_in,d_out,b_in,b_out", [
+    ("f32", 256, 256, 32, 32), ("f32", 96, 64, 8, 16), ("bf16", 256, 384, 32, 64),
+    ("bf16", 1024, 1024, 128, 128), ("bf16", 2048, 2048, 256, 256), ("bf16", 64, 128, 4, 8)])
+def test_fold_w0_parity(dt, d_in, d_out, b_in, b_out):
+    """W0_new = R W0 P from the merged weight, against the oracle's dense product
+    (the blocks are seeded random matrices: the fold is linear in them)."""
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    g = torch.Generator().manual_seed(7 * d_in + d_out)
+    W0 = (torch.randn(d_out, d_in, generator=g) * d_in ** -0.5).to(tdt)
+    QP = (torch.randn(d_in // b_in, b_in, b_in, generator=g) * b_in ** -0.5).to(tdt)
+    QR = (torch.randn(d_out // b_out, b_out, b_out, generator=g) * b_out ** -0.5).to(tdt)
+    pi = torch.randperm(d_in, generator=g).to(torch.int32)
+    po = torch.randperm(d_out, generator=g).to(torch.int32)
+    W0m = torch.empty(d_out, d_in, dtype=tdt, device="cuda")
+    _lib.poetx_merge_w0(W0.cuda(), W0m, po.cuda(), pi.cuda())
+    ws = torch.empty(_lib.poetx_fold_workspace_bytes(d_out, d_in, b_in, b_out, tdt),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(W0m)
+    _lib.poetx_fold_w0(W0m, QP.cuda(), QR.cuda(), pi.cuda(), po.cuda(), b_in, b_out, out, ws)
+    inplace = W0m.clone()
+    _lib.poetx_fold_w0(inplace, QP.cuda(), QR.cuda(), pi.cuda(), po.cuda(), b_in, b_out, inplace,
+                       ws)
+    _lib.poetx_stream_status()
+    torch.cuda.synchronize()
+    ref = oracle.fold_w0(to64(W0), to64(QP), to64(QR), pi.numpy(), po.numpy())
+    assert_close("W0_new", to64(out), ref, tol_for(dt))
+    assert torch.equal(out, inplace)
+
+
+def test_fold_w0_rejects_a_small_workspace():
+    W0m = torch.zeros(64, 64, device="cuda")
+    Q = torch.zeros(4, 16, 16, device="cuda")
+    p = torch.arange(64, dtype=torch.int32, device="cuda")
+    need = _lib.poetx_fold_workspace_bytes(64, 64, 16, 16, torch.float32)
+    ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(_lib.PoetxError) as e:
+        _lib.poetx_fold_w0(W0m, Q, Q, p, p, 16, 16, W0m, ws)
+    assert e.value.code == 2
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_merge_and_resample_keeps_the_function(dtype):
+    """An inner loop ends: W0 <- R W0 P, theta <- 0, new permutations.  The
+    layer's forward is the same function before and after (both against the
+    oracle's forward with the original parameters)."""
+    case = inputs.LinearCase("resample", 512, 768, 128, 256, 3, 300, 0.05, dtype, 911)
+    inp = inputs.make_linear_inputs(case)
+    lay = TransformedLinear(inp["W0"].cuda(), inp["theta_P"], inp["theta_R"], inp["perm_in"],
+                            inp["perm_out"], case.b_in, case.b_out, case.n, T_max=case.T)
+    x = inp["x"].cuda()
+    lay.cayley_neumann()
+    y0 = lay.forward(x).clone()
+    g = torch.Generator().manual_seed(3)
+    pi1 = torch.randperm(case.d_in, generator=g).to(torch.int32)
+    po1 = torch.randperm(case.d_out, generator=g).to(torch.int32)
+    lay.merge_and_resample(pi1, po1)
+    y1 = lay.forward(x)
+    _lib.poetx_stream_status()
+    torch.cuda.synchronize()
+    assert float(lay.theta_P.abs().max()) == 0.0 and float(lay.theta_R.abs().max()) == 0.0
+    assert torch.equal(lay.perm_in.cpu(), pi1) and torch.equal(lay.perm_out.cpu(), po1)
+    assert torch.equal(lay.inv_in.cpu()[pi1.long()], torch.arange(case.d_in, dtype=torch.int32))
+    eye = torch.eye(case.b_in, dtype=lay.Q_P.dtype, device="cuda")
+    assert torch.equal(lay.Q_P, eye.expand_as(lay.Q_P))
+    o = oracle_inputs(inp)
+    QP = oracle.cnp(o["thP"], case.b_in, case.n)
+    QR = oracle.cnp(o["thR"], case.b_out, case.n)
+    ref = oracle.forward(o["x"], o["W0"], QP, QR, o["pi"], o["po"])
+    tol = tol_for(dtype)
+    assert_close("y before", to64(y0), ref, tol)
+    assert_close("y after", to64(y1), ref, tol)
+
+
 # ------------------------------------------------------------------ the layer
 
 @pytest.mark.parametrize("save_z", [True, False])

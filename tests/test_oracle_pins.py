@@ -255,6 +255,47 @@ def test_spectrum_preserved_with_exact_cayley_blocks():
     assert np.abs(np.linalg.svd(R1 @ W0 @ P1, compute_uv=False) - s0).max() > 1e-3
 
 
+# ---------------------------------------------------------------- end of an inner loop (§2.B)
+
+@pytest.mark.parametrize("shape", [(16, 16, 4, 4, 5), (8, 12, 4, 6, 3), (32, 16, 8, 4, 7)])
+def test_fold_w0_is_the_effective_weight(shape):
+    d_in, d_out, b_in, b_out, T = shape
+    x, W0, thP, thR, pi, po, dy, n = _layer_case(d_in, d_out, b_in, b_out, T)
+    QP, QR = oracle.cnp(thP, b_in, n), oracle.cnp(thR, b_out, n)
+    W = oracle.fold_w0(W0, QP, QR, pi, po)
+    # the C oracle's token-by-token forward, with the unmerged W0
+    np.testing.assert_allclose(x @ W.T, oracle.forward(x, W0, QP, QR, pi, po), rtol=0, atol=1e-12)
+    # brute-force dense construction (numpy permutation rows, scipy block_diag)
+    P, R = _np_dense_PR(QP, QR, pi, po)
+    np.testing.assert_allclose(W, R @ W0 @ P, rtol=0, atol=1e-13)
+
+
+def test_fold_w0_with_identity_blocks_is_w0():
+    x, W0, thP, thR, pi, po, dy, n = _layer_case(24, 16, 8, 4, 1)
+    IP = np.broadcast_to(np.eye(8), (3, 8, 8))
+    IR = np.broadcast_to(np.eye(4), (4, 4, 4))
+    np.testing.assert_array_equal(oracle.fold_w0(W0, IP, IR, pi, po), W0)
+
+
+def test_fold_then_fresh_permutations_and_zero_theta_keep_the_function():
+    # an inner loop ends: W0 <- R W0 P, theta <- 0 (Q = I), new permutations
+    d_in, d_out, b_in, b_out, T = 32, 16, 8, 4, 6
+    x, W0, thP, thR, pi, po, dy, n = _layer_case(d_in, d_out, b_in, b_out, T)
+    QP, QR = oracle.cnp(thP, b_in, n), oracle.cnp(thR, b_out, n)
+    y0 = oracle.forward(x, W0, QP, QR, pi, po)
+    W1 = oracle.fold_w0(W0, QP, QR, pi, po)
+    rng = np.random.default_rng(7)
+    pi1 = rng.permutation(d_in).astype(np.int32)
+    po1 = rng.permutation(d_out).astype(np.int32)
+    QP1 = oracle.cnp(np.zeros_like(thP), b_in, n)
+    QR1 = oracle.cnp(np.zeros_like(thR), b_out, n)
+    np.testing.assert_allclose(oracle.forward(x, W1, QP1, QR1, pi1, po1), y0, rtol=0, atol=1e-12)
+    # and the fold keeps the spectrum when the blocks are exactly orthogonal
+    CP, CR = oracle.cayley(thP, b_in), oracle.cayley(thR, b_out)
+    np.testing.assert_allclose(np.linalg.svd(oracle.fold_w0(W0, CP, CR, pi, po), compute_uv=False),
+                               np.linalg.svd(W0, compute_uv=False), rtol=1e-12, atol=1e-12)
+
+
 @pytest.mark.parametrize("shape", [(16, 16, 4, 4, 5), (8, 12, 4, 6, 3)])
 def test_backward_dx_is_transpose_product(shape):
     d_in, d_out, b_in, b_out, T = shape
