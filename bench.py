@@ -459,6 +459,40 @@ def fold_point(lay, dev, peaks):
             "note": "the weight and the intermediate fit in L2 at this shape"}
 
 
+def xq_point(case, inp, lay, xs, dys, y, dX, dev):
+    """POET-XQ at the bench shape: the weight kept as INT8 codes + per-row
+    scales, dequantised into the workspace by every forward and backward.
+    Eager steps of the XQ layer beside eager steps of the bf16 layer (same
+    inputs, same loop), and the dequantisation alone."""
+    xq = TransformedLinear(inp["W0"].to(dev), inp["theta_P"], inp["theta_R"], inp["perm_in"],
+                           inp["perm_out"], case.b_in, case.b_out, case.n, T_max=case.T,
+                           save_z=True, device=dev, w0_int8=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, reps):
+        for k in range(3):
+            fn(k)
+        torch.cuda.synchronize()
+        e0.record()
+        for k in range(reps):
+            fn(k)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    reps = 20
+    ms_xq = timed(lambda k: xq.step(xs[k % len(xs)], dys[k % len(dys)], y, dX), reps)
+    ms_bf16 = timed(lambda k: lay.step(xs[k % len(xs)], dys[k % len(dys)], y, dX), reps)
+    Wd = torch.empty(case.d_out, case.d_in, dtype=torch.bfloat16, device=dev)
+    us_deq = 1e3 * timed(lambda k: _lib.poetx_dequantize_w0(xq.W0q, xq.w0_scale, Wd), 50)
+    out = {"ms_per_step_eager": round(ms_xq, 4), "bf16_ms_per_step_eager": round(ms_bf16, 4),
+           "dequantize_us": round(us_deq, 2),
+           "resident_w0_bytes": xq.W0q.numel() + 4 * xq.w0_scale.numel(),
+           "bf16_w0_bytes": 2 * case.d_out * case.d_in}
+    del xq, Wd
+    return out
+
+
 def run_poetx(args, world, rank, local):
     dev = torch.device("cuda", local)
     peaks = load_peaks()
@@ -641,6 +675,7 @@ def run_poetx(args, world, rank, local):
 
     cnp = cnp_points(dev) if rank == 0 else None
     fold = fold_point(lay, dev, peaks) if rank == 0 else None
+    xq = xq_point(case, inp, lay, xs, dys, y, dX, dev) if rank == 0 else None
 
     # ---------------- CPU oracle baseline (rank 0, N = 1 only)
     cpu = None
@@ -665,7 +700,7 @@ def run_poetx(args, world, rank, local):
             "data": "synthetic", "config": workload_config(world),
             "step_tflops": round(flops / (ms_per_step * 1e-3) / 1e12 / 1, 2),
             "step_frac_of_bf16_peak": round(flops / (ms_per_step * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-            "cnp_blocks_per_s": cnp, "fold_w0": fold, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "cnp_blocks_per_s": cnp, "fold_w0": fold, "xq": xq, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(launches), "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)

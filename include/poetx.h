@@ -230,6 +230,51 @@ poetx_status poetx_forward_noalloc(const void *x, const void *W0m, const void *Q
                                    poetx_dtype act_dtype, void *y, void *z_save,
                                    cudaStream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* POET-XQ [POET-X §2.E]: the frozen weight stored in INT8                   */
+/* ------------------------------------------------------------------------ */
+/* The page stores the base weight in INT8 and dequantises it on the fly; it
+ * gives no scale granularity.  Reading: one fp32 scale per row, symmetric,
+ * codes in [-127, 127]:
+ *   scale[i] = max_k |W0[i][k]| / 127              (fp32 division)
+ *   W0q[i][k] = rint(W0[i][k] / scale[i])          (fp32 division, ties to even;
+ *                                                   a zero row: scale 0, codes 0)
+ *   dequantised W0[i][k] = W0q[i][k] * scale[i]    (fp32 product, rounded to dtype)
+ * Quantise the merged weight (poetx_merge_w0's output): permuting rows or
+ * columns commutes with this quantiser.
+ *
+ * poetx_quantize_w0: W0 [d_out, d_in] in `dtype` -> W0q int8 [d_out, d_in],
+ *   scale fp32 [d_out].  d_in % 4 == 0.
+ * poetx_dequantize_w0: the inverse map, W0 [d_out, d_in] in `dtype` written.
+ * poetx_forward_xq / poetx_backward_xq: poetx_forward / poetx_backward with
+ *   the weight given as (W0q, scale) of the merged weight; every call first
+ *   dequantises it into the head of `workspace` (read back by the
+ *   tensor-core products while it is still in L2), so only the INT8 codes
+ *   and the scales stay resident.  `workspace` of ws_bytes >=
+ *   poetx_workspace_bytes_xq(...) = d_out * d_in * sizeof(act) rounded up to
+ *   256 bytes + poetx_workspace_bytes(...).  Other arguments, results and
+ *   errors as in poetx_forward / poetx_backward. */
+poetx_status poetx_quantize_w0(const void *W0, int d_out, int d_in, poetx_dtype dtype,
+                               int8_t *W0q, float *scale, cudaStream_t stream);
+poetx_status poetx_dequantize_w0(const int8_t *W0q, const float *scale, int d_out, int d_in,
+                                 poetx_dtype dtype, void *W0, cudaStream_t stream);
+size_t poetx_workspace_bytes_xq(int T, int d_in, int d_out, int b_in, int b_out,
+                                poetx_dtype dtype);
+poetx_status poetx_forward_xq(const void *x, const int8_t *W0q, const float *scale,
+                              const void *Q_P, const void *Q_R, const int32_t *perm_in,
+                              const int32_t *inv_in, const int32_t *perm_out,
+                              const int32_t *inv_out, int T, int d_in, int d_out, int b_in,
+                              int b_out, poetx_dtype act_dtype, void *y, void *z_save,
+                              void *workspace, size_t ws_bytes, cudaStream_t stream);
+poetx_status poetx_backward_xq(const void *x, const void *dy, const int8_t *W0q,
+                               const float *scale, const float *theta_P, const float *theta_R,
+                               int n, const void *Q_P, const void *Q_R, const void *z_saved,
+                               const int32_t *perm_in, const int32_t *inv_in,
+                               const int32_t *perm_out, const int32_t *inv_out, int T, int d_in,
+                               int d_out, int b_in, int b_out, poetx_dtype act_dtype, void *dX,
+                               float *dtheta_P, float *dtheta_R, void *workspace,
+                               size_t ws_bytes, cudaStream_t stream);
+
 /* Synchronises `stream` and reports the first error since the last call:
  * a CUDA error (POETX_ERR_CUDA) or an expired device-side wait
  * (POETX_ERR_TIMEOUT).  Clears the device error word. */

@@ -181,6 +181,28 @@ def fold_w0(W0, QP, QR, perm_in, perm_out):
     return R @ W0 @ P
 
 
+def quantize_rows_int8(W):
+    """[POET-X §2.E] POET-XQ: the frozen weight as INT8 codes, one symmetric
+    scale per row (the page gives no granularity; this is the reading).
+
+    s_i = max_k |W[i, k]| / 127 and q[i, k] = rint(W[i, k] / s_i), ties to even,
+    clipped to [-127, 127]; a row of zeros has s_i = 0 and codes 0.  The codes
+    are integers decided by floating point, so this takes the decisions in the
+    precision the kernel takes them in: IEEE fp32 divisions.  Returns (q int8,
+    s float32)."""
+    W = np.asarray(W, dtype=np.float32)
+    s = (np.abs(W).max(axis=1) / np.float32(127)).astype(np.float32)
+    q = np.zeros(W.shape, dtype=np.int8)
+    nz = s > 0
+    q[nz] = np.clip(np.rint(W[nz] / s[nz, None]), -127, 127).astype(np.int8)
+    return q, s
+
+
+def dequantize_rows(q, s):
+    """Inverse map of ``quantize_rows_int8``: W'[i, k] = q[i, k] * s_i, in double."""
+    return np.asarray(q, dtype=np.float64) * np.asarray(s, dtype=np.float64)[:, None]
+
+
 def forward(x, W0, QP, QR, perm_in, perm_out, return_z=False):
     """[POET-X §2.A-§2.C] y = Pi_R^T B_R Pi_R W0 Pi_P^T B_P Pi_P x, token by token.
 

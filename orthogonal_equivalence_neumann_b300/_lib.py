@@ -26,7 +26,8 @@ EXPORTS = ["poetx_status_string", "poetx_version", "poetx_cayley_neumann",
            "poetx_merge_w0", "poetx_workspace_bytes", "poetx_forward", "poetx_backward",
            "poetx_stream_status", "poetx_launch_count", "poetx_profile_enable",
            "poetx_profile_report", "poetx_forward_noalloc", "poetx_fold_workspace_bytes",
-           "poetx_fold_w0"]
+           "poetx_fold_w0", "poetx_quantize_w0", "poetx_dequantize_w0",
+           "poetx_workspace_bytes_xq", "poetx_forward_xq", "poetx_backward_xq"]
 
 
 class PoetxError(RuntimeError):
@@ -68,6 +69,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "poetx_profile_report": (I, [ctypes.c_char_p, Z]),
         "poetx_fold_workspace_bytes": (Z, [I, I, I, I, I]),
         "poetx_fold_w0": (I, [P, P, P, P, P, I, I, I, I, I, P, P, Z, P]),
+        "poetx_quantize_w0": (I, [P, I, I, I, P, P, P]),
+        "poetx_dequantize_w0": (I, [P, P, I, I, I, P, P]),
+        "poetx_workspace_bytes_xq": (Z, [I, I, I, I, I, I]),
+        "poetx_forward_xq": (I, [P] * 9 + [I] * 6 + [P, P, P, Z, P]),
+        "poetx_backward_xq": (I, [P] * 6 + [I] + [P] * 7 + [I] * 6 + [P] * 4 + [Z, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -204,6 +210,45 @@ def poetx_forward_noalloc(x, W0m, Q_P, Q_R, perm_in, inv_in, perm_out, inv_out, 
         _ptr(x), _ptr(W0m), _ptr(Q_P), _ptr(Q_R), _ptr(perm_in), _ptr(inv_in), _ptr(perm_out),
         _ptr(inv_out), T, d_in, d_out, b_in, b_out, dtype_code(x.dtype), _ptr(y), _ptr(z_save),
         _stream(stream)))
+
+
+def poetx_quantize_w0(W0, W0q, scale, stream=None):
+    d_out, d_in = W0.shape
+    _check("poetx_quantize_w0", load().poetx_quantize_w0(
+        _ptr(W0), d_out, d_in, dtype_code(W0.dtype), _ptr(W0q), _ptr(scale), _stream(stream)))
+
+
+def poetx_dequantize_w0(W0q, scale, W0, stream=None):
+    d_out, d_in = W0q.shape
+    _check("poetx_dequantize_w0", load().poetx_dequantize_w0(
+        _ptr(W0q), _ptr(scale), d_out, d_in, dtype_code(W0.dtype), _ptr(W0), _stream(stream)))
+
+
+def poetx_workspace_bytes_xq(T, d_in, d_out, b_in, b_out, dtype) -> int:
+    return int(load().poetx_workspace_bytes_xq(T, d_in, d_out, b_in, b_out, dtype_code(dtype)))
+
+
+def poetx_forward_xq(x, W0q, scale, Q_P, Q_R, perm_in, inv_in, perm_out, inv_out, b_in, b_out, y,
+                     z_save, workspace, stream=None):
+    T, d_in = x.shape
+    d_out = W0q.shape[0]
+    _check("poetx_forward_xq", load().poetx_forward_xq(
+        _ptr(x), _ptr(W0q), _ptr(scale), _ptr(Q_P), _ptr(Q_R), _ptr(perm_in), _ptr(inv_in),
+        _ptr(perm_out), _ptr(inv_out), T, d_in, d_out, b_in, b_out, dtype_code(x.dtype), _ptr(y),
+        _ptr(z_save), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def poetx_backward_xq(x, dy, W0q, scale, theta_P, theta_R, n, Q_P, Q_R, z_saved, perm_in, inv_in,
+                      perm_out, inv_out, b_in, b_out, dX, dtheta_P, dtheta_R, workspace,
+                      stream=None):
+    T, d_in = x.shape
+    d_out = W0q.shape[0]
+    _check("poetx_backward_xq", load().poetx_backward_xq(
+        _ptr(x), _ptr(dy), _ptr(W0q), _ptr(scale), _ptr(theta_P), _ptr(theta_R), n, _ptr(Q_P),
+        _ptr(Q_R), _ptr(z_saved), _ptr(perm_in), _ptr(inv_in), _ptr(perm_out), _ptr(inv_out), T,
+        d_in, d_out, b_in, b_out, dtype_code(x.dtype), _ptr(dX), _ptr(dtheta_P), _ptr(dtheta_R),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def poetx_stream_status(stream=None):

@@ -375,6 +375,76 @@ poetx_status poetx_backward(const void* x, const void* dy, const void* W0m, cons
   return POETX_OK;
 }
 
+// ---- POET-XQ [§2.E]: INT8 frozen weight, dequantised per call -----------------
+
+poetx_status poetx_quantize_w0(const void* W0, int d_out, int d_in, poetx_dtype dtype,
+                               int8_t* W0q, float* scale, cudaStream_t stream) {
+  if (!valid_dtype(dtype)) return POETX_ERR_INVALID_ARG;
+  if (d_out <= 0 || d_in <= 0 || d_in % 4) return POETX_ERR_SHAPE;
+  if (!W0 || !W0q || !scale || !aligned16(W0) || !aligned16(W0q) || !aligned16(scale))
+    return POETX_ERR_INVALID_ARG;
+  return launch_quantize_w0(W0, d_out, d_in, dtype, W0q, scale, stream);
+}
+
+poetx_status poetx_dequantize_w0(const int8_t* W0q, const float* scale, int d_out, int d_in,
+                                 poetx_dtype dtype, void* W0, cudaStream_t stream) {
+  if (!valid_dtype(dtype)) return POETX_ERR_INVALID_ARG;
+  if (d_out <= 0 || d_in <= 0 || d_in % 4) return POETX_ERR_SHAPE;
+  if (!W0 || !W0q || !scale || !aligned16(W0) || !aligned16(W0q) || !aligned16(scale))
+    return POETX_ERR_INVALID_ARG;
+  return launch_dequantize_w0(W0q, scale, d_out, d_in, dtype, W0, stream);
+}
+
+// The dequantised weight's region, at the head of the XQ workspace.
+static size_t xq_weight_bytes(int d_in, int d_out, poetx_dtype dtype) {
+  return round_up((size_t)d_out * d_in * dtype_size(dtype), 256);
+}
+
+size_t poetx_workspace_bytes_xq(int T, int d_in, int d_out, int b_in, int b_out,
+                                poetx_dtype dtype) {
+  const size_t rest = poetx_workspace_bytes(T, d_in, d_out, b_in, b_out, dtype);
+  if (rest == 0 || d_in % 4) return 0;
+  return xq_weight_bytes(d_in, d_out, dtype) + rest;
+}
+
+poetx_status poetx_forward_xq(const void* x, const int8_t* W0q, const float* scale,
+                              const void* Q_P, const void* Q_R, const int32_t* perm_in,
+                              const int32_t* inv_in, const int32_t* perm_out,
+                              const int32_t* inv_out, int T, int d_in, int d_out, int b_in,
+                              int b_out, poetx_dtype act_dtype, void* y, void* z_save,
+                              void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  POETX_TRY(check_linear_args(T, d_in, d_out, b_in, b_out, act_dtype, {W0q, scale, workspace}));
+  if (d_in % 4) return POETX_ERR_SHAPE;
+  if (ws_bytes < poetx_workspace_bytes_xq(T, d_in, d_out, b_in, b_out, act_dtype))
+    return POETX_ERR_SHAPE;
+  const size_t head = xq_weight_bytes(d_in, d_out, act_dtype);
+  void* W0m = workspace;
+  POETX_TRY(launch_dequantize_w0(W0q, scale, d_out, d_in, act_dtype, W0m, stream));
+  return poetx_forward(x, W0m, Q_P, Q_R, perm_in, inv_in, perm_out, inv_out, T, d_in, d_out, b_in,
+                       b_out, act_dtype, y, z_save, static_cast<char*>(workspace) + head,
+                       ws_bytes - head, stream);
+}
+
+poetx_status poetx_backward_xq(const void* x, const void* dy, const int8_t* W0q,
+                               const float* scale, const float* theta_P, const float* theta_R,
+                               int n, const void* Q_P, const void* Q_R, const void* z_saved,
+                               const int32_t* perm_in, const int32_t* inv_in,
+                               const int32_t* perm_out, const int32_t* inv_out, int T, int d_in,
+                               int d_out, int b_in, int b_out, poetx_dtype act_dtype, void* dX,
+                               float* dtheta_P, float* dtheta_R, void* workspace,
+                               size_t ws_bytes, cudaStream_t stream) {
+  POETX_TRY(check_linear_args(T, d_in, d_out, b_in, b_out, act_dtype, {W0q, scale, workspace}));
+  if (d_in % 4) return POETX_ERR_SHAPE;
+  if (ws_bytes < poetx_workspace_bytes_xq(T, d_in, d_out, b_in, b_out, act_dtype))
+    return POETX_ERR_SHAPE;
+  const size_t head = xq_weight_bytes(d_in, d_out, act_dtype);
+  void* W0m = workspace;
+  POETX_TRY(launch_dequantize_w0(W0q, scale, d_out, d_in, act_dtype, W0m, stream));
+  return poetx_backward(x, dy, W0m, theta_P, theta_R, n, Q_P, Q_R, z_saved, perm_in, inv_in,
+                        perm_out, inv_out, T, d_in, d_out, b_in, b_out, act_dtype, dX, dtheta_P,
+                        dtheta_R, static_cast<char*>(workspace) + head, ws_bytes - head, stream);
+}
+
 poetx_status poetx_stream_status(cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) {
     cudaGetLastError();

@@ -36,4 +36,10 @@ poetx_status launch_transpose(const void* in, void* out, int rows, int cols, poe
 poetx_status launch_merge_w0(const void* W0, void* W0m, int d_out, int d_in, poetx_dtype dt,
                              const int32_t* po, const int32_t* pi, cudaStream_t s);
 
+// ---- POET-XQ: per-row INT8 codes of the frozen weight --------------------------
+poetx_status launch_quantize_w0(const void* W, int d_out, int d_in, poetx_dtype dt, int8_t* q,
+                                float* scale, cudaStream_t s);
+poetx_status launch_dequantize_w0(const int8_t* q, const float* scale, int d_out, int d_in,
+                                  poetx_dtype dt, void* W, cudaStream_t s);
+
 }  // namespace poetx

@@ -10,7 +10,9 @@ order of one training step:
   3. poetx_backward  dX, dtheta_P, dtheta_R
 
 and, when an inner loop ends, ``merge_and_resample`` (poetx_fold_w0, then
-fresh permutations merged by poetx_merge_w0) [POET-X §2.B]
+fresh permutations merged by poetx_merge_w0) [POET-X §2.B].  With
+``w0_int8`` the merged weight is kept as INT8 codes and per-row scales
+(POET-XQ, §2.E) and the _xq entry points dequantise it per call.
 
 (source: "POET-X: Memory-efficient LLM Training by Scaling Orthogonal
 Transformation", gist.science summary, section 2).  PyTorch only allocates
@@ -25,7 +27,7 @@ from . import _lib
 
 class TransformedLinear:
     def __init__(self, W0, theta_P, theta_R, perm_in, perm_out, b_in, b_out, n, T_max,
-                 save_z=True, device="cuda"):
+                 save_z=True, device="cuda", w0_int8=False):
         dev = torch.device(device)
         self.dtype = W0.dtype
         self.d_out, self.d_in = W0.shape
@@ -44,13 +46,23 @@ class TransformedLinear:
         # [§2.B] merge the two inner permutations into W0 once (per inner loop)
         self.W0m = torch.empty_like(self.W0)
         _lib.poetx_merge_w0(self.W0, self.W0m, self.perm_out, self.perm_in)
+        # [§2.E] POET-XQ: keep only INT8 codes and per-row scales of the merged
+        # weight resident; every forward / backward dequantises them into its
+        # workspace
+        self.w0_int8 = bool(w0_int8)
+        self.W0q = self.w0_scale = None
+        if self.w0_int8:
+            self.W0q = torch.empty(self.d_out, self.d_in, dtype=torch.int8, device=dev)
+            self.w0_scale = torch.empty(self.d_out, dtype=torch.float32, device=dev)
+            _lib.poetx_quantize_w0(self.W0m, self.W0q, self.w0_scale)
+            self.W0 = self.W0m = None
         nbi, nbo = self.d_in // self.b_in, self.d_out // self.b_out
         self.Q_P = torch.empty(nbi, self.b_in, self.b_in, dtype=self.dtype, device=dev)
         self.Q_R = torch.empty(nbo, self.b_out, self.b_out, dtype=self.dtype, device=dev)
         self.dtheta_P = torch.empty_like(self.theta_P)
         self.dtheta_R = torch.empty_like(self.theta_R)
-        ws = _lib.poetx_workspace_bytes(self.T_max, self.d_in, self.d_out, self.b_in, self.b_out,
-                                        self.dtype)
+        ws_bytes = (_lib.poetx_workspace_bytes_xq if self.w0_int8 else _lib.poetx_workspace_bytes)
+        ws = ws_bytes(self.T_max, self.d_in, self.d_out, self.b_in, self.b_out, self.dtype)
         if ws == 0:
             raise ValueError("invalid layer sizes")
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
@@ -66,9 +78,14 @@ class TransformedLinear:
         if y is None:
             y = torch.empty(T, self.d_out, dtype=self.dtype, device=x.device)
         z = self.z[:T] if self.z is not None else None
-        _lib.poetx_forward(x, self.W0m, self.Q_P, self.Q_R, self.perm_in, self.inv_in,
-                           self.perm_out, self.inv_out, self.b_in, self.b_out, y, z,
-                           self.workspace)
+        if self.w0_int8:
+            _lib.poetx_forward_xq(x, self.W0q, self.w0_scale, self.Q_P, self.Q_R, self.perm_in,
+                                  self.inv_in, self.perm_out, self.inv_out, self.b_in, self.b_out,
+                                  y, z, self.workspace)
+        else:
+            _lib.poetx_forward(x, self.W0m, self.Q_P, self.Q_R, self.perm_in, self.inv_in,
+                               self.perm_out, self.inv_out, self.b_in, self.b_out, y, z,
+                               self.workspace)
         return y
 
     def backward(self, x, dy, dX=None):
@@ -76,10 +93,16 @@ class TransformedLinear:
         if dX is None:
             dX = torch.empty(T, self.d_in, dtype=self.dtype, device=x.device)
         z = self.z[:T] if self.z is not None else None
-        _lib.poetx_backward(x, dy, self.W0m, self.theta_P, self.theta_R, self.n, self.Q_P,
-                            self.Q_R, z, self.perm_in, self.inv_in, self.perm_out, self.inv_out,
-                            self.b_in, self.b_out, dX, self.dtheta_P, self.dtheta_R,
-                            self.workspace)
+        if self.w0_int8:
+            _lib.poetx_backward_xq(x, dy, self.W0q, self.w0_scale, self.theta_P, self.theta_R,
+                                   self.n, self.Q_P, self.Q_R, z, self.perm_in, self.inv_in,
+                                   self.perm_out, self.inv_out, self.b_in, self.b_out, dX,
+                                   self.dtheta_P, self.dtheta_R, self.workspace)
+        else:
+            _lib.poetx_backward(x, dy, self.W0m, self.theta_P, self.theta_R, self.n, self.Q_P,
+                                self.Q_R, z, self.perm_in, self.inv_in, self.perm_out,
+                                self.inv_out, self.b_in, self.b_out, dX, self.dtheta_P,
+                                self.dtheta_R, self.workspace)
         return dX, self.dtheta_P, self.dtheta_R
 
     def step(self, x, dy, y=None, dX=None):
@@ -96,21 +119,30 @@ class TransformedLinear:
         (poetx_merge_w0).  The layer then computes the same function as
         before, up to the fold's rounding, with fresh permutations."""
         self.cayley_neumann()                       # Q of the current theta
+        dev = self.Q_P.device
         need = _lib.poetx_fold_workspace_bytes(self.d_out, self.d_in, self.b_in, self.b_out,
                                                self.dtype)
         if need == 0:
             raise ValueError("invalid layer sizes")
         ws = (self.workspace if self.workspace.numel() >= need else
-              torch.empty(need, dtype=torch.uint8, device=self.W0.device))
-        _lib.poetx_fold_w0(self.W0m, self.Q_P, self.Q_R, self.perm_in, self.perm_out, self.b_in,
-                           self.b_out, self.W0, ws)
+              torch.empty(need, dtype=torch.uint8, device=dev))
+        if self.w0_int8:   # the bf16 weights exist only while the fold runs
+            W0m = torch.empty(self.d_out, self.d_in, dtype=self.dtype, device=dev)
+            _lib.poetx_dequantize_w0(self.W0q, self.w0_scale, W0m)
+            W0 = torch.empty_like(W0m)
+        else:
+            W0m, W0 = self.W0m, self.W0
+        _lib.poetx_fold_w0(W0m, self.Q_P, self.Q_R, self.perm_in, self.perm_out, self.b_in,
+                           self.b_out, W0, ws)
         self.theta_P.zero_()
         self.theta_R.zero_()
         self.perm_in.copy_(perm_in.to(torch.int32))
         self.perm_out.copy_(perm_out.to(torch.int32))
         _lib.poetx_invert_perm(self.perm_in, self.inv_in)
         _lib.poetx_invert_perm(self.perm_out, self.inv_out)
-        _lib.poetx_merge_w0(self.W0, self.W0m, self.perm_out, self.perm_in)
+        _lib.poetx_merge_w0(W0, W0m, self.perm_out, self.perm_in)
+        if self.w0_int8:
+            _lib.poetx_quantize_w0(W0m, self.W0q, self.w0_scale)
         self.cayley_neumann()
 
     def capture_step(self, x, dy, y, dX, warm=True):

@@ -269,6 +269,89 @@ def test_merge_and_resample_keeps_the_function(dtype):
     assert_close("y after", to64(y1), ref, tol)
 
 
+# ------------------------------------------------------------------ POET-XQ (INT8 frozen weight)
+
+@pytest.mark.parametrize("dt,d_out,d_in", [(torch.bfloat16, 2048, 2048), (torch.float32, 384, 260),
+                                           (torch.bfloat16, 5632, 2048)])
+def test_quantize_w0_codes_bit_exact(dt, d_out, d_in):
+    g = torch.Generator().manual_seed(d_out + d_in)
+    W = (torch.randn(d_out, d_in, generator=g) * torch.rand(d_out, 1, generator=g)).to(dt)
+    W[3] = 0                                              # a zero row: scale 0, codes 0
+    q = torch.empty(d_out, d_in, dtype=torch.int8, device="cuda")
+    sc = torch.empty(d_out, dtype=torch.float32, device="cuda")
+    _lib.poetx_quantize_w0(W.cuda(), q, sc)
+    Wd = torch.empty(d_out, d_in, dtype=dt, device="cuda")
+    _lib.poetx_dequantize_w0(q, sc, Wd)
+    _lib.poetx_stream_status()
+    torch.cuda.synchronize()
+    q_ref, s_ref = oracle.quantize_rows_int8(W.float().numpy())
+    np.testing.assert_array_equal(sc.cpu().numpy(), s_ref)
+    np.testing.assert_array_equal(q.cpu().numpy(), q_ref)
+    # dequantised: the fp32 product code * scale, rounded once to the dtype
+    want = (torch.from_numpy(q_ref).float() * torch.from_numpy(s_ref)[:, None]).to(dt)
+    assert torch.equal(Wd.cpu(), want)
+
+
+def xq_oracle_layer(case, inp, rows=None):
+    """The oracle layer with the weight the GPU multiplies by: the INT8 codes
+    of W0 dequantised (in double)."""
+    o = oracle_inputs(inp)
+    q, s = oracle.quantize_rows_int8(inp["W0"].float().numpy())
+    W0 = oracle.dequantize_rows(q, s)
+    QP = oracle.cnp(o["thP"], case.b_in, case.n)
+    QR = oracle.cnp(o["thR"], case.b_out, case.n)
+    xr = o["x"] if rows is None else o["x"][rows]
+    y = oracle.forward(xr, W0, QP, QR, o["pi"], o["po"])
+    dX, dQP, dQR = oracle.backward(o["x"], o["dy"], W0, QP, QR, o["pi"], o["po"])
+    return dict(y=y, dX=dX if rows is None else dX[rows],
+                dtheta_P=oracle.cnp_backward(o["thP"], case.b_in, case.n, dQP),
+                dtheta_R=oracle.cnp_backward(o["thR"], case.b_out, case.n, dQR))
+
+
+@pytest.mark.parametrize("name,d,b,T,dtype,save_z", [
+    ("xq_tiny", 256, 32, 64, "f32", True), ("xq_tiny", 256, 32, 64, "f32", False),
+    ("xq_1024", 1024, 128, 1000, "bf16", True), ("xq_1024", 1024, 128, 1000, "bf16", False),
+    ("xq_2048", 2048, 256, 8192, "bf16", True)])
+def test_xq_layer_parity(name, d, b, T, dtype, save_z):
+    case = inputs.LinearCase(name, d, d, b, b, 3, T, 0.01, dtype, 913)
+    inp = inputs.make_linear_inputs(case)
+    lay = TransformedLinear(inp["W0"].cuda(), inp["theta_P"], inp["theta_R"], inp["perm_in"],
+                            inp["perm_out"], b, b, 3, T_max=T, save_z=save_z, w0_int8=True)
+    assert lay.W0m is None and lay.W0q.dtype == torch.int8
+    y, dX, dtp, dtr = lay.step(inp["x"].cuda(), inp["dy"].cuda())
+    _lib.poetx_stream_status()
+    torch.cuda.synchronize()
+    rows = SAMPLE_ROWS(T) if T > 2048 else None
+    r = xq_oracle_layer(case, inp, rows=rows)
+    tol = tol_for(dtype)
+    got = dict(y=to64(y), dX=to64(dX), dtheta_P=dtp.double().cpu().numpy(),
+               dtheta_R=dtr.double().cpu().numpy())
+    for k in ("dtheta_P", "dtheta_R"):
+        assert_close(k, got[k], r[k], tol)
+    for k in ("y", "dX"):
+        assert_close(k, got[k] if rows is None else got[k][rows], r[k], tol)
+
+
+def test_xq_merge_and_resample_keeps_the_function():
+    case = inputs.LinearCase("xq_resample", 512, 768, 128, 256, 3, 300, 0.05, "bf16", 914)
+    inp = inputs.make_linear_inputs(case)
+    lay = TransformedLinear(inp["W0"].cuda(), inp["theta_P"], inp["theta_R"], inp["perm_in"],
+                            inp["perm_out"], case.b_in, case.b_out, case.n, T_max=case.T,
+                            w0_int8=True)
+    x = inp["x"].cuda()
+    lay.cayley_neumann()
+    y0 = lay.forward(x).clone()
+    g = torch.Generator().manual_seed(4)
+    lay.merge_and_resample(torch.randperm(case.d_in, generator=g),
+                           torch.randperm(case.d_out, generator=g))
+    y1 = lay.forward(x)
+    _lib.poetx_stream_status()
+    torch.cuda.synchronize()
+    ref = xq_oracle_layer(case, inp)["y"]
+    assert_close("y before", to64(y0), ref, TOL_BF16)
+    assert_close("y after", to64(y1), ref, TOL_BF16)
+
+
 # ------------------------------------------------------------------ the layer
 
 @pytest.mark.parametrize("save_z", [True, False])

@@ -370,3 +370,36 @@ def test_oracle_results_do_not_depend_on_thread_count():
                                    capture_output=True,
                                    cwd=os.path.dirname(os.path.dirname(__file__))).stdout)
     assert outs[0] == outs[1] and len(outs[0]) > 0
+
+
+# ---------------------------------------------------------------- POET-XQ (§2.E)
+
+def test_quantize_rows_int8_golden():
+    g = read_golden("xq_rows.txt")
+    q, s = oracle.quantize_rows_int8(as_f64(g["W"]))
+    np.testing.assert_array_equal(s, as_f64(g["scale"]).astype(np.float32))
+    np.testing.assert_array_equal(q, as_f64(g["codes"]).astype(np.int8))
+
+
+def test_quantize_rows_int8_bounds_and_round_trip_error():
+    rng = np.random.default_rng(11)
+    W = (rng.standard_normal((37, 64)) * rng.uniform(0.01, 3.0, (37, 1))).astype(np.float32)
+    q, s = oracle.quantize_rows_int8(W)
+    assert q.dtype == np.int8 and s.dtype == np.float32
+    # every row uses the full code range at its maximum, and nothing beyond it
+    np.testing.assert_array_equal(np.abs(q.astype(np.int32)).max(axis=1), 127)
+    # nearest code: |W - q s| <= s / 2 (plus the fp32 rounding of the division)
+    err = np.abs(W.astype(np.float64) - oracle.dequantize_rows(q, s))
+    assert np.all(err <= s.astype(np.float64)[:, None] * (0.5 + 1e-6))
+
+
+def test_quantize_commutes_with_the_merge():
+    # quantising the merged weight = merging the quantised weight (codes and scales)
+    rng = np.random.default_rng(12)
+    W = rng.standard_normal((24, 16)).astype(np.float32)
+    po = rng.permutation(24).astype(np.int32)
+    pi = rng.permutation(16).astype(np.int32)
+    qm, sm = oracle.quantize_rows_int8(oracle.merge_w0(W, po, pi))
+    q, s = oracle.quantize_rows_int8(W)
+    np.testing.assert_array_equal(qm, q[po][:, pi])
+    np.testing.assert_array_equal(sm, s[po])
