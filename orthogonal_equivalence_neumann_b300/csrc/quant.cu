@@ -74,24 +74,34 @@ __device__ __forceinline__ void store_deq(__nv_bfloat16* dst, const float* v) {
   *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(h);
 }
 
-// W'[i][k] = q[i][k] * s_i, four codes per thread (d_in % 4 == 0: one 32-bit
-// load of codes, one 8- or 16-byte store); grid-stride over the matrix.
-template <typename T>
+// W'[i][k] = q[i][k] * s_i, V codes per thread (V = 16 when d_in % 16 == 0:
+// one 16-byte load of codes and two (bf16) or four (fp32) 16-byte stores;
+// else V = 4); grid-stride over the matrix.
+template <typename T, int V>
 __global__ void __launch_bounds__(kQuantThreads) dequantize_kernel(const int8_t* __restrict__ q,
                                                                    const float* __restrict__ scale,
                                                                    int d_out, int d_in,
                                                                    T* __restrict__ W) {
-  const size_t quads = (size_t)d_out * d_in / 4;
-  const int row_quads = d_in / 4;
-  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < quads;
+  const size_t groups = (size_t)d_out * d_in / V;
+  const int row_groups = d_in / V;
+  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < groups;
        e += (size_t)gridDim.x * blockDim.x) {
-    const int i = (int)(e / row_quads);
+    const int i = (int)(e / row_groups);
     const float s = __ldg(scale + i);
-    const uint32_t c4 = __ldg(reinterpret_cast<const uint32_t*>(q) + e);
-    float v[4];
+    uint32_t c[V / 4];
+    if constexpr (V == 16) {
+      const uint4 c16 = __ldg(reinterpret_cast<const uint4*>(q) + e);
+      c[0] = c16.x; c[1] = c16.y; c[2] = c16.z; c[3] = c16.w;
+    } else {
+      c[0] = __ldg(reinterpret_cast<const uint32_t*>(q) + e);
+    }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] = __fmul_rn((float)(int8_t)(c4 >> (8 * j)), s);
-    store_deq(W + e * 4, v);
+    for (int w = 0; w < V / 4; ++w) {
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = __fmul_rn((float)(int8_t)(c[w] >> (8 * j)), s);
+      store_deq(W + e * V + w * 4, v);
+    }
   }
 }
 
@@ -115,19 +125,23 @@ poetx_status launch_dequantize_w0(const int8_t* q, const float* scale, int d_out
                                   poetx_dtype dt, void* W, cudaStream_t s) {
   if (d_out <= 0 || d_in <= 0) return POETX_OK;
   if (d_in % 4) return POETX_ERR_SHAPE;
-  const size_t quads = (size_t)d_out * d_in / 4;
-  // enough CTAs to fill every SM several times over, no more than the work
-  size_t blocks = (quads + kQuantThreads - 1) / kQuantThreads;
-  const size_t cap = (size_t)device_sm_count() * 8;
+  const bool v16 = d_in % 16 == 0;
+  const size_t groups = (size_t)d_out * d_in / (v16 ? 16 : 4);
+  // one group per thread while that fills every SM several times over
+  size_t blocks = (groups + kQuantThreads - 1) / kQuantThreads;
+  const size_t cap = (size_t)device_sm_count() * 16;
   if (blocks > cap) blocks = cap;
+  const unsigned nb = (unsigned)blocks;
   {
     KernelScope ks_("dequantize_w0", s);
-    if (dt == POETX_F32)
-      dequantize_kernel<float><<<(unsigned)blocks, kQuantThreads, 0, s>>>(q, scale, d_out, d_in,
-                                                                          (float*)W);
-    else
-      dequantize_kernel<__nv_bfloat16><<<(unsigned)blocks, kQuantThreads, 0, s>>>(
-          q, scale, d_out, d_in, (__nv_bfloat16*)W);
+    if (dt == POETX_F32) {
+      if (v16) dequantize_kernel<float, 16><<<nb, kQuantThreads, 0, s>>>(q, scale, d_out, d_in, (float*)W);
+      else dequantize_kernel<float, 4><<<nb, kQuantThreads, 0, s>>>(q, scale, d_out, d_in, (float*)W);
+    } else {
+      __nv_bfloat16* Wb = (__nv_bfloat16*)W;
+      if (v16) dequantize_kernel<__nv_bfloat16, 16><<<nb, kQuantThreads, 0, s>>>(q, scale, d_out, d_in, Wb);
+      else dequantize_kernel<__nv_bfloat16, 4><<<nb, kQuantThreads, 0, s>>>(q, scale, d_out, d_in, Wb);
+    }
   }
   return check_launch();
 }
