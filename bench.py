@@ -28,7 +28,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from orthogonal_equivalence_neumann_b300 import TransformedLinear, _lib, inputs  # noqa: E402
+from orthogonal_equivalence_neumann_b300 import TransformedLinear, _lib, dp, inputs  # noqa: E402
 
 METRIC = "transformed-linear tokens/s (fwd+bwd) and Cayley-Neumann blocks/s; % of roofline"
 CASE = inputs.SQUARE_2048
@@ -281,21 +281,13 @@ def barrier(world):
 
 
 def max_over_ranks(v, world):
-    if world == 1:
-        return v
-    import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    return dp.max_over_ranks(v) if world > 1 else v
 
 
 def allreduce_grads(layer, world):
     """The data-parallel exchange: sum the packed skew gradients over ranks."""
-    if world == 1:
-        return
-    import torch.distributed as dist
-    dist.all_reduce(layer.dtheta_P)
-    dist.all_reduce(layer.dtheta_R)
+    if world > 1:
+        dp.allreduce_dtheta(layer.dtheta_P, layer.dtheta_R)
 
 
 class OracleSample:
