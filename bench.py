@@ -98,18 +98,28 @@ def step_flops(case):
     return fwd + bwd
 
 
+def sources_sha(srcs):
+    """sha1[:12] over the concatenated contents of comma-separated source paths."""
+    h = hashlib.sha1()
+    for src in srcs.split(","):
+        path = os.path.join(ROOT, src)
+        if not os.path.exists(path):
+            return None
+        h.update(open(path, "rb").read())
+    return h.hexdigest()[:12]
+
+
 def read_traffic(kernel):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if the
-    kernel's source is unchanged since the capture (else None)."""
+    kernel's sources are unchanged since the capture (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
     for line in open(p):
         parts = line.split("#", 1)[0].split()
         if len(parts) == 4 and parts[0] == kernel:
-            src, sha, nbytes = parts[1], parts[2], parts[3]
-            path = os.path.join(ROOT, src)
-            if os.path.exists(path) and hashlib.sha1(open(path, "rb").read()).hexdigest()[:12] == sha:
+            srcs, sha, nbytes = parts[1], parts[2], parts[3]
+            if sources_sha(srcs) == sha:
                 return float(nbytes)
     return None
 

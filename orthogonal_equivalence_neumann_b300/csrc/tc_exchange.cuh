@@ -33,7 +33,8 @@ namespace xchg {
 
 constexpr int TT = 64;          // tokens per tile (the epilogues hold a tile row in two 32-wide TMEM loads)
 constexpr int kMovers = 256;    // threads that write feature rows (warps 2..9)
-constexpr int kMaxSlots = 8;    // exchange slots in the workspace ring (at most)
+constexpr int kMaxSlots = 4;    // exchange slots in the workspace ring (at most; 4 measured
+                                // faster than 8 or 6 at the square 2048 layer: less L2 held)
 constexpr int kTableOff = 512;  // routing table, after the barrier block
 
 __device__ __forceinline__ void movers_bar() {

@@ -8,7 +8,10 @@
 //   backward  g_u = g_z . W0m     (B = W0m [K = d_out, N = d_in], MN-major)
 // C[M, N] (bf16) = A[M, K] (bf16, K-major) . B^T, fp32 accumulation in TMEM.
 //
-// Persistent kernel, one CTA per SM, 128 x 256 output tiles, 64-deep k steps:
+// Persistent kernel, one CTA per SM, 128 x 256 output tiles, 64-deep k steps;
+// tiles go out column block fastest, so the CTAs of one round cover a few row
+// blocks across every column block (each A tile read by several CTAs at once,
+// while it is in L2; a small working set of A per round):
 //   warp 0  one thread issues TMA loads of A and B tiles (128-byte swizzle)
 //           into a 4-stage shared-memory ring;
 //   warp 1  allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
@@ -79,7 +82,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int m_blk = tile % m_tiles, n_blk = tile / m_tiles;
+        const int m_blk = tile / n_tiles, n_blk = tile % n_tiles;
         for (int kb = 0; kb < k_iters; ++kb) {
           if (!(ok = mbar_wait(empty + stage, phase ^ 1, err))) break;
           mbar_arrive_expect_tx(full + stage, STAGE_BYTES);
@@ -134,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int m_blk = tile % m_tiles, n_blk = tile / m_tiles;
+      const int m_blk = tile / n_tiles, n_blk = tile % n_tiles;
       if (!mbar_wait(tfull + acc, acc_phase, err)) break;
       tc_fence_after();
       const int row = m_blk * BM + row_in_tile;
