@@ -52,13 +52,13 @@ struct Bars {
   uint64_t* s_empty;    // [4] own-column input tile consumed
   uint64_t* x_full;     // [8] every writer has written this CTA's part of an exchange slot
   uint64_t* x_free;     // [8] every reader has fetched its part of an exchange slot
-  uint64_t* r_full;     // [2] fetched part landed in shared memory
-  uint64_t* r_empty;    // [2] fetched part consumed
+  uint64_t* r_full;     // [4] fetched part landed in shared memory
+  uint64_t* r_empty;    // [4] fetched part consumed
   uint64_t* a_full;     // [2] accumulators ready
   uint64_t* a_empty;    // [2] accumulators drained
   uint64_t* q_full;     // [1] one-time operand staged (Q blocks; the dQ sums)
-  uint64_t* v_full;     // [2] second, unpermuted operand landed (TMA)
-  uint64_t* v_empty;    // [2] second operand consumed
+  uint64_t* v_full;     // [4] second, unpermuted operand landed (TMA)
+  uint64_t* v_empty;    // [4] second operand consumed
   uint64_t* moved;      // [8] this CTA's writers have stored their rows of an exchange slot
   uint32_t* tmem_slot;
 };
@@ -71,14 +71,14 @@ __device__ __forceinline__ Bars bars_at(uint8_t* smem) {
   r.x_full = b + 8;
   r.x_free = b + 16;
   r.r_full = b + 24;
-  r.r_empty = b + 26;
-  r.a_full = b + 28;
-  r.a_empty = b + 30;
-  r.q_full = b + 32;
-  r.v_full = b + 33;
-  r.v_empty = b + 35;
-  r.moved = b + 37;
-  r.tmem_slot = reinterpret_cast<uint32_t*>(b + 45);
+  r.r_empty = b + 28;
+  r.a_full = b + 32;
+  r.a_empty = b + 34;
+  r.q_full = b + 36;
+  r.v_full = b + 37;
+  r.v_empty = b + 41;
+  r.moved = b + 45;
+  r.tmem_slot = reinterpret_cast<uint32_t*>(b + 53);   // 432 bytes in all, under kTableOff
   return r;
 }
 
@@ -95,13 +95,15 @@ __device__ __forceinline__ void init_bars(const Bars& br, int C, uint32_t s_empt
     mbar_init(br.s_full + i, 1);
     mbar_init(br.s_empty + i, s_empty_count);
   }
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < 4; ++i) {
     mbar_init(br.r_full + i, 1);
     mbar_init(br.r_empty + i, r_empty_count);
-    mbar_init(br.a_full + i, 1);
-    mbar_init(br.a_empty + i, 128);
     mbar_init(br.v_full + i, 1);
     mbar_init(br.v_empty + i, 1);
+  }
+  for (int i = 0; i < 2; ++i) {
+    mbar_init(br.a_full + i, 1);
+    mbar_init(br.a_empty + i, 128);
   }
   mbar_init(br.q_full, 1);
   fence_mbar_init();
