@@ -551,12 +551,14 @@ bool ca_geometry(int d, int b, bool gather, CaGeo* out) {
     const int table = 4 * (gather ? g.F : g.G * b);
     g.hdr = (kTableOff + table + 1023) / 1024 * 1024;
     const int qstage = g.G * b * b * 2;   // staged in the pipeline buffers before first use
-    // deeper input rings first (they hide the HBM latency), then double
-    // output staging (the TMA store of one tile overlaps the next)
-    const int cand[8][3] = {{4, 2, 2}, {3, 2, 2}, {4, 1, 2}, {3, 1, 2},
+    // three fetched parts first (the exchange hand-off is the longest wait;
+    // measured best at the square 2048 layer), then deeper input rings (they
+    // hide the HBM latency), then double output staging (the TMA store of one
+    // tile overlaps the next)
+    const int cand[9][3] = {{2, 2, 3}, {4, 2, 2}, {3, 2, 2}, {4, 1, 2}, {3, 1, 2},
                             {2, 2, 2}, {2, 1, 2}, {2, 1, 1}, {1, 1, 1}};
     bool found = false;
-    for (int ci = 0; ci < 8 && !found; ++ci) {
+    for (int ci = 0; ci < 9 && !found; ++ci) {
       const int NS = cand[ci][0], NST = cand[ci][1], NR = cand[ci][2];
       const int body = NS * g.s_bytes + NR * g.r_bytes + NST * g.st_bytes;
       const int smem = 1024 + g.hdr + body;

@@ -252,9 +252,11 @@ bool dq_geometry(int d, int b, DqGeo* out) {
     g.r_bytes = g.G * b * TT * 2;
     g.v_bytes = g.G * b * TT * 2;
     g.hdr = (kTableOff + 4 * g.F + 1023) / 1024 * 1024;
-    const int cand[6][3] = {{3, 2, 2}, {2, 2, 2}, {2, 2, 1}, {2, 1, 1}, {1, 2, 1}, {1, 1, 1}};
+    // (input, fetched, second operand) stages; a third second-operand stage
+    // first (measured best at the square 2048 layer)
+    const int cand[7][3] = {{2, 2, 3}, {3, 2, 2}, {2, 2, 2}, {2, 2, 1}, {2, 1, 1}, {1, 2, 1}, {1, 1, 1}};
     bool found = false;
-    for (int ci = 0; ci < 6 && !found; ++ci) {
+    for (int ci = 0; ci < 7 && !found; ++ci) {
       const int smem = 1024 + g.hdr + cand[ci][0] * g.s_bytes + cand[ci][1] * g.r_bytes +
                        cand[ci][2] * g.v_bytes;
       // the epilogue's transpose tiles live in the input ring
