@@ -95,3 +95,39 @@ def test_host_validation_rejects_before_launch(lib):
     bargs = [null] * 5 + [0] + [null] * 7 + [16, 256, 256, 32, 32, _lib.F32, null, null, null,
                                             null, 0, null]
     assert bwd(*bargs) == 1                                   # n < 1
+
+
+def test_fold_and_xq_host_logic(lib):
+    """Workspace sizes and argument checks of the inner-loop fold and POET-XQ
+    entry points (host only: every call here returns before any launch)."""
+    null = None
+    fb = lib.poetx_fold_workspace_bytes
+    # one [d_out, d_in] matrix at least; invalid sizes give 0
+    assert fb(384, 256, 32, 64, _lib.BF16) >= 384 * 256 * 2
+    assert fb(384, 256, 32, 64, _lib.F32) >= 384 * 256 * 4
+    assert fb(384, 250, 32, 64, _lib.F32) == 0          # d_in % b_in != 0
+    assert fb(384, 256, 24, 64, _lib.F32) == 0          # b not a power of two
+    assert fb(384, 256, 32, 64, 5) == 0                 # bad dtype
+    fold = lib.poetx_fold_w0
+    ok_ptr = ctypes.c_void_p(4096)
+    args = [ok_ptr] * 5
+    assert fold(*args, 384, 256, 32, 64, _lib.F32, ok_ptr, ok_ptr, 0, null) == 2   # workspace too small
+    assert fold(*args, 384, 256, 32, 64, 7, ok_ptr, ok_ptr, 1 << 30, null) == 1    # bad dtype
+    assert fold(null, *args[1:], 384, 256, 32, 64, _lib.F32, ok_ptr, ok_ptr, 1 << 30, null) == 1
+    assert fold(*args, 384, 256, 48, 64, _lib.F32, ok_ptr, ok_ptr, 1 << 30, null) == 3  # b_in = 48
+    # POET-XQ: the workspace adds the dequantised weight to the layer's
+    wq, w = lib.poetx_workspace_bytes_xq, lib.poetx_workspace_bytes
+    for dt, es in ((_lib.F32, 4), (_lib.BF16, 2)):
+        extra = -(-2048 * 2048 * es // 256) * 256
+        assert wq(1024, 2048, 2048, 256, 256, dt) == w(1024, 2048, 2048, 256, 256, dt) + extra
+    assert wq(64, 250, 256, 2, 32, _lib.F32) == 0       # d_in % 4 != 0 is not supported
+    q = lib.poetx_quantize_w0
+    assert q(ok_ptr, 16, 10, _lib.F32, ok_ptr, ok_ptr, null) == 2       # d_in % 4 != 0
+    assert q(ok_ptr, 16, 16, 9, ok_ptr, ok_ptr, null) == 1              # bad dtype
+    assert q(ok_ptr, 16, 16, _lib.F32, null, ok_ptr, null) == 1         # null codes
+    assert q(ctypes.c_void_p(4100), 16, 16, _lib.F32, ok_ptr, ok_ptr, null) == 1   # misaligned
+    dq = lib.poetx_dequantize_w0
+    assert dq(ok_ptr, null, 16, 16, _lib.BF16, ok_ptr, null) == 1       # null scales
+    assert dq(ok_ptr, ok_ptr, 0, 16, _lib.BF16, ok_ptr, null) == 2      # no rows
+    fx = lib.poetx_forward_xq
+    assert fx(*([ok_ptr] * 9), 64, 256, 256, 32, 32, _lib.F32, ok_ptr, null, ok_ptr, 0, null) == 2
