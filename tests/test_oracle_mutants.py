@@ -96,3 +96,46 @@ def test_mutant_is_caught_by_a_pin(name, old, new, tmpdir_mod):
     finally:
         oracle._LIB = saved
     assert caught, "no pin caught the planted mistake: " + name
+
+
+# ---- the oracle's numpy-level functions (the fold, the INT8 quantiser): the
+# mutated function is a copy of the oracle's own source with one change,
+# compiled into a namespace of its own and swapped in for the pins' calls.
+PY_MUTANTS = [
+    ("fold: P-side permutation transposed", "fold_w0",
+     "P = Pi_P.T @ blockdiag(QP) @ Pi_P", "P = Pi_P @ blockdiag(QP) @ Pi_P.T"),
+    ("fold: R blocks transposed", "fold_w0",
+     "R = Pi_R.T @ blockdiag(QR) @ Pi_R", "R = Pi_R.T @ blockdiag(QR).T @ Pi_R"),
+    ("fold: R applied as its transpose", "fold_w0", "return R @ W0 @ P", "return R.T @ W0 @ P"),
+    ("quantiser: truncation instead of rounding", "quantize_rows_int8",
+     "np.rint(W[nz] / s[nz, None])", "np.trunc(W[nz] / s[nz, None])"),
+    ("quantiser: ties away from zero", "quantize_rows_int8",
+     "np.rint(W[nz] / s[nz, None])", "np.sign(W[nz]) * np.floor(np.abs(W[nz] / s[nz, None]) + 0.5)"),
+    ("quantiser: scale over 128", "quantize_rows_int8", "np.float32(127)", "np.float32(128)"),
+]
+
+PY_PIN_CALLS = [
+    ("fold = effective weight", lambda: pins.test_fold_w0_is_the_effective_weight((8, 12, 4, 6, 3))),
+    ("fold keeps the function", lambda: pins.test_fold_then_fresh_permutations_and_zero_theta_keep_the_function()),
+    ("quantiser golden", lambda: pins.test_quantize_rows_int8_golden()),
+    ("quantiser bounds", lambda: pins.test_quantize_rows_int8_bounds_and_round_trip_error()),
+]
+
+
+@pytest.mark.parametrize("name,fn,old,new", PY_MUTANTS, ids=[m[0] for m in PY_MUTANTS])
+def test_python_mutant_is_caught_by_a_pin(name, fn, old, new, monkeypatch):
+    import inspect
+    import textwrap
+    src = textwrap.dedent(inspect.getsource(getattr(oracle, fn)))
+    assert src.count(old) == 1, "mutation anchor not found: " + name
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), "<mutant %s>" % name, "exec"), ns)
+    monkeypatch.setattr(oracle, fn, ns[fn])
+    caught = []
+    for pin_name, call in PY_PIN_CALLS:
+        try:
+            with np.errstate(all="ignore"):
+                call()
+        except (AssertionError, ValueError, ArithmeticError):
+            caught.append(pin_name)
+    assert caught, "no pin caught the planted mistake: " + name
