@@ -405,9 +405,27 @@ def workload_config(world):
                 ROTATE, ROTATE * 2 * CASE.T * CASE.d_in * 2 // 2 ** 20)}
 
 
-def cnp_points(dev):
-    """Cayley-Neumann generation throughput at 4096 blocks, n = 3, sigma = 1e-2."""
-    out = {}
+def cnp_roofline_point(b, out_bytes, n, nblocks, seconds, peaks):
+    """Roofline of one Cayley-Neumann generation call: algorithmic bytes (packed
+    theta in, Q out) and flops (n products of b x b x b per block) against the
+    measured HBM and bf16 tensor peaks; fp32 Q runs on the CUDA cores, so its
+    points carry the HBM fraction only."""
+    byts = nblocks * (4 * (b * (b - 1) // 2) + out_bytes * b * b)
+    flops = nblocks * 2.0 * n * b ** 3
+    t_hbm = byts / (peaks["hbm_gbs"] * 1e9)
+    out = {"gbs": round(byts / seconds / 1e9, 1), "tflops": round(flops / seconds / 1e12, 2),
+           "hbm_frac": round(t_hbm / seconds, 4)}
+    if out_bytes == 2:
+        t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+        out["bound"] = "hbm" if t_hbm >= t_tc else "tensor"
+        out["frac"] = round(max(t_hbm, t_tc) / seconds, 4)
+    return out
+
+
+def cnp_points(dev, peaks):
+    """Cayley-Neumann generation throughput at 4096 blocks, n = 3, sigma = 1e-2,
+    and each point's roofline fraction."""
+    out, roof = {}, {}
     for b in (32, 64, 128, 256):
         th = inputs.make_theta(4096, b, 1e-2, inputs.sweep_seed(b, 1e-2, 3)).to(dev)
         for dt, nm in ((torch.float32, "f32"), (torch.bfloat16, "bf16")):
@@ -424,8 +442,10 @@ def cnp_points(dev):
             torch.cuda.synchronize()
             ms = e0.elapsed_time(e1) / reps
             out["b%d_%s" % (b, nm)] = round(4096 / (ms * 1e-3))
+            roof["b%d_%s" % (b, nm)] = cnp_roofline_point(b, Q.element_size(), 3, 4096, ms * 1e-3,
+                                                          peaks)
         del th, Q
-    return out
+    return out, roof
 
 
 def fold_point(lay, dev, peaks):
@@ -675,7 +695,7 @@ def run_poetx(args, world, rank, local):
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "copies": "pinned host buffers; uploads and downloads on their own streams, double-buffered"}
 
-    cnp = cnp_points(dev) if rank == 0 else None
+    cnp, cnp_roof = cnp_points(dev, peaks) if rank == 0 else (None, None)
     fold = fold_point(lay, dev, peaks) if rank == 0 else None
     xq = xq_point(case, inp, lay, xs, dys, y, dX, dev) if rank == 0 else None
 
@@ -702,7 +722,7 @@ def run_poetx(args, world, rank, local):
             "data": "synthetic", "config": workload_config(world),
             "step_tflops": round(flops / (ms_per_step * 1e-3) / 1e12 / 1, 2),
             "step_frac_of_bf16_peak": round(flops / (ms_per_step * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-            "cnp_blocks_per_s": cnp, "fold_w0": fold, "xq": xq, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "cnp_blocks_per_s": cnp, "cnp_roofline": cnp_roof, "fold_w0": fold, "xq": xq, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(launches), "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)

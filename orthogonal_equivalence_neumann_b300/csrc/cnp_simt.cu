@@ -225,6 +225,102 @@ __global__ void __launch_bounds__(kThreads) cnp_bwd_kernel(const float* __restri
   }
 }
 
+// Forward for small blocks (b = 16, 32, 64): one CTA holds a whole block, K
+// and the running factor in shared memory, and evaluates the truncated
+// series in Horner form,
+//   H_1 = 2I + K,  H_{s+1} = 2I + K H_s,  Q = I + K H_n
+// (= I + 2K + ... + 2K^n + K^{n+1}): n products of b x b.  Each thread owns
+// OUT = b*b/256 entries of one row, in groups of four columns 4*TPR apart so
+// that the threads of a row read one contiguous row of H per step.
+template <int B, typename OutT>
+__global__ void __launch_bounds__(kThreads) cnp_fwd_small_kernel(const float* __restrict__ theta,
+                                                                 int n, OutT* __restrict__ Q) {
+  constexpr int OUT = B * B / kThreads;   // entries per thread: 1, 4, 16
+  constexpr int TPR = B / OUT;            // threads per row: 16, 8, 4
+  constexpr int NP = B * (B - 1) / 2;
+  constexpr int LDK = B + 1;
+  __shared__ float ths[NP];
+  __shared__ float Ks[B * LDK];
+  __shared__ __align__(16) float Hs[B * B];
+  const int j = blockIdx.x;
+  const float* th = theta + (size_t)j * NP;
+  for (int e = threadIdx.x; e < NP; e += kThreads) ths[e] = __ldg(th + e);
+  __syncthreads();
+  for (int e = threadIdx.x; e < B * B; e += kThreads) {
+    const int i = e / B, k = e % B;
+    Ks[i * LDK + k] = k > i ? ths[skew_index(i, k, B)] : (k < i ? -ths[skew_index(k, i, B)] : 0.f);
+  }
+  __syncthreads();
+  const int row = threadIdx.x / TPR;
+  const int lane_c = threadIdx.x % TPR;
+  // column of the thread's entry (q-th group of four, e-th in the group)
+  auto col = [&](int q, int e) { return OUT >= 4 ? lane_c * 4 + q * 4 * TPR + e : lane_c; };
+  constexpr int NG = OUT >= 4 ? OUT / 4 : 1;   // groups of four
+  constexpr int GE = OUT >= 4 ? 4 : 1;         // entries per group
+#pragma unroll
+  for (int q = 0; q < NG; ++q)
+#pragma unroll
+    for (int e = 0; e < GE; ++e) {
+      const int c = col(q, e);
+      Hs[row * B + c] = Ks[row * LDK + c] + (row == c ? 2.f : 0.f);
+    }
+  __syncthreads();
+  float acc[OUT];
+  for (int step = 1; step <= n; ++step) {
+#pragma unroll
+    for (int t = 0; t < OUT; ++t) acc[t] = 0.f;
+#pragma unroll 4
+    for (int k = 0; k < B; ++k) {
+      const float a = Ks[row * LDK + k];
+      if constexpr (OUT >= 4) {
+#pragma unroll
+        for (int q = 0; q < NG; ++q) {
+          const float4 h = *reinterpret_cast<const float4*>(Hs + k * B + col(q, 0));
+          acc[4 * q + 0] = fmaf(a, h.x, acc[4 * q + 0]);
+          acc[4 * q + 1] = fmaf(a, h.y, acc[4 * q + 1]);
+          acc[4 * q + 2] = fmaf(a, h.z, acc[4 * q + 2]);
+          acc[4 * q + 3] = fmaf(a, h.w, acc[4 * q + 3]);
+        }
+      } else {
+        acc[0] = fmaf(a, Hs[k * B + col(0, 0)], acc[0]);
+      }
+    }
+    if (step < n) {
+      __syncthreads();   // every thread is done reading H_s
+#pragma unroll
+      for (int q = 0; q < NG; ++q)
+#pragma unroll
+        for (int e = 0; e < GE; ++e) {
+          const int c = col(q, e);
+          Hs[row * B + c] = acc[q * GE + e] + (row == c ? 2.f : 0.f);
+        }
+      __syncthreads();
+    }
+  }
+  OutT* qrow = Q + (size_t)j * B * B + (size_t)row * B;
+#pragma unroll
+  for (int q = 0; q < NG; ++q)
+#pragma unroll
+    for (int e = 0; e < GE; ++e) {
+      const int c = col(q, e);
+      qrow[c] = from_f32<OutT>(acc[q * GE + e] + (row == c ? 1.f : 0.f));
+    }
+}
+
+template <int B>
+poetx_status launch_cnp_fwd_small(const float* theta, int nb, int n, void* Q, poetx_dtype out_dtype,
+                                  cudaStream_t s) {
+  if (nb <= 0) return POETX_OK;
+  {
+    KernelScope ks_("cnp_fwd_simt", s);
+    if (out_dtype == POETX_F32)
+      cnp_fwd_small_kernel<B, float><<<nb, kThreads, 0, s>>>(theta, n, (float*)Q);
+    else
+      cnp_fwd_small_kernel<B, __nv_bfloat16><<<nb, kThreads, 0, s>>>(theta, n, (__nv_bfloat16*)Q);
+  }
+  return check_launch();
+}
+
 }  // namespace
 
 size_t cnp_fwd_simt_smem(int b) {
@@ -241,6 +337,9 @@ size_t cnp_bwd_simt_smem(int b) {
 
 poetx_status launch_cnp_fwd_simt(const float* theta, int nb, int b, int n, void* Q,
                                  poetx_dtype out_dtype, cudaStream_t s) {
+  if (b == 16) return launch_cnp_fwd_small<16>(theta, nb, n, Q, out_dtype, s);
+  if (b == 32) return launch_cnp_fwd_small<32>(theta, nb, n, Q, out_dtype, s);
+  if (b == 64) return launch_cnp_fwd_small<64>(theta, nb, n, Q, out_dtype, s);
   const int rows = b < kRowSlab ? b : kRowSlab;
   dim3 grid(b / rows, nb);
   const size_t smem = cnp_fwd_simt_smem(b);
