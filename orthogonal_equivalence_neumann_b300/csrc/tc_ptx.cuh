@@ -110,12 +110,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
   return r;
 }
 
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-
 // Remote (cluster) arrive on an mbarrier of CTA `rank`, release at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
@@ -151,24 +145,6 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
   return false;
 }
 
-// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory into
-// the shared memory of a CTA of the cluster (both addresses 16-byte aligned);
-// the bytes count against that CTA's mbarrier `remote_bar` (complete_tx).
-__device__ __forceinline__ void bulk_copy_s2s(uint32_t remote_dst, uint32_t local_src, uint32_t bytes,
-                                              uint32_t remote_bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(remote_dst),
-      "r"(local_src), "r"(bytes), "r"(remote_bar)
-      : "memory");
-}
-
-// Orders this thread's prior memory accesses (and, cumulatively, those it has
-// observed, e.g. through a CTA barrier) before its later ones, cluster-wide.
-__device__ __forceinline__ void fence_acq_rel_cluster() {
-  asm volatile("fence.acq_rel.cluster;" ::: "memory");
-}
-
 // Makes global-memory data observed through the generic proxy visible to this
 // thread's subsequent async-proxy (TMA / bulk copy) accesses.
 __device__ __forceinline__ void fence_proxy_async_global() {
@@ -182,16 +158,6 @@ __device__ __forceinline__ void bulk_load_g2s(void* dst, const void* src, uint32
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// 16-byte asynchronous store into the shared memory of a CTA of the cluster;
-// its bytes count against that CTA's mbarrier `remote_bar` (complete_tx).
-__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint4 v, uint32_t remote_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
-          "r"(remote_addr),
-      "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
       : "memory");
 }
 
@@ -292,16 +258,6 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
