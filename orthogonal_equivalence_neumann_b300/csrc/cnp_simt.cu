@@ -225,9 +225,20 @@ __global__ void __launch_bounds__(kThreads) cnp_bwd_kernel(const float* __restri
   }
 }
 
-// Forward for small blocks (b = 16, 32, 64): one CTA holds a whole block, K
-// and the running factor in shared memory, and evaluates the truncated
-// series in Horner form,
+// Shared-memory layout of the one-CTA-per-block forward: the packed
+// parameters, K with a padded row, then H (16-byte aligned).
+template <int B>
+__host__ __device__ constexpr int small_fwd_h_off() {
+  return ((B * (B - 1) / 2 + B * (B + 1)) + 3) / 4 * 4;
+}
+template <int B>
+constexpr size_t small_fwd_smem() {
+  return sizeof(float) * ((size_t)small_fwd_h_off<B>() + (size_t)B * B);
+}
+
+// Forward for blocks up to b = 128: one CTA holds a whole block, K and the
+// running factor in shared memory, and evaluates the truncated series in
+// Horner form,
 //   H_1 = 2I + K,  H_{s+1} = 2I + K H_s,  Q = I + K H_n
 // (= I + 2K + ... + 2K^n + K^{n+1}): n products of b x b.  Each thread owns
 // OUT = b*b/256 entries of one row, in groups of four columns 4*TPR apart so
@@ -235,13 +246,14 @@ __global__ void __launch_bounds__(kThreads) cnp_bwd_kernel(const float* __restri
 template <int B, typename OutT>
 __global__ void __launch_bounds__(kThreads) cnp_fwd_small_kernel(const float* __restrict__ theta,
                                                                  int n, OutT* __restrict__ Q) {
-  constexpr int OUT = B * B / kThreads;   // entries per thread: 1, 4, 16
-  constexpr int TPR = B / OUT;            // threads per row: 16, 8, 4
+  constexpr int OUT = B * B / kThreads;   // entries per thread: 1, 4, 16, 64
+  constexpr int TPR = B / OUT;            // threads per row: 16, 8, 4, 2
   constexpr int NP = B * (B - 1) / 2;
   constexpr int LDK = B + 1;
-  __shared__ float ths[NP];
-  __shared__ float Ks[B * LDK];
-  __shared__ __align__(16) float Hs[B * B];
+  extern __shared__ float small_smem[];   // small_fwd_smem<B>() bytes
+  float* ths = small_smem;                                 // [NP] packed parameters
+  float* Ks = small_smem + small_fwd_h_off<B>() - B * LDK;  // [B][LDK]
+  float* Hs = small_smem + small_fwd_h_off<B>();           // [B][B], 16-byte aligned
   const int j = blockIdx.x;
   const float* th = theta + (size_t)j * NP;
   for (int e = threadIdx.x; e < NP; e += kThreads) ths[e] = __ldg(th + e);
@@ -311,12 +323,17 @@ template <int B>
 poetx_status launch_cnp_fwd_small(const float* theta, int nb, int n, void* Q, poetx_dtype out_dtype,
                                   cudaStream_t s) {
   if (nb <= 0) return POETX_OK;
+  constexpr size_t smem = small_fwd_smem<B>();
   {
     KernelScope ks_("cnp_fwd_simt", s);
-    if (out_dtype == POETX_F32)
-      cnp_fwd_small_kernel<B, float><<<nb, kThreads, 0, s>>>(theta, n, (float*)Q);
-    else
-      cnp_fwd_small_kernel<B, __nv_bfloat16><<<nb, kThreads, 0, s>>>(theta, n, (__nv_bfloat16*)Q);
+    if (out_dtype == POETX_F32) {
+      set_max_dynamic_smem((const void*)cnp_fwd_small_kernel<B, float>, (int)smem);
+      cnp_fwd_small_kernel<B, float><<<nb, kThreads, smem, s>>>(theta, n, (float*)Q);
+    } else {
+      set_max_dynamic_smem((const void*)cnp_fwd_small_kernel<B, __nv_bfloat16>, (int)smem);
+      cnp_fwd_small_kernel<B, __nv_bfloat16><<<nb, kThreads, smem, s>>>(theta, n,
+                                                                        (__nv_bfloat16*)Q);
+    }
   }
   return check_launch();
 }
@@ -340,6 +357,7 @@ poetx_status launch_cnp_fwd_simt(const float* theta, int nb, int b, int n, void*
   if (b == 16) return launch_cnp_fwd_small<16>(theta, nb, n, Q, out_dtype, s);
   if (b == 32) return launch_cnp_fwd_small<32>(theta, nb, n, Q, out_dtype, s);
   if (b == 64) return launch_cnp_fwd_small<64>(theta, nb, n, Q, out_dtype, s);
+  if (b == 128) return launch_cnp_fwd_small<128>(theta, nb, n, Q, out_dtype, s);
   const int rows = b < kRowSlab ? b : kRowSlab;
   dim3 grid(b / rows, nb);
   const size_t smem = cnp_fwd_simt_smem(b);
