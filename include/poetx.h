@@ -218,7 +218,9 @@ poetx_status poetx_backward(const void *x, const void *dy, const void *W0m, cons
  *     d_in = d_out = 2048 in bf16).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *     that first call before any stream capture.  The cached address belongs
+ *     to the device's current context: calls must not span a
+ *     cudaDeviceReset (which may reload the library's device code elsewhere).
  *   - Every call on a device shares the one array, which keeps the last
  *     call's contents; calls that overlap on the GPU (on streams with no
  *     ordering between them) race on it and must be serialised by the
@@ -274,6 +276,17 @@ poetx_status poetx_backward_xq(const void *x, const void *dy, const int8_t *W0q,
                                int d_out, int b_in, int b_out, poetx_dtype act_dtype, void *dX,
                                float *dtheta_P, float *dtheta_R, void *workspace,
                                size_t ws_bytes, cudaStream_t stream);
+
+/* Diagnostic of the failure path (no counterpart on the page): launches one
+ * thread that waits, through the same bounded wait as every tensor-core
+ * kernel, on an mbarrier in its own shared memory that nothing arrives on.
+ * After `polls` polls (1 <= polls <= 2^20; cluster_scope 0 = the CTA-scope
+ * wait, 1 = the cluster-scope wait) it gives up and records
+ * POETX_ERR_TIMEOUT in the device error word, which the next
+ * poetx_stream_status() on `stream` returns (and clears).  Nothing else is
+ * touched: the context stays usable.  Returns POETX_ERR_INVALID_ARG for
+ * arguments out of range, else the launch status. */
+poetx_status poetx_diag_expire_wait(int cluster_scope, unsigned polls, cudaStream_t stream);
 
 /* Synchronises `stream` and reports the first error since the last call:
  * a CUDA error (POETX_ERR_CUDA) or an expired device-side wait

@@ -268,9 +268,28 @@ def orth_error(Q):
 
 
 def rel_fro(got, ref):
-    """Relative Frobenius error ||got - ref||_F / ||ref||_F (the parity metric)."""
+    """Relative Frobenius error ||got - ref||_F / ||ref||_F (the parity metric).
+
+    An all-zero reference gives the absolute error ||got||_F instead."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     den = np.linalg.norm(ref.ravel())
     num = np.linalg.norm((got - ref).ravel())
     return num / den if den > 0 else num
+
+
+def rel_fro_rows(got, ref):
+    """The same metric for every slice along the first axis (a token row of an
+    activation, one block of Q, the packed parameters of one block):
+    ||got[i] - ref[i]||_F / ||ref[i]||_F, or the absolute ||got[i]||_F where
+    ref[i] is all zeros.  Returns a vector of length shape[0]."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    g = got.reshape(got.shape[0], -1)
+    r = ref.reshape(ref.shape[0], -1)
+    den = np.sqrt((r * r).sum(axis=1))
+    num = np.sqrt(((g - r) ** 2).sum(axis=1))
+    out = num.copy()
+    nz = den > 0
+    out[nz] = num[nz] / den[nz]
+    return out

@@ -27,7 +27,8 @@ EXPORTS = ["poetx_status_string", "poetx_version", "poetx_cayley_neumann",
            "poetx_stream_status", "poetx_launch_count", "poetx_profile_enable",
            "poetx_profile_report", "poetx_forward_noalloc", "poetx_fold_workspace_bytes",
            "poetx_fold_w0", "poetx_quantize_w0", "poetx_dequantize_w0",
-           "poetx_workspace_bytes_xq", "poetx_forward_xq", "poetx_backward_xq"]
+           "poetx_workspace_bytes_xq", "poetx_forward_xq", "poetx_backward_xq",
+           "poetx_diag_expire_wait"]
 
 
 class PoetxError(RuntimeError):
@@ -63,6 +64,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "poetx_backward": (I, [P, P, P, P, P, I, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P,
                                P, Z, P]),
         "poetx_stream_status": (I, [P]),
+        "poetx_diag_expire_wait": (I, [I, U, P]),
         "poetx_forward_noalloc": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P]),
         "poetx_launch_count": (ctypes.c_ulonglong, []),
         "poetx_profile_enable": (I, [I]),
@@ -253,6 +255,12 @@ def poetx_backward_xq(x, dy, W0q, scale, theta_P, theta_R, n, Q_P, Q_R, z_saved,
 
 def poetx_stream_status(stream=None):
     _check("poetx_stream_status", load().poetx_stream_status(_stream(stream)))
+
+
+def poetx_diag_expire_wait(cluster_scope: int, polls: int, stream=None):
+    """Launch one bounded device wait that runs out (the failure path's check)."""
+    _check("poetx_diag_expire_wait", load().poetx_diag_expire_wait(cluster_scope, polls,
+                                                                   _stream(stream)))
 
 
 def poetx_launch_count() -> int:

@@ -81,12 +81,16 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits until the phase of `bar` with parity `parity` has completed.  Gives
-// up after kWaitLimit polls: records POETX_ERR_TIMEOUT and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
+// up after `limit` polls: records POETX_ERR_TIMEOUT and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit,
+                                                  int* err) {
+  for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   raise_device_error(err, POETX_ERR_TIMEOUT);
   return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+  return mbar_wait_bounded(bar, parity, kWaitLimit, err);
 }
 
 // ---------------------------------------------------------------- clusters
@@ -138,11 +142,15 @@ __device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t* bar, uint32_t p
 }
 
 // As mbar_wait, for barriers that other CTAs of the cluster arrive on.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int* err) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity,
+                                                          uint32_t limit, int* err) {
+  for (uint32_t i = 0; i < limit; ++i)
     if (mbar_test_wait_cluster(bar, parity)) return true;
   raise_device_error(err, POETX_ERR_TIMEOUT);
   return false;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int* err) {
+  return mbar_wait_cluster_bounded(bar, parity, kWaitLimit, err);
 }
 
 // Makes global-memory data observed through the generic proxy visible to this

@@ -131,3 +131,11 @@ def test_fold_and_xq_host_logic(lib):
     assert dq(ok_ptr, ok_ptr, 0, 16, _lib.BF16, ok_ptr, null) == 2      # no rows
     fx = lib.poetx_forward_xq
     assert fx(*([ok_ptr] * 9), 64, 256, 256, 32, 32, _lib.F32, ok_ptr, null, ok_ptr, 0, null) == 2
+
+
+def test_diag_expire_wait_rejects_bad_arguments(lib):
+    # host checks only: nothing is launched for arguments out of range
+    assert lib.poetx_diag_expire_wait(2, 10, None) == 1
+    assert lib.poetx_diag_expire_wait(-1, 10, None) == 1
+    assert lib.poetx_diag_expire_wait(0, 0, None) == 1
+    assert lib.poetx_diag_expire_wait(1, (1 << 20) + 1, None) == 1

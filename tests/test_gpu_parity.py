@@ -1,8 +1,9 @@
 """GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
 
-Bars (relative Frobenius error ||gpu - oracle||_F / ||oracle||_F per output):
-fp32 paths <= 1e-5; bf16-input / fp32-accumulate paths <= 2e-2; permutation
-indices and the merged weight bit-exact.  The oracle reads exactly the values
+Bars (relative Frobenius error ||gpu - oracle||_F / ||oracle||_F per output,
+and the same bar on each token row / block of it): fp32 paths <= 1e-5;
+bf16-input / fp32-accumulate paths <= 2e-2; permutation indices and the merged
+weight bit-exact.  The oracle reads exactly the values
 the GPU reads (bf16 inputs widened exactly to double) and rounds nothing.
 """
 import numpy as np
@@ -27,8 +28,20 @@ def tol_for(dtype):
 
 
 def assert_close(name, got, ref, tol):
+    """The bar on the whole tensor, and the same bar on every slice along the
+    first axis (a token row of y or dX, one block of Q, the packed parameters
+    of one block), so that a few wrong rows or one wrong tile cannot hide in
+    the norm of a large tensor."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, "%s: shape %s != %s" % (name, got.shape, ref.shape)
     err = oracle.rel_fro(got, ref)
     assert err <= tol, "%s: relative Frobenius error %.3e > %.1e" % (name, err, tol)
+    if ref.ndim >= 2 and ref.shape[0] > 1:
+        per = oracle.rel_fro_rows(got, ref)
+        worst = int(np.argmax(per))
+        assert per[worst] <= tol, "%s: slice %d of %d has relative error %.3e > %.1e" % (
+            name, worst, ref.shape[0], per[worst], tol)
     return err
 
 
@@ -123,6 +136,22 @@ def test_cnp_sweep_full_size_sampled_blocks(b, sigma, n, out):
         q2 = np.linalg.norm(ref, ord=2, axis=(1, 2))
         bound = 2 * q2 * dq + dq ** 2 + 4 * b * 2.0 ** -24
         assert np.all(np.abs(e_got - e_ref) <= bound), (e_got, e_ref, bound)
+
+
+def test_cnp_bf16_b128_beyond_the_tensor_core_grid():
+    """Above 65535 blocks the bf16 Q at b = 128 comes from the CUDA-core Horner
+    kernel instead of the tensor-core chain: 65541 blocks (2.1 GB of theta and
+    of Q), blocks sampled at both ends and in between against the oracle."""
+    nb, b, n = 65541, 128, 3
+    th = inputs.make_theta(nb, b, 0.01, 5150)
+    Q = torch.empty(nb, b, b, dtype=torch.bfloat16, device="cuda")
+    _lib.poetx_cayley_neumann(th.cuda(), b, n, Q)
+    _lib.poetx_stream_status()
+    idx = np.array([0, 1, 777, 32768, 65534, 65535, 65536, nb - 1])
+    ref = oracle.cnp(th[idx].double().numpy(), b, n)
+    assert_close("Q", to64(Q[torch.as_tensor(idx, device="cuda")]), ref, TOL_BF16)
+    del Q
+    torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("b,n", [(2, 1), (4, 3), (32, 4), (64, 2), (128, 3), (256, 3), (256, 6)])

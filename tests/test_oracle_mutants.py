@@ -112,6 +112,22 @@ PY_MUTANTS = [
     ("quantiser: ties away from zero", "quantize_rows_int8",
      "np.rint(W[nz] / s[nz, None])", "np.sign(W[nz]) * np.floor(np.abs(W[nz] / s[nz, None]) + 0.5)"),
     ("quantiser: scale over 128", "quantize_rows_int8", "np.float32(127)", "np.float32(128)"),
+    ("parity metric: divided by the result's norm", "rel_fro",
+     "den = np.linalg.norm(ref.ravel())", "den = np.linalg.norm(got.ravel())"),
+    ("parity metric: squared ratio", "rel_fro",
+     "return num / den if den > 0 else num", "return (num / den) ** 2 if den > 0 else num"),
+    ("parity metric: largest entry instead of the norm", "rel_fro",
+     "num = np.linalg.norm((got - ref).ravel())", "num = np.abs(got - ref).max()"),
+    ("per-row metric: rows against the whole tensor's norm", "rel_fro_rows",
+     "den = np.sqrt((r * r).sum(axis=1))", "den = np.full(r.shape[0], np.sqrt((r * r).sum()))"),
+    ("per-row metric: largest entry of a row", "rel_fro_rows",
+     "num = np.sqrt(((g - r) ** 2).sum(axis=1))", "num = np.sqrt(((g - r) ** 2).max(axis=1))"),
+    ("orthogonality defect: Q Q without the transpose", "orth_error",
+     "np.swapaxes(Q, -1, -2) @ Q", "Q @ Q"),
+    ("orthogonality defect: identity not subtracted", "orth_error", " - eye) ** 2", ") ** 2"),
+    ("orthogonality defect: no square root", "orth_error", "return np.sqrt(", "return ("),
+    ("orthogonality defect: summed over all blocks", "orth_error",
+     ".sum(axis=(-1, -2))", ".sum()"),
 ]
 
 PY_PIN_CALLS = [
@@ -119,6 +135,11 @@ PY_PIN_CALLS = [
     ("fold keeps the function", lambda: pins.test_fold_then_fresh_permutations_and_zero_theta_keep_the_function()),
     ("quantiser golden", lambda: pins.test_quantize_rows_int8_golden()),
     ("quantiser bounds", lambda: pins.test_quantize_rows_int8_bounds_and_round_trip_error()),
+    ("parity metric hand values", lambda: pins.test_rel_fro_hand_values()),
+    ("per-row metric hand values", lambda: pins.test_rel_fro_rows_hand_values()),
+    ("orthogonality defect hand values", lambda: pins.test_orth_error_hand_values()),
+    ("orthogonality defect closed form",
+     lambda: pins.test_orth_error_closed_form_of_the_neumann_truncation(3)),
 ]
 
 

@@ -403,3 +403,62 @@ def test_quantize_commutes_with_the_merge():
     q, s = oracle.quantize_rows_int8(W)
     np.testing.assert_array_equal(qm, q[po][:, pi])
     np.testing.assert_array_equal(sm, s[po])
+
+
+# ---------------------------------------------------------------- parity metrics
+# Every GPU parity verdict is taken with these functions, so they are pinned to
+# values worked out by hand (not by retyping their formulas).
+
+def test_rel_fro_hand_values():
+    # ||(0, 2, 2)|| / ||(1, 0, 0)|| = sqrt(8)
+    assert oracle.rel_fro([1.0, 2.0, 2.0], [1.0, 0.0, 0.0]) == pytest.approx(np.sqrt(8.0), rel=1e-15)
+    # ||(0, 5)|| / ||(3, 4)|| = 1; dividing by ||got|| = sqrt(90) would give 0.527
+    assert oracle.rel_fro([3.0, 9.0], [3.0, 4.0]) == pytest.approx(1.0, rel=1e-15)
+    # matrices are measured as one vector: ||[[0, 1], [0, 0]]|| / ||[[2, 0], [0, 0]]|| = 1/2
+    assert oracle.rel_fro([[2.0, 1.0], [0.0, 0.0]], [[2.0, 0.0], [0.0, 0.0]]) == pytest.approx(0.5)
+    # equal arguments: exactly zero; an all-zero reference: the absolute error ||(3, 4)|| = 5
+    assert oracle.rel_fro([1.5, -2.0], [1.5, -2.0]) == 0.0
+    assert oracle.rel_fro([3.0, 4.0], [0.0, 0.0]) == pytest.approx(5.0, rel=1e-15)
+    # the error is not symmetric in its arguments: ||(2)|| / ||(1)|| = 2 but ||(2)|| / ||(3)|| = 2/3
+    assert oracle.rel_fro([3.0], [1.0]) == pytest.approx(2.0)
+    assert oracle.rel_fro([1.0], [3.0]) == pytest.approx(2.0 / 3.0)
+
+
+def test_rel_fro_rows_hand_values():
+    got = np.array([[1.0, 2.0, 2.0], [3.0, 9.0, 0.0], [0.0, 0.0, 0.0], [3.0, 4.0, 0.0]])
+    ref = np.array([[1.0, 0.0, 0.0], [3.0, 4.0, 0.0], [0.0, 0.0, 0.0], [0.0, 0.0, 0.0]])
+    np.testing.assert_allclose(oracle.rel_fro_rows(got, ref), [np.sqrt(8.0), 1.0, 0.0, 5.0],
+                               rtol=1e-15)
+    # one slice per block of a [nb, b, b] stack
+    Qg = np.stack([np.eye(2), [[2.0, 1.0], [0.0, 0.0]]])
+    Qr = np.stack([np.eye(2), [[2.0, 0.0], [0.0, 0.0]]])
+    np.testing.assert_allclose(oracle.rel_fro_rows(Qg, Qr), [0.0, 0.5], rtol=1e-15)
+
+
+def test_orth_error_hand_values():
+    # A = diag(2, 1): A^T A - I = diag(3, 0) -> 3.
+    # A = [[1, 1], [0, 1]]: A^T A - I = [[0, 1], [1, 1]] -> sqrt(3); A A - I = [[0, 2], [0, 0]]
+    # would give 2 instead.  One value per block.
+    A = np.stack([np.diag([2.0, 1.0]), [[1.0, 1.0], [0.0, 1.0]]])
+    np.testing.assert_allclose(oracle.orth_error(A), [3.0, np.sqrt(3.0)], rtol=1e-15)
+    # an orthogonal matrix (a rotation) has no defect; a zero matrix has ||I||_F = sqrt(b)
+    c, s = np.cos(0.3), np.sin(0.3)
+    assert oracle.orth_error(np.array([[c, -s], [s, c]])) == pytest.approx(0.0, abs=1e-15)
+    assert oracle.orth_error(np.zeros((5, 5))) == pytest.approx(np.sqrt(5.0), rel=1e-15)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6])
+def test_orth_error_closed_form_of_the_neumann_truncation(n):
+    # ||Q^T Q - I||_F = ||K^{2n+2}||_F (n even), ||-2K^{n+1} + K^{2n+2}||_F (n odd),
+    # with the powers from numpy.linalg.matrix_power.  (Q Q^T gives the same norm for
+    # any square Q -- same trace and same Frobenius norm of the Gram matrix -- so the
+    # order of the product is pinned by the hand values above, not here.)
+    b = 10
+    th = rand_theta(3, b, 0.25)
+    K = oracle.unpack_skew(th, b)
+    want = []
+    for j in range(3):
+        Kn1 = np.linalg.matrix_power(K[j], n + 1)
+        K2n2 = np.linalg.matrix_power(K[j], 2 * n + 2)
+        want.append(np.linalg.norm(K2n2 if n % 2 == 0 else -2 * Kn1 + K2n2))
+    np.testing.assert_allclose(oracle.orth_error(oracle.cnp(th, b, n)), want, rtol=1e-10)
