@@ -84,6 +84,8 @@ def kernel_work(case):
         "tc_dq": ("hbm", dq_flops, dq_bytes),
         "tc_cluster_dq": ("hbm", dq_flops, dq_bytes),
         "tc_permute_cols": ("hbm", 0.0, es * (T * di + T * do)),
+        "tc_cnp_tile": ("tensor", 2 * cnp_f, 4 * npk + 2 * nbb),
+        "tc_cnp_tile_f32": ("tensor", 2 * cnp_f, 4 * npk + 4 * nbb),
         "tc_cnp_unpack": ("hbm", 0.0, 4 * npk + 2 * nbb),
         "tc_cnp_fwd": ("tensor", 2 * cnp_f, 2 * nbb + 2 * nbb),
         "tc_cnp_bwd_prep": ("hbm", 0.0, 4 * npk + 4 * nbb + 3 * 2 * nbb),
@@ -408,17 +410,24 @@ def workload_config(world):
 def cnp_roofline_point(b, out_bytes, n, nblocks, seconds, peaks):
     """Roofline of one Cayley-Neumann generation call: algorithmic bytes (packed
     theta in, Q out) and flops (n products of b x b x b per block) against the
-    measured HBM and bf16 tensor peaks; fp32 Q runs on the CUDA cores, so its
-    points carry the HBM fraction only."""
+    measured HBM peak and the peak of the unit the products run on: bf16 Q on
+    the bf16 tensor cores; fp32 Q at b <= 128 on the tensor cores as three bf16
+    MMA chains per product (so a third of the bf16 peak); fp32 Q at b = 256 on
+    the CUDA cores (fp32 FMA peak from the unit counts and the clock)."""
     byts = nblocks * (4 * (b * (b - 1) // 2) + out_bytes * b * b)
     flops = nblocks * 2.0 * n * b ** 3
     t_hbm = byts / (peaks["hbm_gbs"] * 1e9)
     out = {"gbs": round(byts / seconds / 1e9, 1), "tflops": round(flops / seconds / 1e12, 2),
            "hbm_frac": round(t_hbm / seconds, 4)}
     if out_bytes == 2:
-        t_tc = flops / (peaks["bf16_tflops"] * 1e12)
-        out["bound"] = "hbm" if t_hbm >= t_tc else "tensor"
-        out["frac"] = round(max(t_hbm, t_tc) / seconds, 4)
+        unit, peak = "tensor", peaks["bf16_tflops"]
+    elif b <= 128:
+        unit, peak = "tensor_split3", peaks["bf16_tflops"] / 3
+    else:
+        unit, peak = "alu", ALU_FP32_PEAK_TFLOPS
+    t_c = flops / (peak * 1e12)
+    out["bound"] = "hbm" if t_hbm >= t_c else unit
+    out["frac"] = round(max(t_hbm, t_c) / seconds, 4)
     return out
 
 

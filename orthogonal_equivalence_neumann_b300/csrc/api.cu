@@ -142,6 +142,8 @@ poetx_status poetx_cayley_neumann(const float* theta, int nb, int b, int n, void
   if (!valid_block(b)) return POETX_ERR_UNSUPPORTED;
   if (nb == 0) return POETX_OK;
   if (!theta || !Q || !aligned16(theta) || !aligned16(Q)) return POETX_ERR_INVALID_ARG;
+  if (tc::cnp_tile_supported(b))
+    return tc::cnp_tile_fwd(theta, nb, theta, 0, b, n, Q, Q, out_dtype == POETX_F32, stream);
   if (tc_cnp_supported(b, out_dtype) && nb <= 65535)
     return tc_cnp_fwd(theta, nb, b, n, Q, out_dtype, stream);
   return launch_cnp_fwd_simt(theta, nb, b, n, Q, out_dtype, stream);
@@ -156,6 +158,9 @@ poetx_status poetx_cayley_neumann_pair(const float* theta_P, int nb_P, int b_P,
   if ((nb_P > 0 && (!theta_P || !Q_P || !aligned16(theta_P) || !aligned16(Q_P))) ||
       (nb_R > 0 && (!theta_R || !Q_R || !aligned16(theta_R) || !aligned16(Q_R))))
     return POETX_ERR_INVALID_ARG;
+  if (b_P == b_R && tc::cnp_tile_supported(b_P))
+    return tc::cnp_tile_fwd(theta_P, nb_P, theta_R, nb_R, b_P, n, Q_P, Q_R,
+                            out_dtype == POETX_F32, stream);
   if (b_P == b_R && tc_cnp_supported(b_P, out_dtype) && nb_P + nb_R <= 65535)
     return tc::cnp_fwd_pair_bf16ops(theta_P, nb_P, theta_R, nb_R, b_P, n, Q_P, Q_R, false, stream);
   POETX_TRY(poetx_cayley_neumann(theta_P, nb_P, b_P, n, Q_P, out_dtype, stream));

@@ -9,8 +9,10 @@
 // memory, streaming K itself through shared memory in row chunks unpacked
 // straight from the packed parameters (the dense K never touches HBM).
 //
-// This is the exact-fp32 path (any power-of-two b <= 256).  It serves fp32
-// outputs and every block size the tensor-core kernel does not take.
+// This is the exact-fp32 path (any power-of-two b <= 256).  The forward
+// serves the block sizes the tensor-core kernels do not take: b <= 16, fp32 Q
+// at b = 256, and bf16 Q at b = 256 beyond 65535 blocks; the backward serves
+// the standalone poetx_cayley_neumann_backward and the fp32 layer.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "profile.cuh"
@@ -236,9 +238,9 @@ constexpr size_t small_fwd_smem() {
   return sizeof(float) * ((size_t)small_fwd_h_off<B>() + (size_t)B * B);
 }
 
-// Forward for blocks up to b = 128: one CTA holds a whole block, K and the
-// running factor in shared memory, and evaluates the truncated series in
-// Horner form,
+// Forward for b = 16 (the template takes b up to 128): one CTA holds a whole
+// block, K and the running factor in shared memory, and evaluates the
+// truncated series in Horner form,
 //   H_1 = 2I + K,  H_{s+1} = 2I + K H_s,  Q = I + K H_n
 // (= I + 2K + ... + 2K^n + K^{n+1}): n products of b x b.  Each thread owns
 // OUT = b*b/256 entries of one row, in groups of four columns 4*TPR apart so
@@ -354,10 +356,8 @@ size_t cnp_bwd_simt_smem(int b) {
 
 poetx_status launch_cnp_fwd_simt(const float* theta, int nb, int b, int n, void* Q,
                                  poetx_dtype out_dtype, cudaStream_t s) {
+  // b = 32, 64, 128 take the tensor-core tile kernel (tc_cnp_tile.cu) at any block count
   if (b == 16) return launch_cnp_fwd_small<16>(theta, nb, n, Q, out_dtype, s);
-  if (b == 32) return launch_cnp_fwd_small<32>(theta, nb, n, Q, out_dtype, s);
-  if (b == 64) return launch_cnp_fwd_small<64>(theta, nb, n, Q, out_dtype, s);
-  if (b == 128) return launch_cnp_fwd_small<128>(theta, nb, n, Q, out_dtype, s);
   const int rows = b < kRowSlab ? b : kRowSlab;
   dim3 grid(b / rows, nb);
   const size_t smem = cnp_fwd_simt_smem(b);

@@ -99,6 +99,15 @@ bool permute_supported(int d);
 poetx_status permute_cols_bf16(const void* in, void* out, const int32_t* perm, int T, int d,
                                cudaStream_t s);
 
+// Cayley-Neumann forward for b in {32, 64, 128}: the parameters unpacked in
+// shared memory, 128 / b blocks per 128-row tile (block-diagonal), bf16 Q
+// from bf16 operands or fp32 Q from a three-term bf16 split of every
+// operand; both factors of a layer in one launch (nb0 or nb1 may be 0).  Any
+// block count.
+bool cnp_tile_supported(int b);
+poetx_status cnp_tile_fwd(const float* theta0, int nb0, const float* theta1, int nb1, int b, int n,
+                          void* Q0, void* Q1, bool out_f32, cudaStream_t s);
+
 // Cayley-Neumann forward / backward with bf16 operands and fp32 accumulation
 // (tcgen05), b in {128, 256}.  The backward overwrites dtheta.
 bool cnp_supported(int b);

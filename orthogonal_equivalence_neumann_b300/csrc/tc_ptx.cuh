@@ -1,7 +1,7 @@
 // tc_ptx.cuh -- inline-PTX building blocks for the sm_103a tensor-core kernels:
 // mbarriers with bounded waits, TMA tensor loads, TMEM allocation, tcgen05.mma
-// (kind::f16 / kind::tf32, single-CTA), tcgen05.commit and tcgen05.ld, plus
-// the shared-memory matrix and instruction descriptors.
+// (kind::f16, one CTA or a CTA pair), tcgen05.commit and tcgen05.ld, plus the
+// shared-memory matrix and instruction descriptors.
 //
 // Descriptor formats (as documented for tcgen05 in the PTX ISA):
 //  * shared-memory matrix descriptor (64 bit): start address >> 4 in [0,14),
@@ -14,7 +14,7 @@
 //    is stored as 64-element x 8-row atoms (SBO = stride between 8-row K
 //    groups, LBO = stride between 64-element MN chunks).
 //  * instruction descriptor (32 bit): D format in [4,6) (1 = f32), A format
-//    in [7,10) and B format in [10,13) (kind::f16: 1 = bf16; kind::tf32: 2),
+//    in [7,10) and B format in [10,13) (kind::f16: 1 = bf16),
 //    A / B major in bits 15 / 16 (1 = MN-major), N >> 3 in [17,23),
 //    M >> 4 in [24,29).
 #pragma once
@@ -28,8 +28,9 @@
 namespace poetx {
 namespace tc {
 
-// Spin limit of every bounded wait: far beyond any legitimate wait of these
-// kernels (microseconds), short enough that a broken pipeline returns.
+// Poll limit of every bounded wait (about a tenth of a second of polling):
+// far beyond any legitimate wait of these kernels (microseconds), short
+// enough that a broken pipeline returns.
 constexpr uint32_t kWaitLimit = 1u << 22;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -55,18 +56,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.b32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Non-blocking test of the phase with parity `parity` (acquire, CTA scope).
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -80,12 +69,15 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits until the phase of `bar` with parity `parity` has completed.  Gives
-// up after `limit` polls: records POETX_ERR_TIMEOUT and returns false.
+// Waits until the phase of `bar` with parity `parity` has completed, by
+// polling the non-blocking test (a suspending try_wait can stay asleep for
+// microseconds after the phase completes, which a chain of short dependent
+// steps cannot afford).  Gives up after `limit` polls: records
+// POETX_ERR_TIMEOUT and returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit,
                                                   int* err) {
   for (uint32_t i = 0; i < limit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
   raise_device_error(err, POETX_ERR_TIMEOUT);
   return false;
 }
@@ -239,11 +231,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// kind::tf32 with tf32 A and B, f32 accumulator.
-__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4) | (2u << 7) | (2u << 10) | ((a_mn ? 1u : 0u) << 15) |
-         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
 
 // ---------------------------------------------------------------- MMA
 // D[tmem] (+)= A[smem] . B[smem]^T, issued by one thread.
@@ -277,6 +264,66 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       : "memory");
 }
 
+// ---------------------------------------------------------------- CTA pairs (cta_group::2)
+// A pair is the two CTAs of a cluster whose ranks differ in bit 0.  One MMA
+// issued by the pair's first CTA spans both: A (M = 256) is split by rows,
+// 128 in each CTA's shared memory, B by its N columns, N/2 in each; the
+// accumulator rows of each CTA land in that CTA's tensor memory.
+
+// Tensor load into this CTA's shared memory whose completion is counted on
+// an mbarrier of either CTA of the pair (`bar_cluster`: shared::cluster
+// address, e.g. the first CTA's barrier through mapa_shared).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
+}
+
+// Whole-warp operations, executed by one warp in EACH CTA of the pair: the
+// same columns are allocated in both CTAs' tensor memory.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// D[tmem] (+)= A[smem] . B[smem]^T over the pair (issued by the first CTA).
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives on the barrier at the same shared-memory offset in both CTAs of the
+// pair once every pair MMA this thread issued before has completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+
+// As mma_commit_pair, arriving on this CTA's barrier only.
+__device__ __forceinline__ void mma_commit_pair_local(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
 // ---------------------------------------------------------------- TMEM -> registers
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp gets lane
 // (base lane + t), columns [col, col + 32).
@@ -291,6 +338,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
         "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
         "=r"(r[31])
+      : "r"(taddr));
+}
+
+// 32 lanes x 16 consecutive 32-bit columns (as tmem_ld32, half the columns).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
 
@@ -318,9 +376,10 @@ __device__ __forceinline__ void tmem_ld_wait() {
 
 // After tmem_ld_wait(): ties the loaded registers to the wait, so no use of
 // them can be scheduled before it (the load's outputs are only valid then).
-__device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[32]) {
+template <int N>
+__device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[N]) {
 #pragma unroll
-  for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -28,11 +28,19 @@ def test_cnp_roofline_point_bounds():
     assert p["bound"] == "tensor"
     assert p["frac"] == pytest.approx(flops / 1.5e15 / sec, rel=1e-3)
     assert p["hbm_frac"] == pytest.approx(byts / 6e12 / sec, rel=1e-3)
-    # b = 32: HBM-bound; fp32 output carries the HBM fraction only
+    # b = 32: HBM-bound (for either output type)
     q = bench.cnp_roofline_point(32, 2, 3, 4096, sec, PEAKS)
     assert q["bound"] == "hbm" and q["frac"] == q["hbm_frac"]
     r = bench.cnp_roofline_point(32, 4, 3, 4096, sec, PEAKS)
-    assert "frac" not in r and r["hbm_frac"] > q["hbm_frac"]
+    assert r["bound"] == "hbm" and r["hbm_frac"] > q["hbm_frac"]
+    # fp32 Q at b = 128 runs three bf16 MMA chains per product: a third of the bf16 peak
+    f = bench.cnp_roofline_point(128, 4, 6, 4096, sec, PEAKS)
+    t_split = 4096 * 2.0 * 6 * 128 ** 3 / (1.5e15 / 3)
+    assert f["bound"] == "tensor_split3" and f["frac"] == pytest.approx(t_split / sec, rel=1e-3)
+    # fp32 Q at b = 256 is bound by the fp32 FMA units
+    a = bench.cnp_roofline_point(256, 4, 3, 4096, sec, PEAKS)
+    assert a["bound"] == "alu"
+    assert a["frac"] == pytest.approx(flops / (bench.ALU_FP32_PEAK_TFLOPS * 1e12) / sec, rel=1e-3)
 
 
 def test_traffic_entries_follow_their_sources(tmp_path, monkeypatch):

@@ -138,10 +138,29 @@ def test_cnp_sweep_full_size_sampled_blocks(b, sigma, n, out):
         assert np.all(np.abs(e_got - e_ref) <= bound), (e_got, e_ref, bound)
 
 
+@pytest.mark.parametrize("b,nb_P,nb_R", [(32, 7, 5), (64, 3, 9), (128, 2, 3), (32, 1, 0),
+                                         (64, 0, 1)])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_cnp_tile_ragged_tiles_and_both_factors(b, nb_P, nb_R, out):
+    """The tile kernel packs 128 / b blocks per 128-row tile and takes both
+    factors of a layer in one launch: block counts that leave a partial last
+    tile on either factor, every block checked against the oracle."""
+    dt = torch.float32 if out == "f32" else torch.bfloat16
+    thP = inputs.make_theta(nb_P, b, 0.01, 3100 + b + nb_P)
+    thR = inputs.make_theta(nb_R, b, 0.01, 3200 + b + nb_R)
+    QP = torch.full((max(nb_P, 1), b, b), float("nan"), dtype=dt, device="cuda")[:nb_P]
+    QR = torch.full((max(nb_R, 1), b, b), float("nan"), dtype=dt, device="cuda")[:nb_R]
+    _lib.poetx_cayley_neumann_pair(thP.cuda(), b, thR.cuda(), b, 5, QP, QR)
+    _lib.poetx_stream_status()
+    for name, th, Q in (("Q_P", thP, QP), ("Q_R", thR, QR)):
+        if th.shape[0]:
+            assert_close(name, to64(Q), oracle.cnp(th.double().numpy(), b, 5), tol_for(out))
+
+
 def test_cnp_bf16_b128_beyond_the_tensor_core_grid():
-    """Above 65535 blocks the bf16 Q at b = 128 comes from the CUDA-core Horner
-    kernel instead of the tensor-core chain: 65541 blocks (2.1 GB of theta and
-    of Q), blocks sampled at both ends and in between against the oracle."""
+    """bf16 Q at b = 128 past 2^16 blocks (the tile kernel walks any number of
+    tiles): 65541 blocks (2.1 GB of theta and of Q), blocks sampled at both
+    ends and in between against the oracle."""
     nb, b, n = 65541, 128, 3
     th = inputs.make_theta(nb, b, 0.01, 5150)
     Q = torch.empty(nb, b, b, dtype=torch.bfloat16, device="cuda")
@@ -426,7 +445,7 @@ def test_bf16_step_runs_on_the_tensor_core_kernels(b):
         _lib.poetx_profile_enable(False)
     names = set(_lib.poetx_profile_report())
     for k in ("tc_cluster_gather", "tc_cluster_scatter", "tc_gemm_nt", "tc_gemm_nn",
-              "tc_cluster_dq", "tc_cnp_fwd", "tc_cnp_bwd"):
+              "tc_cluster_dq", "tc_cnp_fwd" if b == 256 else "tc_cnp_tile", "tc_cnp_bwd"):
         assert k in names, (k, sorted(names))
     assert not any(n.endswith("_simt") for n in names), sorted(names)
     assert "tc_permute_cols" not in names and "tc_dq" not in names, sorted(names)
