@@ -527,11 +527,10 @@ def xq_point(case, inp, lay, xs, dys, y, dX, dev):
 def config_points(dev, peaks, reps=20):
     """Graph-replayed steps of the workloads' other layer shapes: the MLP
     up-projection 2048 -> 5632 (b = 128, 16384 tokens) and the three linear
-    shapes of the 1B-style stack (b = 256, 8192 tokens), from which the step of
-    the 16-layer stack is composed (q, k, v, o, gate, up and down per layer,
-    each a fresh activation).  Each shape cycles ROTATE input sets, so the
-    inputs of consecutive replays do not sit in L2.  Measured after the
-    headline; a failure here is reported in place of these numbers."""
+    shapes of the 1B-style stack (b = 256, 8192 tokens).  Each shape cycles
+    ROTATE input sets, so the inputs of consecutive replays do not sit in L2.
+    Measured after the headline; a failure here is reported in place of these
+    numbers."""
     out = {}
     try:
         st = inputs.stack_cases(layers=1)
@@ -568,18 +567,122 @@ def config_points(dev, peaks, reps=20):
                          "frac_of_bf16_peak": round(fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
             del lay, graphs, xs, dys, y, dX
             torch.cuda.empty_cache()
-        q, g, d = (out[k] for k in ("stack_qkvo_2048x2048", "stack_gate_up_2048x5632",
-                                    "stack_down_5632x2048"))
-        layer_ms = 4 * q["ms_per_step"] + 2 * g["ms_per_step"] + d["ms_per_step"]
-        layer_fl = 4 * step_flops(st[0]) + 2 * step_flops(st[4]) + step_flops(st[6])
-        out["stack_16_layers_composed"] = {
-            "ms_per_step": round(16 * layer_ms, 3), "tokens_per_s": round(8192 / (16 * layer_ms * 1e-3)),
-            "tflops": round(layer_fl / (layer_ms * 1e-3) / 1e12, 1),
-            "frac_of_bf16_peak": round(layer_fl / (layer_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-            "composed_of": "16 x (4 q/k/v/o + 2 gate/up + 1 down) measured single-shape steps"}
+        out["stack_16_layers"] = stack_point(dev, peaks)
     except Exception as e:   # noqa: BLE001 -- reported, the headline stands
         out["error"] = repr(e)[:300]
     return out
+
+
+def link_bandwidth(dev, mb=64, reps=10):
+    """Pinned host <-> device copy bandwidth of this GPU's link, measured alone:
+    one direction at a time, then both at once on two streams (as the
+    end-to-end loop moves them), GB/s from CUDA events."""
+    n = mb << 20
+    h_src = torch.empty(n, dtype=torch.uint8).pin_memory()
+    h_dst = torch.empty(n, dtype=torch.uint8).pin_memory()
+    d_a = torch.empty(n, dtype=torch.uint8, device=dev)
+    d_b = torch.empty(n, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def timed(st, fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fn()
+        torch.cuda.synchronize()
+        e0.record(st)
+        for _ in range(reps):
+            fn()
+        e1.record(st)
+        torch.cuda.synchronize()
+        return n * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+
+    with torch.cuda.stream(s1):
+        h2d = timed(s1, lambda: d_a.copy_(h_src, non_blocking=True))
+        d2h = timed(s1, lambda: h_dst.copy_(d_b, non_blocking=True))
+    # both directions at once: each stream's own events over the same interval
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    ev[0].record(s1)
+    ev[2].record(s2)
+    for _ in range(reps):
+        with torch.cuda.stream(s1):
+            d_a.copy_(h_src, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h_dst.copy_(d_b, non_blocking=True)
+    ev[1].record(s1)
+    ev[3].record(s2)
+    torch.cuda.synchronize()
+    c_h2d = n * reps / (ev[0].elapsed_time(ev[1]) * 1e-3) / 1e9
+    c_d2h = n * reps / (ev[2].elapsed_time(ev[3]) * 1e-3) / 1e9
+    del h_src, h_dst, d_a, d_b
+    return {"h2d_gbs": round(h2d, 1), "d2h_gbs": round(d2h, 1), "concurrent_h2d_gbs": round(c_h2d, 1),
+            "concurrent_d2h_gbs": round(c_d2h, 1), "copy_mb": mb}
+
+
+def stack_point(dev, peaks, steps=3):
+    """The 1B-style stack measured as one training step: 16 layers x 7 linears
+    (q, k, v, o 2048 -> 2048; gate, up 2048 -> 5632; down 5632 -> 2048), i.e.
+    112 layers each with its own frozen weight (1.64 GB of W0 in all),
+    parameters and permutations, and a fresh synthetic activation per linear
+    (seeded device draws with the workload's distributions).  One step = the
+    Cayley-Neumann blocks and forward of every linear in order, then the
+    backward of every linear in reverse order (each keeps its own z), captured
+    into one CUDA graph and replayed; the linears share one workspace."""
+    cases = inputs.stack_cases()
+    bf = torch.bfloat16
+    gen = torch.Generator(device=dev).manual_seed(2468)
+    cpu = torch.Generator().manual_seed(2469)
+    need = max(_lib.poetx_workspace_bytes(c.T, c.d_in, c.d_out, c.b_in, c.b_out, bf) for c in cases)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    lays, xs, dys = [], [], []
+    for c in cases:
+        W0 = (torch.randn(c.d_out, c.d_in, generator=gen, device=dev) * c.d_in ** -0.5).to(bf)
+        thP = torch.randn(c.d_in // c.b_in, c.b_in * (c.b_in - 1) // 2, generator=gen,
+                          device=dev) * c.sigma
+        thR = torch.randn(c.d_out // c.b_out, c.b_out * (c.b_out - 1) // 2, generator=gen,
+                          device=dev) * c.sigma
+        pi = torch.randperm(c.d_in, generator=cpu).to(torch.int32)
+        po = torch.randperm(c.d_out, generator=cpu).to(torch.int32)
+        lays.append(TransformedLinear(W0, thP, thR, pi, po, c.b_in, c.b_out, c.n, T_max=c.T,
+                                      save_z=True, device=dev, workspace=ws))
+        xs.append(torch.randn(c.T, c.d_in, generator=gen, device=dev).to(bf))
+        dys.append(torch.randn(c.T, c.d_out, generator=gen, device=dev).to(bf))
+    outs = {d: torch.empty(cases[0].T, d, dtype=bf, device=dev) for d in (2048, 5632)}
+
+    def step():
+        for lay, x in zip(lays, xs):
+            lay.cayley_neumann()
+            lay.forward(x, outs[lay.d_out])
+        for lay, x, dy in zip(reversed(lays), reversed(xs), reversed(dys)):
+            lay.backward(x, dy, outs[lay.d_in])
+
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+        step()
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    _lib.poetx_stream_status()
+    ms = e0.elapsed_time(e1) / steps
+    fl = sum(step_flops(c) for c in cases)
+    w0_bytes = sum(2 * c.d_in * c.d_out for c in cases)
+    del graph, lays, xs, dys, outs, ws
+    torch.cuda.empty_cache()
+    return {"ms_per_step": round(ms, 3), "tokens_per_s": round(cases[0].T / (ms * 1e-3)),
+            "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
+            "frac_of_bf16_peak": round(fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "linears": len(cases), "w0_bytes": w0_bytes, "steps": steps,
+            "measured": "one CUDA graph: forward of the 112 linears in order, then their "
+                        "backward in reverse order"}
 
 
 def run_poetx(args, world, rank, local):
@@ -719,11 +822,15 @@ def run_poetx(args, world, rank, local):
             d_dy[b].copy_(h_dy[k % 2], non_blocking=True)
             in_ready[b].record(copy_in)
 
+    # the compute of a step is the same captured graph as in the timed region,
+    # one per device buffer set
+    egraphs = [lay.capture_step(d_x[b], d_dy[b], d_y[b], d_dX[b]) for b in range(NB)]
+
     def e2e_step(k):
         b = k % NB
         stream.wait_event(in_ready[b])
         stream.wait_event(out_done[b])            # step k - NB's results have left
-        lay.step(d_x[b], d_dy[b], d_y[b], d_dX[b])
+        egraphs[b].replay()
         allreduce_grads(lay, world)
         d_tp[b].copy_(lay.dtheta_P, non_blocking=True)
         d_tr[b].copy_(lay.dtheta_R, non_blocking=True)
@@ -758,9 +865,16 @@ def run_poetx(args, world, rank, local):
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), world)
     h2d = (d_x[0].numel() + d_dy[0].numel()) * 2
     d2h = (y.numel() + dX.numel()) * 2 + 4 * (h_tp[0].numel() + h_tr[0].numel())
+    link = link_bandwidth(dev)
+    # the bound the host link alone sets: both directions overlapped with the compute
+    t_link = max(h2d / (link["concurrent_h2d_gbs"] * 1e9), d2h / (link["concurrent_d2h_gbs"] * 1e9))
     e2e = {"value": world * case.T * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "copies": "pinned host buffers; uploads and downloads on their own streams, double-buffered"}
+           "copies": "pinned host buffers; uploads and downloads on their own streams, "
+                     "double-buffered; compute as the captured step graph",
+           "link": link, "link_bound_tokens_per_s": round(case.T / t_link),
+           "frac_of_link_bound": round(world * case.T * args.steps / (e2e_ms * 1e-3) /
+                                       (world * case.T / t_link), 4)}
 
     cnp, cnp_roof = cnp_points(dev, peaks) if rank == 0 else (None, None)
     fold = fold_point(lay, dev, peaks) if rank == 0 else None

@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kTileThreads)
         fetch(t + gridDim.x, buf ^ 1);
         ++fetched;
       }
-      lok = mbar_wait(th_full + buf, (it >> 1) & 1, err);
+      lok = mbar_poll(th_full + buf, (it >> 1) & 1, err);
       if (lok) ++landed;
     }
     if (__syncthreads_or(!lok)) {   // every thread leaves together
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kTileThreads)
             }
           }
         mma_commit(mma_done);
-        lok = mbar_wait(mma_done, mma_count & 1, err);
+        lok = mbar_poll(mma_done, mma_count & 1, err);
       }
       if (__syncthreads_or(!lok)) {
         ok = false;

@@ -175,7 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int tile = pair; tile < num_tiles; tile += n_pairs) {
       const int m_blk = tile / n_tiles, n_blk = tile % n_tiles;
-      if (!mbar_wait(tfull + acc, acc_phase, err)) break;
+      // one thread waits, the other epilogue threads sleep at a named barrier
+      bool lok = true;
+      if (quarter == 2 && lane == 0) lok = mbar_wait(tfull + acc, acc_phase, err);
+      if (bar_sync_or(1, 128, !lok)) break;
       tc_fence_after();
       const int row = m_blk * BM + row_in_tile;
       __nv_bfloat16* crow = C + (size_t)row * N + (size_t)n_blk * BN;

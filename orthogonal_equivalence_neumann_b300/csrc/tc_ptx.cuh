@@ -28,9 +28,8 @@
 namespace poetx {
 namespace tc {
 
-// Poll limit of every bounded wait (about a tenth of a second of polling):
-// far beyond any legitimate wait of these kernels (microseconds), short
-// enough that a broken pipeline returns.
+// Test limit of every bounded wait: far beyond any legitimate wait of these
+// kernels (microseconds), short enough that a broken pipeline returns.
 constexpr uint32_t kWaitLimit = 1u << 22;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -56,6 +55,21 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Potentially blocking test of the phase with parity `parity` (acquire, CTA
+// scope): the thread may be suspended (issuing nothing) until the phase
+// completes or a time limit passes.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Non-blocking test of the phase with parity `parity` (acquire, CTA scope).
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -69,20 +83,44 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits until the phase of `bar` with parity `parity` has completed, by
-// polling the non-blocking test (a suspending try_wait can stay asleep for
-// microseconds after the phase completes, which a chain of short dependent
-// steps cannot afford).  Gives up after `limit` polls: records
-// POETX_ERR_TIMEOUT and returns false.
+// Waits until the phase of `bar` with parity `parity` has completed, with the
+// suspending test (a waiting thread takes no issue slots from the warps that
+// do the work).  Gives up after `limit` tests: records POETX_ERR_TIMEOUT and
+// returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit,
                                                   int* err) {
   for (uint32_t i = 0; i < limit; ++i)
-    if (mbar_test_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
   raise_device_error(err, POETX_ERR_TIMEOUT);
   return false;
 }
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
   return mbar_wait_bounded(bar, parity, kWaitLimit, err);
+}
+
+// As mbar_wait, polling the non-blocking test instead: for one thread that
+// waits on a short, latency-critical step (a chain of dependent MMAs), where a
+// suspended thread could wake up late.
+__device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity, int* err) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_test_wait(bar, parity)) return true;
+  raise_device_error(err, POETX_ERR_TIMEOUT);
+  return false;
+}
+
+// Named barrier `id` over `n` threads that also returns whether `v` was true
+// in any of them (so that a group leaves a loop together).
+__device__ __forceinline__ bool bar_sync_or(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
 }
 
 // ---------------------------------------------------------------- clusters
@@ -308,7 +346,8 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, u
 }
 
 // Arrives on the barrier at the same shared-memory offset in both CTAs of the
-// pair once every pair MMA this thread issued before has completed.
+// pair (a cluster of two) once every pair MMA this thread issued before has
+// completed.
 __device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"

@@ -27,7 +27,7 @@ from . import _lib
 
 class TransformedLinear:
     def __init__(self, W0, theta_P, theta_R, perm_in, perm_out, b_in, b_out, n, T_max,
-                 save_z=True, device="cuda", w0_int8=False):
+                 save_z=True, device="cuda", w0_int8=False, workspace=None):
         dev = torch.device(device)
         self.dtype = W0.dtype
         self.d_out, self.d_in = W0.shape
@@ -65,7 +65,14 @@ class TransformedLinear:
         ws = ws_bytes(self.T_max, self.d_in, self.d_out, self.b_in, self.b_out, self.dtype)
         if ws == 0:
             raise ValueError("invalid layer sizes")
-        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+        # layers that run one after another on one stream may share one
+        # workspace (the scratch of a call is dead once the call's kernels end)
+        if workspace is not None:
+            if workspace.dtype != torch.uint8 or workspace.numel() < ws:
+                raise ValueError("shared workspace too small: need %d bytes" % ws)
+            self.workspace = workspace
+        else:
+            self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
         self.z = (torch.empty(self.T_max, self.d_out, dtype=self.dtype, device=dev)
                   if save_z else None)
 
