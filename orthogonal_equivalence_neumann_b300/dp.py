@@ -39,6 +39,48 @@ def allreduce_dtheta(dtheta_P: torch.Tensor, dtheta_R: torch.Tensor, group=None,
     return works if async_op else None
 
 
+class GradientExchange:
+    """The exchange of a multi-layer backward, overlapped with it: the packed
+    gradients of a layer are all-reduced (asynchronously) as soon as that
+    layer's backward has produced them, so that the exchange of layer L runs
+    while the backward of layer L-1 computes -- DDP's overlap of communication
+    with the backward, one bucket per layer.  ``wait`` ends the step: it waits
+    for every exchange issued since the last ``wait``.
+
+    Each layer must own its gradient buffers (the exchange reads and writes
+    them in place until ``wait`` returns); with NCCL the collectives are
+    ordered after the work already queued on the current stream."""
+
+    def __init__(self, group=None):
+        self.group = group
+        self.works = []
+
+    def layer_done(self, dtheta_P: torch.Tensor, dtheta_R: torch.Tensor):
+        self.works.extend(allreduce_dtheta(dtheta_P, dtheta_R, group=self.group, async_op=True))
+
+    def pending(self) -> int:
+        return len(self.works)
+
+    def wait(self):
+        works, self.works = self.works, []
+        for w in works:
+            w.wait()
+
+
+def backward_layers(layers, xs, dy, exchange=None):
+    """Backward of a chain of transformed linears (``layers[i]`` maps xs[i]
+    to xs[i + 1]; ``dy`` is the gradient of the last output): every layer's
+    backward in reverse order, the gradient of a layer's input feeding the
+    layer before it, each layer's packed gradients handed to ``exchange`` as
+    soon as they exist.  Returns the gradient of the chain's input."""
+    g = dy
+    for lay, x in zip(reversed(layers), reversed(xs)):
+        g, dtp, dtr = lay.backward(x, g)
+        if exchange is not None:
+            exchange.layer_done(dtp, dtr)
+    return g
+
+
 def max_over_ranks(value: float, group=None, device=None) -> float:
     """The largest of one float per rank (a job is as slow as its slowest rank)."""
     if not dist.is_available() or not dist.is_initialized() or dist.get_world_size(group) == 1:

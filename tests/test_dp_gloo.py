@@ -100,3 +100,85 @@ def test_single_process_exchange_is_a_no_op():
     assert dp.allreduce_dtheta(a, b) is None
     assert dp.max_over_ranks(4.5) == 4.5
     assert torch.equal(a, torch.ones(3)) and torch.equal(b, torch.full((2,), 2.0))
+
+
+# ---- a three-layer chain with the exchange overlapped: each layer's packed
+# gradients are all-reduced asynchronously as soon as its backward has made
+# them, and the step waits for all of them at the end.
+
+class _OracleLayer:
+    """One layer of a chain for the CPU test: the oracle's forward and backward
+    in double, with the gradient buffers the exchange works on in place."""
+
+    def __init__(self, seed, d_in, d_out, b_in, b_out, n=3):
+        rng = np.random.default_rng(seed)
+        self.W0 = rng.standard_normal((d_out, d_in)) / np.sqrt(d_in)
+        self.thP = rng.standard_normal((d_in // b_in, b_in * (b_in - 1) // 2)) * 0.1
+        self.thR = rng.standard_normal((d_out // b_out, b_out * (b_out - 1) // 2)) * 0.1
+        self.pi = rng.permutation(d_in).astype(np.int32)
+        self.po = rng.permutation(d_out).astype(np.int32)
+        self.b_in, self.b_out, self.n = b_in, b_out, n
+
+    def forward(self, x):
+        import oracle
+        return oracle.layer(x, self.W0, self.thP, self.thR, self.n, self.pi, self.po, self.b_in,
+                            self.b_out)["y"]
+
+    def backward(self, x, dy):
+        import oracle
+        r = oracle.layer(x, self.W0, self.thP, self.thR, self.n, self.pi, self.po, self.b_in,
+                         self.b_out, dy=dy)
+        self.dtheta_P = torch.from_numpy(r["dtheta_P"].copy())
+        self.dtheta_R = torch.from_numpy(r["dtheta_R"].copy())
+        return r["dX"], self.dtheta_P, self.dtheta_R
+
+
+def _chain(T):
+    layers = [_OracleLayer(41, 16, 12, 4, 6), _OracleLayer(42, 12, 12, 6, 3),
+              _OracleLayer(43, 12, 16, 3, 8)]
+    rng = np.random.default_rng(44)
+    return layers, rng.standard_normal((T, 16)), rng.standard_normal((T, 16))
+
+
+def _chain_grads(layers, x, dy, exchange=None):
+    xs = [x]
+    for lay in layers[:-1]:
+        xs.append(lay.forward(xs[-1]))
+    dX = dp.backward_layers(layers, xs, dy, exchange)
+    return dX, [(lay.dtheta_P, lay.dtheta_R) for lay in layers]
+
+
+def _chain_rank_main(rank, port, T, out_dir):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=WORLD)
+    try:
+        layers, x, dy = _chain(T)
+        sh = dp.token_shard(T, WORLD, rank)
+        ex = dp.GradientExchange()
+        dX, grads = _chain_grads(layers, x[sh], dy[sh], ex)
+        issued = ex.pending()
+        ex.wait()
+        np.savez(os.path.join(out_dir, "chain%d.npz" % rank), dX=dX, start=sh.start,
+                 stop=sh.stop, issued=issued, pending=ex.pending(),
+                 **{"g%d_%s" % (i, s): t.numpy() for i, g in enumerate(grads)
+                    for s, t in zip("PR", g)})
+    finally:
+        dist.destroy_process_group()
+
+
+def test_chain_of_three_layers_with_the_exchange_overlapped(tmp_path):
+    T = 9
+    mp.start_processes(_chain_rank_main, args=(_free_port(), T, str(tmp_path)), nprocs=WORLD,
+                       join=True, start_method="spawn")
+    layers, x, dy = _chain(T)
+    dX_full, full = _chain_grads(layers, x, dy)
+    for rank in range(WORLD):
+        g = np.load(tmp_path / ("chain%d.npz" % rank))
+        # one asynchronous all-reduce per side and layer, all finished by wait()
+        assert int(g["issued"]) == 2 * len(layers) and int(g["pending"]) == 0
+        for i, (gp, gr) in enumerate(full):
+            np.testing.assert_allclose(g["g%d_P" % i], gp.numpy(), rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(g["g%d_R" % i], gr.numpy(), rtol=1e-12, atol=1e-13)
+        rows = slice(int(g["start"]), int(g["stop"]))
+        np.testing.assert_allclose(g["dX"], dX_full[rows], rtol=0, atol=1e-12)
