@@ -30,9 +30,10 @@
 // A[r][k] = X[r][k], both K-major with the 128-byte swizzle.  Thread (warp w,
 // lane l) owns row r = 32 (w % 4) + l (its TMEM lane) and half w / 4 of the
 // row's block columns.  Tiles are handed out round-robin; the next tile's
-// parameters are fetched while the current chain runs.  One thread polls each
-// barrier and the CTA follows through a CTA barrier; every wait is bounded
-// (tc_ptx.cuh).
+// parameters are fetched while the current chain runs (or, where a single
+// parameter buffer lets more CTAs share an SM, those CTAs' chains hide each
+// other's latency instead).  One thread polls each barrier and the CTA
+// follows through a CTA barrier; every wait is bounded (tc_ptx.cuh).
 #include "common.cuh"
 #include "profile.cuh"
 #include "tc.cuh"
@@ -78,7 +79,13 @@ struct TileGeo {
   static constexpr int th_floats = G * P;                 // parameters of one tile
   static constexpr int th_bytes = ((th_floats * 4 + 127) / 128) * 128;
   static constexpr int n_ops = F32 ? 4 : 2;               // B hi [lo], A hi [lo]
-  static constexpr int smem = 1024 + n_ops * kOpBytes + 2 * th_bytes + 64;
+  static constexpr int smem_with(int nth) { return 1024 + n_ops * kOpBytes + nth * th_bytes + 64; }
+  static constexpr int per_sm(int bytes) { return 232448 / (bytes + 1024); }
+  // two parameter buffers (the next tile's parameters arrive during this
+  // tile's chain), unless one buffer lets more CTAs share an SM (whose chains
+  // then hide each other's latency)
+  static constexpr int NTH = per_sm(smem_with(1)) > per_sm(smem_with(2)) ? 1 : 2;
+  static constexpr int smem = smem_with(NTH);
 };
 
 // K[ri][kl] of one block from its packed parameters in shared memory, without
@@ -114,8 +121,8 @@ __global__ void __launch_bounds__(kTileThreads)
   uint8_t* b_lo = smem + kOpBytes;                         // (fp32 only) lo part
   uint8_t* a_hi = smem + (F32 ? 2 : 1) * kOpBytes;         // A = X_i
   uint8_t* a_lo = smem + 3 * kOpBytes;                     // (fp32 only)
-  float* th_buf = reinterpret_cast<float*>(smem + Geo::n_ops * kOpBytes);   // [2][th_bytes]
-  uint64_t* th_full = reinterpret_cast<uint64_t*>(smem + Geo::n_ops * kOpBytes + 2 * Geo::th_bytes);
+  float* th_buf = reinterpret_cast<float*>(smem + Geo::n_ops * kOpBytes);   // [NTH][th_bytes]
+  uint64_t* th_full = reinterpret_cast<uint64_t*>(smem + Geo::n_ops * kOpBytes + Geo::NTH * Geo::th_bytes);
   uint64_t* mma_done = th_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
@@ -168,20 +175,22 @@ __global__ void __launch_bounds__(kTileThreads)
   // this thread's columns of its row: half `half` of the block's B columns
   constexpr int HC = B / 2;
   for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
-    const int buf = it & 1;
+    const int buf = it % Geo::NTH;
     const TileSide* sd;
     int b0, nbt;
     locate(t, sd, b0, nbt);
     bool lok = true;
     if (leader) {
-      // the next tile's parameters come in while this tile's chain runs (the
-      // buffer was last read by the tile before this one, finished below)
-      if (t + (int)gridDim.x < tiles) {
+      // two buffers: the next tile's parameters come in while this tile's
+      // chain runs (the buffer was last read by the tile before this one,
+      // finished below); one buffer: this tile's own, after the last one's
+      const int next = Geo::NTH == 2 ? t + (int)gridDim.x : (it > 0 ? t : tiles);
+      if (next < tiles) {
         fence_proxy_async_smem();   // generic reads of the buffer before the copy's writes
-        fetch(t + gridDim.x, buf ^ 1);
+        fetch(next, Geo::NTH == 2 ? buf ^ 1 : 0);
         ++fetched;
       }
-      lok = mbar_poll(th_full + buf, (it >> 1) & 1, err);
+      lok = mbar_poll(th_full + buf, (uint32_t)(it / Geo::NTH) & 1, err);
       if (lok) ++landed;
     }
     if (__syncthreads_or(!lok)) {   // every thread leaves together
@@ -340,7 +349,7 @@ __global__ void __launch_bounds__(kTileThreads)
     // wind-down after an expired wait: the copies and MMAs already issued
     // finish (bounded waits) before the CTA frees its memory
     for (int k = landed; k < fetched; ++k)
-      mbar_wait_bounded(th_full + (k & 1), (uint32_t)(k >> 1) & 1, 1u << 16, nullptr);
+      mbar_wait_bounded(th_full + k % Geo::NTH, (uint32_t)(k / Geo::NTH) & 1, 1u << 16, nullptr);
     if (mma_pending) mbar_wait_bounded(mma_done, mma_count & 1, 1u << 16, nullptr);
   }
   tc_fence_before();
@@ -358,7 +367,7 @@ poetx_status tile_launch(const TileSide& s0, const TileSide& s1, int n, cudaStre
   if (set_max_dynamic_smem(kern, Geo::smem) != cudaSuccess) return check_launch();
   const int tiles = (s0.nb + Geo::G - 1) / Geo::G + (s1.nb + Geo::G - 1) / Geo::G;
   // CTAs resident per SM (shared memory and TMEM: 128 columns each)
-  int per_sm = 232448 / (Geo::smem + 1024);
+  int per_sm = Geo::per_sm(Geo::smem);
   if (per_sm > 4) per_sm = 4;
   if (per_sm < 1) per_sm = 1;
   int grid = device_sm_count() * per_sm;
