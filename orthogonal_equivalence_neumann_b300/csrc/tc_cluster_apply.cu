@@ -62,6 +62,7 @@ struct CaGeo {
   int st_bytes;       // token-row staging of the output tile for the TMA store
   int q_cols, a_cols, tmem_cols;
   int hdr;            // barriers + routing table, in front of the pipeline buffers
+  int q_rel;          // Q staging area, from the start of the pipeline buffers
   int smem;
 };
 
@@ -158,16 +159,28 @@ __global__ void __launch_bounds__(kCaThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *br.tmem_slot;
-  // Q through the (still idle) pipeline buffers into tensor memory
-  if (threadIdx.x == 0) issue_q_loads(&tmQ, smem + s_off, c * G, G, B, br.q_full);
+  // Q into tensor memory through a staging area of the pipeline buffers: at
+  // their end when that leaves the input tiles free (q_rel > 0: the first
+  // tiles load and move through the exchange while Q is staged; the loader
+  // and the MMA wait for q_done), else at their start, before the first tiles
+  const bool early = g.q_rel > 0;
+  uint8_t* qst = smem + s_off + g.q_rel;
+  if (threadIdx.x == 0) issue_q_loads(&tmQ, qst, c * G, G, B, br.q_full);
   bool ok = true;
-  if (warp >= 10 && warp < 14) {
-    if ((ok = mbar_wait(br.q_full, 0, err)))
-      q_stage_to_tmem<B>(smem + s_off, G, transpose_q, tmem_base, warp % 4, lane);
+  auto stage_q = [&]() {
+    if (warp >= 10 && warp < 14) {
+      if ((ok = mbar_wait(br.q_full, 0, err)))
+        q_stage_to_tmem<B>(qst, G, transpose_q, tmem_base, warp % 4, lane);
+      tc_fence_before();
+      mbar_arrive(br.q_done);
+    }
+  };
+  if (!early) {
+    stage_q();
+    tc_fence_before();
+    __syncthreads();
   }
-  tc_fence_before();
-  __syncthreads();
-  // the first input tiles (the Q stage they overwrite has been read)
+  // the first input tiles (disjoint from the staging area, or after it was read)
   int prefetched = 0;
   if (threadIdx.x == 0) {
     fence_proxy_async_smem();
@@ -180,6 +193,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
   }
   cluster_sync();   // every CTA's barriers are initialised before any remote access
   tc_fence_after();
+  if (early) stage_q();
 
   const uint32_t acc0 = tmem_base + (uint32_t)g.q_cols;
   if (warp == 0) {
@@ -199,7 +213,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
     // ---------------------------------------------------------------- loader
     if (lane == 0)
       loader_loop(br, g.NR, g.NX, g.r_bytes, smem + r_off, ring + (size_t)c * g.r_bytes, slot_stride,
-                  cluster_iters(cluster_id, n_clusters, n_tiles), ok, err);
+                  cluster_iters(cluster_id, n_clusters, n_tiles), ok, err, br.q_done);
   } else if (warp == 15) {
     // ---------------------------------------------------------------- signals to the readers
     signal_loop(br, g.NX, cluster_iters(cluster_id, n_clusters, n_tiles), C, lane, ok, err);
@@ -213,6 +227,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
       if (!(ok = mbar_wait(br.r_full + r, (it / g.NR) & 1, err))) break;
       if (lane >= 1) ack_fetch(br, it, g.NX, n_it, lane - 1, C);
       if (lane == 0) {
+        if (it == 0 && !(ok = mbar_wait(br.q_done, 0, err))) break;   // Q is in tensor memory
         if (!(ok = mbar_wait(br.a_empty + a, ((it / g.NA) & 1) ^ 1, err))) break;
         tc_fence_after();
         const uint32_t rb = smem_u32(smem + r_off + r * g.r_bytes);
@@ -344,16 +359,28 @@ __global__ void __launch_bounds__(kCaThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *br.tmem_slot;
-  // Q through the (still idle) pipeline buffers into tensor memory
-  if (threadIdx.x == 0) issue_q_loads(&tmQ, smem + s_off, c * G, G, B, br.q_full);
+  // Q into tensor memory through a staging area of the pipeline buffers: at
+  // their end when that leaves the input tiles free (q_rel > 0: the first
+  // tiles load and move through the exchange while Q is staged; the loader
+  // and the MMA wait for q_done), else at their start, before the first tiles
+  const bool early = g.q_rel > 0;
+  uint8_t* qst = smem + s_off + g.q_rel;
+  if (threadIdx.x == 0) issue_q_loads(&tmQ, qst, c * G, G, B, br.q_full);
   bool ok = true;
-  if (warp >= 10 && warp < 14) {
-    if ((ok = mbar_wait(br.q_full, 0, err)))
-      q_stage_to_tmem<B>(smem + s_off, G, transpose_q, tmem_base, warp % 4, lane);
+  auto stage_q = [&]() {
+    if (warp >= 10 && warp < 14) {
+      if ((ok = mbar_wait(br.q_full, 0, err)))
+        q_stage_to_tmem<B>(qst, G, transpose_q, tmem_base, warp % 4, lane);
+      tc_fence_before();
+      mbar_arrive(br.q_done);
+    }
+  };
+  if (!early) {
+    stage_q();
+    tc_fence_before();
+    __syncthreads();
   }
-  tc_fence_before();
-  __syncthreads();
-  // the first input tiles (the Q stage they overwrite has been read)
+  // the first input tiles (disjoint from the staging area, or after it was read)
   int prefetched = 0;
   if (threadIdx.x == 0) {
     fence_proxy_async_smem();
@@ -368,6 +395,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
   }
   cluster_sync();   // every CTA's barriers are initialised before any remote access
   tc_fence_after();
+  if (early) stage_q();
 
   const uint32_t acc0 = tmem_base + (uint32_t)g.q_cols;
   if (warp == 0) {
@@ -389,7 +417,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
     // ---------------------------------------------------------------- loader
     if (lane == 0)
       loader_loop(br, g.NR, g.NX, g.r_bytes, smem + r_off, ring + (size_t)c * g.r_bytes, slot_stride,
-                  cluster_iters(cluster_id, n_clusters, n_tiles), ok, err);
+                  cluster_iters(cluster_id, n_clusters, n_tiles), ok, err, br.q_done);
   } else if (warp == 15) {
     // ---------------------------------------------------------------- signals to the readers
     signal_loop(br, g.NX, cluster_iters(cluster_id, n_clusters, n_tiles), C, lane, ok, err);
@@ -399,6 +427,7 @@ __global__ void __launch_bounds__(kCaThreads, 1)
       const uint32_t idesc = idesc_bf16(128, TT, false, false);
       for (int it = 0, tile = cluster_id; tile < n_tiles && ok; tile += n_clusters, ++it) {
         const int s = it % g.NS, a = it % g.NA;
+        if (it == 0 && !(ok = mbar_wait(br.q_done, 0, err))) break;   // Q is in tensor memory
         if (!(ok = mbar_wait(br.s_full + s, (it / g.NS) & 1, err))) break;
         if (!(ok = mbar_wait(br.a_empty + a, ((it / g.NA) & 1) ^ 1, err))) break;
         tc_fence_after();
@@ -566,6 +595,9 @@ bool ca_geometry(int d, int b, bool gather, CaGeo* out) {
         g.NS = NS;
         g.NR = NR;
         g.NST = NST;
+        // Q staged at the end of the buffers when that leaves the input tiles
+        // free (the first tiles then load while Q goes to tensor memory)
+        g.q_rel = body - qstage >= NS * g.s_bytes ? body - qstage : 0;
         // at most one CTA per SM, so a CTA never waits for another's tensor memory
         g.smem = smem > kOneCtaSmem ? smem : kOneCtaSmem;
         found = true;

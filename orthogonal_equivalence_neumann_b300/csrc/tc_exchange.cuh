@@ -60,6 +60,7 @@ struct Bars {
   uint64_t* v_full;     // [4] second, unpermuted operand landed (TMA)
   uint64_t* v_empty;    // [4] second operand consumed
   uint64_t* moved;      // [8] this CTA's writers have stored their rows of an exchange slot
+  uint64_t* q_done;     // [1] the one-time operand is in tensor memory (128 arrivals)
   uint32_t* tmem_slot;
 };
 
@@ -78,7 +79,8 @@ __device__ __forceinline__ Bars bars_at(uint8_t* smem) {
   r.v_full = b + 37;
   r.v_empty = b + 41;
   r.moved = b + 45;
-  r.tmem_slot = reinterpret_cast<uint32_t*>(b + 53);   // 432 bytes in all, under kTableOff
+  r.q_done = b + 53;
+  r.tmem_slot = reinterpret_cast<uint32_t*>(b + 54);   // 440 bytes in all, under kTableOff
   return r;
 }
 
@@ -106,6 +108,7 @@ __device__ __forceinline__ void init_bars(const Bars& br, int C, uint32_t s_empt
     mbar_init(br.a_empty + i, 128);
   }
   mbar_init(br.q_full, 1);
+  mbar_init(br.q_done, 128);
   fence_mbar_init();
 }
 
@@ -128,10 +131,13 @@ __device__ __forceinline__ int cluster_iters(int cluster_id, int n_clusters, int
 }
 
 // The loader (one thread): fetches this CTA's part of every exchange slot
-// once all C writers have signalled it.
+// once all C writers have signalled it.  With `gate`, the first fetch also
+// waits for that barrier's first phase (the fetch buffers held another
+// operand until then).
 __device__ __forceinline__ void loader_loop(const Bars& br, int NR, int NX, int r_bytes, uint8_t* rbuf,
                                             const uint8_t* part0, size_t slot_stride, int n_it,
-                                            bool& ok, int* err) {
+                                            bool& ok, int* err, uint64_t* gate = nullptr) {
+  if (gate && n_it > 0) ok = mbar_wait(gate, 0, err);
   for (int it = 0; it < n_it && ok; ++it) {
     const int r = it % NR, x = it % NX;
     if (!(ok = mbar_wait(br.r_empty + r, ((it / NR) & 1) ^ 1, err))) break;   // buffer free
