@@ -9,6 +9,11 @@
     python -m orthogonal_equivalence_neumann_b300.profile_cases cnp
         three Cayley-Neumann calls at each of three sweep points (4096 blocks,
         n = 3, sigma = 1e-2: b = 128 bf16, b = 128 fp32, b = 32 bf16).
+    python -m orthogonal_equivalence_neumann_b300.profile_cases gate|down|upproj
+        the same six steps as ``layer`` for one of the wide shapes: the MLP
+        gate / up projection 2048 -> 5632 and the down projection 5632 -> 2048
+        of the 1B-style stack (b = 256, 8192 tokens), or the up-projection
+        layer 2048 -> 5632 at b = 128 with 16384 tokens.
 
 Both hold a few hundred MB on the device and run in seconds, so a profiler
 can capture one launch of a chosen kernel (e.g. ``ncu -k regex:<name> -s 2
@@ -22,8 +27,17 @@ import torch
 from . import TransformedLinear, _lib, inputs
 
 
-def layer_steps(warm=3, timed=3):
-    case = inputs.SQUARE_2048
+def _case(what):
+    if what == "layer":
+        return inputs.SQUARE_2048
+    if what == "upproj":
+        return inputs.UPPROJ
+    stack = {c.name.split("_")[-1]: c for c in inputs.stack_cases(layers=1)}
+    return stack[what]
+
+
+def layer_steps(what="layer", warm=3, timed=3):
+    case = _case(what)
     inp = inputs.make_linear_inputs(case)
     dev = torch.device("cuda")
     lay = TransformedLinear(inp["W0"].to(dev), inp["theta_P"], inp["theta_R"], inp["perm_in"],
@@ -57,9 +71,10 @@ def cnp_points(calls=3):
 
 if __name__ == "__main__":
     what = sys.argv[1] if len(sys.argv) > 1 else "layer"
-    if what == "layer":
-        layer_steps()
+    if what in ("layer", "gate", "down", "upproj"):
+        layer_steps(what)
     elif what == "cnp":
         cnp_points()
     else:
-        raise SystemExit("usage: python -m orthogonal_equivalence_neumann_b300.profile_cases layer|cnp")
+        raise SystemExit("usage: python -m orthogonal_equivalence_neumann_b300.profile_cases "
+                         "layer|gate|down|upproj|cnp")
