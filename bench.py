@@ -81,6 +81,7 @@ def kernel_work(case):
         "tc_blockapply_scatter": ("hbm", blk_flops, blk_bytes),
         "tc_cluster_gather": ("hbm", blk_flops, blk_bytes),
         "tc_cluster_scatter": ("hbm", blk_flops, blk_bytes),
+        "tc_plain_apply": ("hbm", blk_flops, blk_bytes),
         "tc_dq": ("hbm", dq_flops, dq_bytes),
         "tc_cluster_dq": ("hbm", dq_flops, dq_bytes),
         "tc_permute_cols": ("hbm", 0.0, es * (T * di + T * do)),

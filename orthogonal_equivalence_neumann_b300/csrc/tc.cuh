@@ -73,6 +73,15 @@ poetx_status cluster_apply_bf16(const void* in, void* out, const void* Q, const 
                                 const int32_t* inv, int T, int d, int b, bool transpose_q,
                                 bool scatter, void* ws, size_t ws_bytes, cudaStream_t s, int max_clusters = 0);
 
+// Unpermuted block apply, bf16 in/out, fp32 accumulation (tcgen05), one CTA
+// per (block, token stripe) with the block's Qop resident in tensor memory:
+//   out[t][jb+i] = sum_k Qop_j[i][k] in[t][jb+k],  Qop_j = Q_j or Q_j^T.
+// b in {128, 256}.  With a column permutation before or after it, the
+// permuted applies of the shapes the cluster form does not take.
+bool plain_apply_supported(int d, int b);
+poetx_status plain_apply_bf16(const void* in, void* out, const void* Q, int T, int d, int b,
+                              bool transpose_q, cudaStream_t s);
+
 // dQ_j[i][k] = sum_t G[t][jb+i] V[t][jb+k] (both operands already gathered),
 // as n_split partial sums over token ranges: part [n_split][d/b, b, b] fp32,
 // every slot written (the sum over slots is dQ).  dq_splits gives the count

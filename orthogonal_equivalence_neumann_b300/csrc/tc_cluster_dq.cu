@@ -234,12 +234,15 @@ int pow2_cols(int used) {
   return c;
 }
 
+// Cluster sizes up to 8 (portable) only: where the blocks need more CTAs the
+// permuted operand is gathered once into the scratch and summed by tc_dq
+// (faster at the 2048 -> 5632 layer than 11-CTA clusters).
 bool dq_geometry(int d, int b, DqGeo* out) {
   if ((b != 128 && b != 256) || d % b) return false;
   const int nb = d / b;
   const int halves = b / 128;
-  const int order[15] = {8, 7, 6, 5, 4, 3, 2, 16, 15, 14, 13, 12, 11, 10, 9};
-  for (int oi = 0; oi < 15; ++oi) {
+  const int order[7] = {8, 7, 6, 5, 4, 3, 2};
+  for (int oi = 0; oi < 7; ++oi) {
     const int C = order[oi];
     if (nb % C) continue;
     DqGeo g;

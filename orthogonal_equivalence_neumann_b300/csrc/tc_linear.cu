@@ -7,7 +7,10 @@
 // so do the permuted block-diagonal applies (tc_blockapply.cu) for b in
 // {128, 256}, and so do the dQ token sums (tc_cluster_dq.cu, which gathers
 // the permuted operand in flight; tc_permute.cu + tc_dq.cu where the cluster
-// form does not fit); other block sizes use the CUDA-core kernels.
+// form does not fit); other block sizes use the CUDA-core kernels.  Where the
+// cluster applies do not fit (a CTA's share of the blocks exceeds its tensor
+// memory), a permuted apply is a column permutation through the scratch and
+// the unpermuted block apply (tc_plain_apply.cu).
 #include <mutex>
 
 #include "common.cuh"
@@ -54,13 +57,26 @@ static size_t ring_bytes(int T, int d, int b, bool scatter) {
                                                     : 0;
 }
 
-// Exchange rings of the block applies (forward, and the backward's g_z and dX).
+// A permuted apply the cluster form does not take: permutation of the
+// columns through a [T, d] bf16 copy in the scratch plus the unpermuted apply.
+static bool apply_staged(int d, int b, bool scatter) {
+  return !tc::cluster_apply_supported(d, b, scatter) && tc::plain_apply_supported(d, b) &&
+         tc::permute_supported(d);
+}
+
+// Scratch of one permuted apply: the exchange ring, or the staged copy.
+static size_t apply_bytes(int T, int d, int b, bool scatter) {
+  if (tc::cluster_apply_supported(d, b, scatter)) return ring_bytes(T, d, b, scatter);
+  return apply_staged(d, b, scatter) ? (size_t)T * d * 2 : 0;
+}
+
+// Scratch of the block applies (forward, and the backward's g_z and dX).
 static size_t apply_region_bytes(int T, int d_in, int d_out, int b_in, int b_out, bool backward) {
   // the backward may also run the forward applies (z recomputed without a saved copy)
   size_t bytes = 0;
-  const size_t rings[4] = {ring_bytes(T, d_in, b_in, false), ring_bytes(T, d_out, b_out, true),
-                           backward ? ring_bytes(T, d_out, b_out, false) : 0,
-                           backward ? ring_bytes(T, d_in, b_in, true) : 0};
+  const size_t rings[4] = {apply_bytes(T, d_in, b_in, false), apply_bytes(T, d_out, b_out, true),
+                           backward ? apply_bytes(T, d_out, b_out, false) : 0,
+                           backward ? apply_bytes(T, d_in, b_in, true) : 0};
   for (size_t r : rings)
     if (r > bytes) bytes = r;
   return round_up(bytes, 256);
@@ -106,9 +122,11 @@ size_t tc_cnp_ws_offset(int T, int d_in, int d_out, int b_in, int b_out) {
   return shared_region_bytes(T, d_in, d_out, b_in, b_out, true);
 }
 
-// Permuted block apply: a thread-block cluster when the shape allows, else one
-// CTA per token slab on the tensor cores, else the CUDA cores.  `inv` is the
-// inverse of the gather permutation.
+// Permuted block apply: a thread-block cluster when the shape allows, else a
+// column permutation through the scratch (`ws`, apply_bytes of it) and the
+// unpermuted apply, else one CTA per token slab on the tensor cores, else the
+// CUDA cores.  `inv` is the inverse of the permutation (gath or scat) in use;
+// a scatter without it takes the slab form where the cluster form does not fit.
 static poetx_status block_apply(const void* in, void* out, const void* Q, int T, int d, int b,
                                 const int32_t* gath, const int32_t* inv, const int32_t* scat,
                                 bool transpose_q, void* ws, cudaStream_t s, int max_clusters = 0) {
@@ -117,6 +135,15 @@ static poetx_status block_apply(const void* in, void* out, const void* Q, int T,
     return tc::cluster_apply_bf16(in, out, Q, scatter ? scat : gath, inv, T, d, b, transpose_q,
                                   scatter, ws, tc::cluster_apply_workspace_bytes(T, d, b, scatter), s,
                                   max_clusters);
+  if (apply_staged(d, b, scatter) && ws && (!scatter || inv)) {
+    if (!scatter) {   // out = apply(in[:, gath])
+      TC_TRY(tc::permute_cols_bf16(in, ws, gath, T, d, s));
+      return tc::plain_apply_bf16(ws, out, Q, T, d, b, transpose_q, s);
+    }
+    // out[:, scat[c]] = apply(in)[:, c], i.e. out = apply(in)[:, inv]
+    TC_TRY(tc::plain_apply_bf16(in, ws, Q, T, d, b, transpose_q, s));
+    return tc::permute_cols_bf16(ws, out, inv, T, d, s);
+  }
   if (tc::blockapply_supported(d, b))
     return tc::blockapply_bf16(in, out, Q, gath ? gath : scat, T, d, b, transpose_q, scatter, s);
   return launch_block_apply_simt(in, out, Q, T, d, b, gath, scat, transpose_q, POETX_BF16, s);
@@ -151,7 +178,7 @@ poetx_status tc_forward(const void* x, const void* W0m, const void* Q_P, const v
                         void* u, void* z, void* y, void* ws, cudaStream_t s) {
   TC_TRY(block_apply(x, u, Q_P, T, d_in, b_in, perm_in, inv_in, nullptr, false, ws, s));
   TC_TRY(tc::gemm_bf16(u, W0m, z, T, d_out, d_in, false, s));
-  if (y) TC_TRY(block_apply(z, y, Q_R, T, d_out, b_out, nullptr, nullptr, perm_out, false, ws, s));
+  if (y) TC_TRY(block_apply(z, y, Q_R, T, d_out, b_out, nullptr, inv_out, perm_out, false, ws, s));
   return POETX_OK;
 }
 
@@ -205,13 +232,29 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
   const size_t dq_bytes = dq_region_bytes(T, d_in, d_out, b_in, b_out);
   void* ws_dq = static_cast<uint8_t*>(ws) + apply_bytes;
   const int nb_in = d_in / b_in, nb_out = d_out / b_out;
-  auto sequential = [&](cudaStream_t st) -> poetx_status {
+  // the R side's g_z apply and dQ_R sums
+  auto r_side = [&](cudaStream_t st) -> poetx_status {
+    if (apply_staged(d_out, b_out, false) && !dq_cluster(T, d_out, b_out) && dq_tc(T, d_out, b_out)) {
+      // dy gathered once, for both g_z and the dQ_R sums
+      TC_TRY(tc::permute_cols_bf16(dy, ws_dq, perm_out, T, d_out, st));
+      TC_TRY(tc::plain_apply_bf16(ws_dq, gz, Q_R, T, d_out, b_out, true, st));
+      return tc::dq_bf16(ws_dq, z, T, d_out, b_out, slots_r, dqr, st);
+    }
     TC_TRY(block_apply(dy, gz, Q_R, T, d_out, b_out, perm_out, inv_out, nullptr, true, ws, st));
-    TC_TRY(dq(dy, z, T, d_out, b_out, perm_out, inv_out, nullptr, nullptr, dqr, slots_r, ws_dq,
-              dq_bytes, st));
-    TC_TRY(tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, st));
-    TC_TRY(block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, nullptr, perm_in, true, ws, st));
+    return dq(dy, z, T, d_out, b_out, perm_out, inv_out, nullptr, nullptr, dqr, slots_r, ws_dq,
+              dq_bytes, st);
+  };
+  auto p_dq = [&](cudaStream_t st) -> poetx_status {
     return dq(gu, x, T, d_in, b_in, nullptr, nullptr, perm_in, inv_in, dqp, slots_p, ws_dq, dq_bytes, st);
+  };
+  auto p_apply = [&](cudaStream_t st) -> poetx_status {
+    return block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, inv_in, perm_in, true, ws, st);
+  };
+  auto sequential = [&](cudaStream_t st) -> poetx_status {
+    TC_TRY(r_side(st));
+    TC_TRY(tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, st));
+    TC_TRY(p_apply(st));
+    return p_dq(st);
   };
   if (!cnp) return sequential(s);
   uint8_t* cnp_ws = static_cast<uint8_t*>(cnp->ws);
@@ -225,13 +268,42 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
   const bool dq_r = dq_cluster(T, d_out, b_out), dq_p = dq_cluster(T, d_in, b_in);
   std::unique_lock<std::mutex> lk(g_side_mu);
   SideStream* side = side_stream();
-  if (!side || 2 * ctas_r > sms || 2 * ctas_p > sms || cl_r < 2 || cl_p < 2 || !dq_r || !dq_p) {
+  if (!side || 2 * ctas_r > sms || 2 * ctas_p > sms) {
     // no overlap: everything in order on `s`
     lk.unlock();
     TC_TRY(sequential(s));
     TC_TRY(tc::cnp_bwd_side(cnp->theta_R, dqr, slots_r, nb_out, b_out, cnp->n, cnp->dtheta_R,
                             cnp_ws_r, s));
     return tc::cnp_bwd_side(cnp->theta_P, dqp, slots_p, nb_in, b_in, cnp->n, cnp->dtheta_P, cnp_ws, s);
+  }
+  auto fork = [&]() -> poetx_status {
+    if (cudaEventRecord(side->fork, s) != cudaSuccess ||
+        cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
+      return check_launch();
+    return POETX_OK;
+  };
+  if (cl_r < 2 || cl_p < 2 || !dq_r || !dq_p) {
+    // A side outside the cluster form: the applies and the dQ sums in order on
+    // `s`, each side's Cayley-Neumann backward on the library stream as soon
+    // as its dQ sums are done, beside the GEMM (which leaves the chain's SMs
+    // free) for the R side and beside the dX apply for the P side:
+    //   main: g_z apply, dQ_R | g_u GEMM | dQ_P | dX apply | join
+    //   side:                 | R prep + chain   | P prep + chain
+    poetx_status st = r_side(s);
+    if (st == POETX_OK) st = fork();
+    if (st == POETX_OK)
+      st = tc::cnp_bwd_side(cnp->theta_R, dqr, slots_r, nb_out, b_out, cnp->n, cnp->dtheta_R,
+                            cnp_ws_r, side->stream);
+    if (st == POETX_OK) st = tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s, ctas_r);
+    if (st == POETX_OK) st = p_dq(s);
+    if (st == POETX_OK) st = fork();
+    if (st == POETX_OK)
+      st = tc::cnp_bwd_side(cnp->theta_P, dqp, slots_p, nb_in, b_in, cnp->n, cnp->dtheta_P, cnp_ws,
+                            side->stream);
+    if (st == POETX_OK && cudaEventRecord(side->join, side->stream) != cudaSuccess) st = check_launch();
+    if (st == POETX_OK) st = p_apply(s);
+    if (cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess && st == POETX_OK) st = check_launch();
+    return st;
   }
   // Schedule (main = `s`, side = the library stream):
   //   main: g_z apply      | g_u GEMM (leaves the chain's SMs) | dX apply
@@ -246,12 +318,6 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
   const int side_r = cl_r - main_r, side_p = cl_p - main_p;
   const int used_r = tc::cluster_dq_splits(T, d_out, b_out) < side_r ? tc::cluster_dq_splits(T, d_out, b_out) : side_r;
   const int used_p = tc::cluster_dq_splits(T, d_in, b_in) < side_p ? tc::cluster_dq_splits(T, d_in, b_in) : side_p;
-  auto fork = [&]() -> poetx_status {
-    if (cudaEventRecord(side->fork, s) != cudaSuccess ||
-        cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
-      return check_launch();
-    return POETX_OK;
-  };
   poetx_status st = fork();
   if (st == POETX_OK)
     st = dq(dy, z, T, d_out, b_out, perm_out, inv_out, nullptr, nullptr, dqr, slots_r, ws_dq, dq_bytes,
@@ -271,7 +337,7 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
                           side->stream);
   if (st == POETX_OK && cudaEventRecord(side->join, side->stream) != cudaSuccess) st = check_launch();
   if (st == POETX_OK)
-    st = block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, nullptr, perm_in, true, ws, s, main_p);
+    st = block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, inv_in, perm_in, true, ws, s, main_p);
   if (cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess && st == POETX_OK) st = check_launch();
   return st;
 }

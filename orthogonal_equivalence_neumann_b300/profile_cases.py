@@ -49,12 +49,17 @@ def layer_steps(what="layer", warm=3, timed=3):
     _lib.poetx_stream_status()
     _lib.poetx_profile_report()
     _lib.poetx_profile_enable(True)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
     for _ in range(timed):
         lay.step(x, dy)
+    t1.record()
     torch.cuda.synchronize()
     _lib.poetx_profile_enable(False)
     for k, (n, ms) in sorted(_lib.poetx_profile_report().items()):
         print("%-22s %3d launches %8.1f us each" % (k, n, 1000.0 * ms / n))
+    print("eager step (event pairs recorded around every kernel) %.1f us" %
+          (1000.0 * t0.elapsed_time(t1) / timed))
 
 
 def cnp_points(calls=3):

@@ -451,6 +451,44 @@ def test_bf16_step_runs_on_the_tensor_core_kernels(b):
     assert "tc_permute_cols" not in names and "tc_dq" not in names, sorted(names)
 
 
+@pytest.mark.parametrize("d_in,d_out,b,T", [(4352, 512, 128, 333), (512, 5632, 256, 200),
+                                           (5632, 256, 256, 131)])
+def test_staged_applies_parity(d_in, d_out, b, T):
+    """Sides whose blocks do not fit the cluster applies (34 blocks of 128, 22
+    of 256: a CTA's share exceeds its tensor memory) run a column permutation
+    through the scratch plus the unpermuted block apply; ragged token tiles."""
+    case = inputs.LinearCase("staged_%d_%d_%d" % (d_in, d_out, b), d_in, d_out, b, b, 3, T, 0.005,
+                             "bf16", 880 + T)
+    check_layer(case, inputs.make_linear_inputs(case))
+
+
+@pytest.mark.parametrize("which", [4, 6])   # gate 2048 -> 5632, down 5632 -> 2048
+def test_wide_stack_layers_run_on_the_staged_applies(which):
+    """The stack's 5632-wide side (22 blocks of 256) takes the column
+    permutation plus the unpermuted apply on the tensor cores, not the slab
+    kernel or the CUDA cores (checked by name: parity alone would not show a
+    fall-back)."""
+    case = inputs.stack_cases(T=256, layers=1)[which]
+    inp = inputs.make_linear_inputs(case)
+    lay = TransformedLinear(inp["W0"].cuda(), inp["theta_P"], inp["theta_R"], inp["perm_in"],
+                            inp["perm_out"], case.b_in, case.b_out, case.n, T_max=case.T)
+    x, dy = inp["x"].cuda(), inp["dy"].cuda()
+    lay.step(x, dy)
+    torch.cuda.synchronize()
+    _lib.poetx_profile_report()
+    _lib.poetx_profile_enable(True)
+    try:
+        lay.step(x, dy)
+        torch.cuda.synchronize()
+    finally:
+        _lib.poetx_profile_enable(False)
+    names = set(_lib.poetx_profile_report())
+    for k in ("tc_plain_apply", "tc_permute_cols", "tc_dq", "tc_cluster_gather",
+              "tc_cluster_scatter", "tc_cluster_dq", "tc_gemm_nt", "tc_gemm_nn"):
+        assert k in names, (k, sorted(names))
+    assert not any(n.startswith("tc_blockapply") or n.endswith("_simt") for n in names), sorted(names)
+
+
 def test_xfast_and_xmem_give_the_same_gradients():
     """POET-Xmem recomputes z with the forward's own kernels, so y and dX are
     bit-identical to POET-Xfast; the block gradients are token sums kept as
