@@ -130,10 +130,15 @@ poetx_status cnp_fwd_pair_bf16ops(const float* theta0, int nb0, const float* the
 size_t cnp_bwd_workspace_bytes(int d_in, int b_in, int d_out, int b_out);
 // One side alone (its workspace part: 10 * nb * b * b bytes, the P side's at
 // the start of the CNP backward workspace, the R side's after it); the chain
-// kernel takes cnp_bwd_ctas(nb, b) CTAs.  parts: 1 = the prep kernel (K, K^T and the
-// summed dQ in bf16), 2 = the chain kernel (after the prep), 3 = both.
+// kernel runs one cluster of (b/128) * (b/64) CTAs per block, and
+// with `narrow` two CTAs per block that stream K and G through a ring (for
+// running beside a kernel that holds most SMs: cnp_bwd_ctas(nb, b) = nb * b /
+// 128 is the count of SMs that kernel leaves free).  parts: 1 = the prep
+// kernel (K, K^T and the summed dQ in bf16), 2 = the chain kernel (after the
+// prep), 3 = both.
 poetx_status cnp_bwd_side(const float* theta, const float* dQ, int splits, int nb, int b, int n,
-                          float* dtheta, void* ws, cudaStream_t s, int parts = 3);
+                          float* dtheta, void* ws, cudaStream_t s, int parts = 3,
+                          bool narrow = false);
 int cnp_bwd_ctas(int nb, int b);
 // dQ_P / dQ_R come as `splits_P` / `splits_R` partial-sum slots [splits][nb, b, b].
 poetx_status cnp_bwd_layer(const float* theta_P, const float* dQ_P, int splits_P, int nb_P, int b_P,

@@ -376,10 +376,288 @@ __global__ void __launch_bounds__(kPrepThreads)
   }
 }
 
-constexpr int kBwdThreads = 320;   // warp 0: TMEM + MMA; warp 1: TMA; warps 2..9: workers
-constexpr int kBwdWorkers = 256;
+// One cluster per block: CTA (row half mh, column slab ns) of the cluster
+// (rank = ns * MH + mh; MH = B / 128 row halves, NS = B / 64 slabs of 64
+// columns) runs the transpose of the adjoint chain on rows [128 mh, 128 mh +
+// 128) and columns [64 ns, 64 ns + 64) of
+//   X^T_1 = K, Y^T_1 = G^T,
+//   X^T_{i+1} = K X^T_i + 2K,  Y^T_{i+1} = G^T X^T_i + K Y^T_i + 2G^T,  dK^T = Y^T_{n+1}
+// (the transpose of X_{i+1} = X_i A + 2A, Y_{i+1} = X_i G + Y_i A + 2G with
+// A = K^T).  The A operands are resident for the whole chain: the CTA's rows
+// of K (K-major) and of G^T (MN-major: rows of G); the B operands are the
+// slab's columns of X^T_i and Y^T_i over all B rows.  Each step's MMAs
+// (M = 128, N = 64, K = 16, fp32 in TMEM) give the CTA's rows of the next B
+// operands: the workers write them as bf16 into the CTA's own B buffers and
+// one bulk copy per operand sends the same rows into the other row half's
+// buffers (the only exchange; both halves' MMAs of a step signal both CTAs
+// through one multicast commit, so a buffer is overwritten only after every
+// MMA reading it has finished).  The terms 2K and 2G^T enter as MMAs of the
+// slab's 64 columns of K and G^T against a 2I tile.  At the end the workers
+// write the CTA's tile of dK^T (fp32) to the workspace, and after a cluster
+// barrier the cluster packs dtheta(i, k) = dK[i][k] - dK[k][i] = dK^T[k][i] -
+// dK^T[i][k] (i < k) from 32 x 32 tile pairs, every entry written once.
+constexpr int kBwdThreads = 192;   // warp 0: TMA and copies; warp 1: TMEM + MMA; warps 2..5: workers
+constexpr int kBwdWorkers = 128;
 constexpr int kPackPitch = 33;     // fp32 pitch of the 32 x 32 transpose tiles
 
+template <int B>
+struct BwdGeo {
+  static constexpr int MH = B / 128, NS = B / 64, CL = MH * NS;
+  static constexpr int a_bytes = 128 * B * 2;   // one A operand: 128 rows x B
+  static constexpr int b_bytes = B * 128;       // one B operand: B rows x 64 columns
+  static constexpr int i_bytes = 64 * 128;      // the 2I tile
+  static constexpr int half_bytes = 128 * 128;  // a row half of a B operand
+  static constexpr int off_a1 = 1024;
+  static constexpr int off_a2 = off_a1 + a_bytes;
+  static constexpr int off_bx = off_a2 + a_bytes;
+  static constexpr int off_by = off_bx + b_bytes;
+  static constexpr int off_bi = off_by + b_bytes;
+  static constexpr int smem = 1024 + off_bi + i_bytes;   // + alignment slack
+  static constexpr uint32_t load_bytes = 2 * a_bytes + 2 * b_bytes;
+};
+
+template <int B>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    cnp_bwd_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_constant__ CUtensorMap tg0,
+                   const __grid_constant__ CUtensorMap tk1, const __grid_constant__ CUtensorMap tg1,
+                   Side s0, Side s1, int n, int* err) {
+  using Geo = BwdGeo<B>;
+  constexpr int MH = Geo::MH, CL = Geo::CL;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int blk = (int)blockIdx.x / CL;
+  const bool second = blk >= s0.nb;
+  const Side& sd = second ? s1 : s0;
+  const CUtensorMap* tk = second ? &tk1 : &tk0;
+  const CUtensorMap* tg = second ? &tg1 : &tg0;
+  const int j = second ? blk - s0.nb : blk;
+  const int rank = (int)cluster_ctarank();
+  const int mh = rank % MH, ns = rank / MH;
+  const int peer = rank ^ 1;   // the other row half of the slab (MH == 2)
+  uint8_t* a1 = smem + Geo::off_a1;
+  uint8_t* a2 = smem + Geo::off_a2;
+  uint8_t* bx = smem + Geo::off_bx;
+  uint8_t* by = smem + Geo::off_by;
+  uint8_t* bi = smem + Geo::off_bi;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* ops_full = bars;        // operands loaded and the 2I tile written
+  uint64_t* mma_done = bars + 1;    // this step's MMAs of both row halves have completed
+  uint64_t* rows_ready = bars + 2;  // the workers have written this CTA's rows of the next B operands
+  uint64_t* recv = bars + 3;        // the other row half's rows have landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    mbar_init(ops_full, 2);
+    mbar_init(mma_done, MH);
+    mbar_init(rows_ready, kBwdWorkers);
+    mbar_init(recv, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 128);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // every CTA's barriers are initialised before any remote arrival or copy
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t dx = tmem_base, dy = tmem_base + 64;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA: the operands; then the row exchange
+    if (lane == 0) {
+      mbar_arrive_expect_tx(ops_full, Geo::load_bytes);
+      const int r0 = j * B;
+      for (int q = 0; q < B / 64; ++q)       // A1: K rows [128 mh, +128), K-major
+        for (int rb = 0; rb < 2; ++rb)
+          tma_load_2d(a1 + q * (128 * 128) + rb * (64 * 128), tk, q * 64, r0 + 128 * mh + 64 * rb, ops_full);
+      for (int mc = 0; mc < 2; ++mc)         // A2: G^T rows = G columns [128 mh, +128), MN-major
+        for (int kb = 0; kb < B / 64; ++kb)
+          tma_load_2d(a2 + mc * Geo::b_bytes + kb * (64 * 128), tg, 128 * mh + 64 * mc, r0 + 64 * kb, ops_full);
+      for (int kb = 0; kb < B / 64; ++kb)    // B_X = X^T_1 = K columns of the slab, MN-major
+        tma_load_2d(bx + kb * (64 * 128), tk, 64 * ns, r0 + 64 * kb, ops_full);
+      for (int q = 0; q < B / 64; ++q)       // B_Y = Y^T_1 = G^T: rows of G in the slab, K-major
+        tma_load_2d(by + q * (64 * 128), tg, q * 64, r0 + 64 * ns, ops_full);
+      if constexpr (MH == 2) {
+        // after each step but the last: this CTA's new rows to the other half
+        const uint32_t rx = mapa_shared(smem_u32(bx + mh * Geo::half_bytes), (uint32_t)peer);
+        const uint32_t ry = mapa_shared(smem_u32(by + mh * Geo::half_bytes), (uint32_t)peer);
+        const uint32_t rb = mapa_shared(smem_u32(recv), (uint32_t)peer);
+        for (int i = 1; i < n && ok; ++i) {
+          if (!(ok = mbar_wait(rows_ready, (i - 1) & 1, err))) break;
+          bulk_copy_s2cluster(rx, bx + mh * Geo::half_bytes, Geo::half_bytes, rb);
+          bulk_copy_s2cluster(ry, by + mh * Geo::half_bytes, Geo::half_bytes, rb);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA
+    if (lane == 0) {
+      const uint32_t id_km = idesc_bf16(128, 64, false, true);    // A K-major, B MN-major
+      const uint32_t id_kk = idesc_bf16(128, 64, false, false);   // A K-major, B K-major
+      const uint32_t id_mm = idesc_bf16(128, 64, true, true);     // A MN-major, B MN-major
+      const uint32_t id_mk = idesc_bf16(128, 64, true, false);    // A MN-major, B K-major
+      const uint32_t a1b = smem_u32(a1), a2b = smem_u32(a2), bxb = smem_u32(bx), byb = smem_u32(by),
+                     bib = smem_u32(bi);
+      const uint16_t mask = (uint16_t)((1u << rank) | (1u << peer));
+      ok = mbar_wait(ops_full, 0, err);
+      for (int i = 1; i <= n && ok; ++i) {
+        if (i > 1) {
+          if (!(ok = mbar_wait(rows_ready, (i - 2) & 1, err))) break;
+          if constexpr (MH == 2)
+            if (!(ok = mbar_wait(recv, (i - 2) & 1, err))) break;
+        }
+        tc_fence_after();
+        // X^T_{i+1} = K X^T_i + 2K (not needed after the last step)
+        if (i < n) {
+#pragma unroll 4
+          for (int kk = 0; kk < B / 16; ++kk)
+            mma_bf16(dx, sw128_desc(a1b + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024),
+                     sw128_desc(bxb + kk * 2048, Geo::b_bytes, 1024), id_km, kk != 0);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(dx, sw128_desc(a1b + ns * (128 * 128) + kk * 32, 16, 1024),
+                     sw128_desc(bib + kk * 32, 16, 1024), id_kk, 1);
+        }
+        // Y^T_{i+1} = G^T X^T_i + K Y^T_i + 2G^T
+#pragma unroll 4
+        for (int kk = 0; kk < B / 16; ++kk)
+          mma_bf16(dy, sw128_desc(a2b + kk * 2048, Geo::b_bytes, 1024),
+                   sw128_desc(bxb + kk * 2048, Geo::b_bytes, 1024), id_mm, kk != 0);
+        if (i == 1) {   // Y^T_1 = G^T as loaded: K-major
+#pragma unroll 4
+          for (int kk = 0; kk < B / 16; ++kk)
+            mma_bf16(dy, sw128_desc(a1b + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024),
+                     sw128_desc(byb + (kk >> 2) * (64 * 128) + (kk & 3) * 32, 16, 1024), id_kk, 1);
+        } else {
+#pragma unroll 4
+          for (int kk = 0; kk < B / 16; ++kk)
+            mma_bf16(dy, sw128_desc(a1b + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024),
+                     sw128_desc(byb + kk * 2048, Geo::b_bytes, 1024), id_km, 1);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16(dy, sw128_desc(a2b + (4 * ns + kk) * 2048, Geo::b_bytes, 1024),
+                   sw128_desc(bib + kk * 32, 16, 1024), id_mk, 1);
+        // the other half's rows of the next operands land on `recv`; expected
+        // before this step's commit, so before the other half may send them
+        if constexpr (MH == 2)
+          if (i < n) mbar_arrive_expect_tx(recv, 2 * Geo::half_bytes);
+        if constexpr (MH == 2) mma_commit_multicast(mma_done, mask);
+        else mma_commit(mma_done);
+      }
+    }
+  } else {
+    // ------------------------------------------------ workers: 2I tile, next operands, dK^T
+    const int wt = threadIdx.x - 64;
+    const int quarter = warp % 4;
+    const int m = quarter * 32 + lane;   // TMEM lane = row of the CTA's half
+    const int k = 128 * mh + m;          // its row in the B operands
+    for (int u = wt; u < Geo::i_bytes / 16; u += kBwdWorkers)
+      reinterpret_cast<uint4*>(bi)[u] = make_uint4(0u, 0u, 0u, 0u);
+    asm volatile("bar.sync 1, %0;" ::"n"(kBwdWorkers) : "memory");
+    if (wt < 64)   // 2.0 at (r, r): K-major [64 n][64 k]
+      *reinterpret_cast<__nv_bfloat16*>(bi + sw128_offset(wt, wt, 64)) = __float2bfloat16_rn(2.f);
+    fence_proxy_async_smem();
+    asm volatile("bar.sync 1, %0;" ::"n"(kBwdWorkers) : "memory");
+    if (wt == 0) mbar_arrive(ops_full);
+    for (int i = 1; i <= n && ok; ++i) {
+      if (!(ok = mbar_wait(mma_done, (i - 1) & 1, err))) break;
+      tc_fence_after();
+      const uint32_t lrow = (uint32_t)(quarter * 32) << 16;
+      if (i < n) {
+        // row k of X^T_{i+1} and Y^T_{i+1}: 64 columns each, bf16, MN-major (128-byte swizzle)
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          uint32_t r[2][32];
+          const uint32_t col = t == 0 ? dx : dy;
+          tmem_ld32(col + lrow, r[0]);
+          tmem_ld32(col + 32u + lrow, r[1]);
+          tmem_ld_wait();
+          tmem_regs_ready(r[0]);
+          tmem_regs_ready(r[1]);
+          uint8_t* row = (t == 0 ? bx : by) + k * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[c >> 2][(c & 3) * 8 + e]);
+            *reinterpret_cast<uint4*>(row + ((c ^ (k & 7)) << 4)) = pack8(v);
+          }
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        mbar_arrive(rows_ready);
+      } else {
+        // dK^T rows: [128 mh + m][64 ns, +64) of block j, fp32
+        uint32_t r[2][32];
+        tmem_ld32(dy + lrow, r[0]);
+        tmem_ld32(dy + 32u + lrow, r[1]);
+        tmem_ld_wait();
+        tmem_regs_ready(r[0]);
+        tmem_regs_ready(r[1]);
+        float4* dst = reinterpret_cast<float4*>(sd.dK + ((size_t)j * B + k) * B + 64 * ns);
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          dst[q] = make_float4(__uint_as_float(r[q >> 3][(q & 7) * 4]), __uint_as_float(r[q >> 3][(q & 7) * 4 + 1]),
+                               __uint_as_float(r[q >> 3][(q & 7) * 4 + 2]),
+                               __uint_as_float(r[q >> 3][(q & 7) * 4 + 3]));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  // every CTA's dK^T tile is written (release/acquire at cluster scope), no
+  // copy into or commit onto another CTA is outstanding
+  cluster_sync();
+  // ---- pack: 32 x 32 tile pairs (ti <= tk) shared round-robin by the cluster's CTAs and warps
+  {
+    constexpr int NT = B / 32;
+    constexpr int W = kBwdThreads / 32;
+    float* tA = reinterpret_cast<float*>(smem + Geo::off_a1) + warp * (2 * 32 * kPackPitch);
+    float* tB = tA + 32 * kPackPitch;
+    const float* dKt = sd.dK + (size_t)j * B * B;
+    float* dth = sd.dtheta + (size_t)j * (B * (B - 1) / 2);
+    int t = 0;
+    for (int ti = 0; ti < NT; ++ti)
+      for (int tk = ti; tk < NT; ++tk, ++t) {
+        if (t % CL != rank || (t / CL) % W != warp) continue;
+        // tA[ii][kk] = dK^T[32ti+ii][32tk+kk],  tB[kk][ii] = dK^T[32tk+kk][32ti+ii]: all 64
+        // row segments requested before any is stored (other CTAs' rows: read at L2)
+        float va[32], vb[32];
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) {
+          va[ii] = __ldcg(dKt + (size_t)(32 * ti + ii) * B + 32 * tk + lane);
+          vb[ii] = __ldcg(dKt + (size_t)(32 * tk + ii) * B + 32 * ti + lane);
+        }
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) {
+          tA[ii * kPackPitch + lane] = va[ii];
+          tB[ii * kPackPitch + lane] = vb[ii];
+        }
+        __syncwarp();
+        for (int ii = 0; ii < 32; ++ii) {
+          const int i = 32 * ti + ii, kc = 32 * tk + lane;
+          if (i < kc)   // dK[i][kc] - dK[kc][i] = dK^T[kc][i] - dK^T[i][kc]
+            dth[skew_row_start(i, B) + (kc - i - 1)] = tB[lane * kPackPitch + ii] - tA[ii * kPackPitch + lane];
+        }
+        __syncwarp();
+      }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 128);
+  }
+}
+
+constexpr int kRingThreads = 320;   // warp 0: TMEM + MMA; warp 1: TMA; warps 2..9: workers
+constexpr int kRingWorkers = 256;
+
+// The narrow form of the same chain, for running beside a kernel that holds
+// most SMs (the R side's chain beside the g_u GEMM): two CTAs per block.
 // One CTA = one 128-row slab of one block; for B = 256 the two slabs of a
 // block form a cluster.  With A = K^T and G = dL/dQ the chain
 //   X_1 = A, Y_1 = G,  X_{i+1} = X_i A + 2A,  Y_{i+1} = X_i G + Y_i A + 2G,  dK = Y_{n+1}
@@ -393,8 +671,8 @@ constexpr int kPackPitch = 33;     // fp32 pitch of the 32 x 32 transpose tiles
 // from 32 x 32 tile pairs transposed through shared memory, each CTA taking
 // half of the tiles, every packed entry written exactly once.
 template <int B>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    cnp_bwd_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_constant__ CUtensorMap tg0,
+__global__ void __launch_bounds__(kRingThreads, 1)
+    cnp_bwd_ring_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_constant__ CUtensorMap tg0,
                    const __grid_constant__ CUtensorMap tt0, const __grid_constant__ CUtensorMap tk1,
                    const __grid_constant__ CUtensorMap tg1, const __grid_constant__ CUtensorMap tt1,
                    Side s0, Side s1, int n, int stages, int* err) {
@@ -432,7 +710,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bfull + st, 1);
       mbar_init(bempty + st, 1);
     }
-    mbar_init(afull, kBwdWorkers);
+    mbar_init(afull, kRingWorkers);
     mbar_init(stepdone, 1);
     mbar_init(a0full, 1);
     fence_mbar_init();
@@ -520,9 +798,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int half = (warp - 2) / 4;
     const int r = quarter * 32 + lane;
     const int row = r0 + r;
-    for (int u = wt; u < i_bytes / 16; u += kBwdWorkers)
+    for (int u = wt; u < i_bytes / 16; u += kRingWorkers)
       reinterpret_cast<uint4*>(itl)[u] = make_uint4(0u, 0u, 0u, 0u);
-    asm volatile("bar.sync 1, %0;" ::"n"(kBwdWorkers) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(kRingWorkers) : "memory");
     if (wt < 128)   // 2.0 at (r, r) of the slab's K range
       *reinterpret_cast<__nv_bfloat16*>(itl + sw128_offset(wt, wt, 128)) = __float2bfloat16_rn(2.f);
     fence_proxy_async_smem();
@@ -587,7 +865,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int t = 0;
     for (int ti = 0; ti < NT; ++ti)
       for (int tk = ti; tk < NT; ++tk, ++t) {
-        if (t % CT != slab || (t / CT) % (kBwdThreads / 32) != warp) continue;
+        if (t % CT != slab || (t / CT) % (kRingThreads / 32) != warp) continue;
         // A[ii][kk] = dK[32ti+ii][32tk+kk],  Bt[kk][ii] = dK[32tk+kk][32ti+ii]: all 64
         // row segments are requested before any is stored (one round trip to L2;
         // the partner slab's rows were written by another CTA: read at L2)
@@ -618,6 +896,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_dealloc(tmem_base, ncols);
   }
 }
+
 
 }  // namespace
 
@@ -685,16 +964,8 @@ size_t cnp_bwd_workspace_bytes(int d_in, int b_in, int d_out, int b_out) {
 namespace {
 
 template <int B>
-poetx_status cnp_bwd_launch(const Side& s0, const Side& s1, int n, cudaStream_t s, int parts = 3) {
+poetx_status cnp_bwd_ring_launch(const Side& s0, const Side& s1, int n, cudaStream_t s) {
   const int nb = s0.nb + s1.nb;
-  if (parts & 1) {
-    {
-      KernelScope ks_("tc_cnp_bwd_prep", s);
-      cnp_prep_kernel<B><<<dim3(B / kPrepRows, nb, kPrepZ), kPrepThreads, 0, s>>>(s0, s1);
-    }
-    const poetx_status st = check_launch();
-    if (st != POETX_OK || !(parts & 2)) return st;
-  }
   CUtensorMap tk0, tg0, tt0, tk1, tg1, tt1;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
@@ -712,11 +983,11 @@ poetx_status cnp_bwd_launch(const Side& s0, const Side& s1, int n, cudaStream_t 
   int stages = (kSmemMax - fixed) / chunk_bytes;
   if (stages > kMaxStages) stages = kMaxStages;
   const int smem = fixed + stages * chunk_bytes;
-  auto kern = cnp_bwd_kernel<B>;
+  auto kern = cnp_bwd_ring_kernel<B>;
   set_max_dynamic_smem((const void*)kern, smem);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(B / 128, nb);
-  cfg.blockDim = dim3(kBwdThreads);
+  cfg.blockDim = dim3(kRingThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -736,16 +1007,66 @@ poetx_status cnp_bwd_launch(const Side& s0, const Side& s1, int n, cudaStream_t 
   return check_launch();
 }
 
+// narrow: the two-CTA ring form (beside a kernel that holds most SMs), else
+// the cluster form (b/128 * b/64 CTAs per block).
+template <int B>
+poetx_status cnp_bwd_launch(const Side& s0, const Side& s1, int n, cudaStream_t s, int parts = 3,
+                            bool narrow = false) {
+  const int nb = s0.nb + s1.nb;
+  if (parts & 1) {
+    {
+      KernelScope ks_("tc_cnp_bwd_prep", s);
+      cnp_prep_kernel<B><<<dim3(B / kPrepRows, nb, kPrepZ), kPrepThreads, 0, s>>>(s0, s1);
+    }
+    const poetx_status st = check_launch();
+    if (st != POETX_OK || !(parts & 2)) return st;
+  }
+  if (narrow) return cnp_bwd_ring_launch<B>(s0, s1, n, s);
+  CUtensorMap tk0, tg0, tk1, tg1;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  const Side& t0 = s0.nb > 0 ? s0 : s1;
+  const Side& t1 = s1.nb > 0 ? s1 : s0;
+  if (!make_tmap_2d(&tk0, t0.Kd, bf, 2, (uint64_t)t0.nb * B, B, 64, 64, sw) ||
+      !make_tmap_2d(&tg0, t0.Gd, bf, 2, (uint64_t)t0.nb * B, B, 64, 64, sw) ||
+      !make_tmap_2d(&tk1, t1.Kd, bf, 2, (uint64_t)t1.nb * B, B, 64, 64, sw) ||
+      !make_tmap_2d(&tg1, t1.Gd, bf, 2, (uint64_t)t1.nb * B, B, 64, 64, sw))
+    return POETX_ERR_CUDA;
+  using Geo = BwdGeo<B>;
+  auto kern = cnp_bwd_kernel<B>;
+  set_max_dynamic_smem((const void*)kern, Geo::smem);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(Geo::CL * nb);
+  cfg.blockDim = dim3(kBwdThreads);
+  cfg.dynamicSmemBytes = Geo::smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = Geo::CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int* err = device_error_word();
+  {
+    KernelScope ks_("tc_cnp_bwd", s);
+    if (cudaLaunchKernelEx(&cfg, kern, tk0, tg0, tk1, tg1, s0, s1, n, err) != cudaSuccess)
+      return check_launch();
+  }
+  return check_launch();
+}
+
 template <int B>
 poetx_status cnp_bwd_sides(const Side& s0, const Side& s1, int n, cudaStream_t s) {
   return cnp_bwd_launch<B>(s0, s1, n, s);
 }
 
-poetx_status cnp_bwd_one(const Side& sd, int b, int n, cudaStream_t s, int parts = 3) {
+poetx_status cnp_bwd_one(const Side& sd, int b, int n, cudaStream_t s, int parts = 3,
+                         bool narrow = false) {
   Side none = sd;
   none.nb = 0;
-  return b == 256 ? cnp_bwd_launch<256>(sd, none, n, s, parts)
-                  : cnp_bwd_launch<128>(sd, none, n, s, parts);
+  return b == 256 ? cnp_bwd_launch<256>(sd, none, n, s, parts, narrow)
+                  : cnp_bwd_launch<128>(sd, none, n, s, parts, narrow);
 }
 
 // The side's part of the workspace: K, K^T, G (bf16) and dK (fp32) of nb blocks.
@@ -769,12 +1090,12 @@ Side carve(const float* theta, const float* dQ, int n_part, float* dtheta, int n
 }  // namespace
 
 poetx_status cnp_bwd_side(const float* theta, const float* dQ, int splits, int nb, int b, int n,
-                          float* dtheta, void* ws, cudaStream_t s, int parts) {
+                          float* dtheta, void* ws, cudaStream_t s, int parts, bool narrow) {
   if (!cnp_supported(b) || n < 1 || nb > 65535 || splits < 1 || parts < 1 || parts > 3)
     return POETX_ERR_UNSUPPORTED;
   if (nb <= 0) return POETX_OK;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  return cnp_bwd_one(carve(theta, dQ, splits, dtheta, nb, b, w), b, n, s, parts);
+  return cnp_bwd_one(carve(theta, dQ, splits, dtheta, nb, b, w), b, n, s, parts, narrow);
 }
 
 int cnp_bwd_ctas(int nb, int b) { return nb * (b / 128); }

@@ -289,17 +289,19 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
     // free) for the R side and beside the dX apply for the P side:
     //   main: g_z apply, dQ_R | g_u GEMM | dQ_P | dX apply | join
     //   side:                 | R prep + chain   | P prep + chain
+    // (both chains in their narrow form: the GEMM and the dX apply beside
+    // them leave few SMs free)
     poetx_status st = r_side(s);
     if (st == POETX_OK) st = fork();
     if (st == POETX_OK)
       st = tc::cnp_bwd_side(cnp->theta_R, dqr, slots_r, nb_out, b_out, cnp->n, cnp->dtheta_R,
-                            cnp_ws_r, side->stream);
+                            cnp_ws_r, side->stream, 3, true);
     if (st == POETX_OK) st = tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s, ctas_r);
     if (st == POETX_OK) st = p_dq(s);
     if (st == POETX_OK) st = fork();
     if (st == POETX_OK)
       st = tc::cnp_bwd_side(cnp->theta_P, dqp, slots_p, nb_in, b_in, cnp->n, cnp->dtheta_P, cnp_ws,
-                            side->stream);
+                            side->stream, 3, true);
     if (st == POETX_OK && cudaEventRecord(side->join, side->stream) != cudaSuccess) st = check_launch();
     if (st == POETX_OK) st = p_apply(s);
     if (cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess && st == POETX_OK) st = check_launch();
@@ -313,7 +315,10 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
   // sums take the larger half: the P chain waits for them, not for dX, so
   // finishing them first lets the chain run beside the end of the dX apply
   // (measured at the square 2048 layer: 15 clusters as 7 + 8 gave 0.379 ms
-  // per step, 8 + 7 0.384, 6 + 9 0.380).
+  // per step, 8 + 7 0.384, 6 + 9 0.380).  The R chain runs in its narrow form
+  // (two CTAs per block: the GEMM beside it leaves 20 SMs free, where the
+  // cluster form's 8 CTAs per block would need four waves and delay dQ_P); the
+  // P chain, beside the dX apply, in the cluster form.
   const int main_r = (cl_r + 1) / 2, main_p = cl_p / 2;
   const int side_r = cl_r - main_r, side_p = cl_p - main_p;
   const int used_r = tc::cluster_dq_splits(T, d_out, b_out) < side_r ? tc::cluster_dq_splits(T, d_out, b_out) : side_r;
@@ -324,7 +329,7 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
             side->stream, side_r);
   if (st == POETX_OK)
     st = tc::cnp_bwd_side(cnp->theta_R, dqr, used_r, nb_out, b_out, cnp->n, cnp->dtheta_R, cnp_ws_r,
-                          side->stream);
+                          side->stream, 3, true);
   if (st == POETX_OK)
     st = block_apply(dy, gz, Q_R, T, d_out, b_out, perm_out, inv_out, nullptr, true, ws, s, main_r);
   if (st == POETX_OK) st = tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s, ctas_r);

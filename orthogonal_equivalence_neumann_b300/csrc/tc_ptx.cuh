@@ -302,6 +302,29 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       : "memory");
 }
 
+// As mma_commit, arriving on the barrier at the same shared-memory offset in
+// every CTA of the cluster whose rank bit is set in `cta_mask`.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// Bulk copy from this CTA's shared memory into another CTA's of the cluster
+// (`dst` and `bar` are shared::cluster addresses, e.g. from mapa_shared; both
+// addresses 16-byte aligned, size a multiple of 16), counted against the
+// destination CTA's mbarrier (complete_tx).
+__device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst, const void* src, uint32_t bytes,
+                                                    uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- CTA pairs (cta_group::2)
 // A pair is the two CTAs of a cluster whose ranks differ in bit 0.  One MMA
 // issued by the pair's first CTA spans both: A (M = 256) is split by rows,

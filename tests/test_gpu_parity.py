@@ -489,6 +489,18 @@ def test_wide_stack_layers_run_on_the_staged_applies(which):
     assert not any(n.startswith("tc_blockapply") or n.endswith("_simt") for n in names), sorted(names)
 
 
+@pytest.mark.parametrize("d_in,d_out,T", [(512, 768, 200), (2048, 2048, 600)])
+@pytest.mark.parametrize("b,n", [(256, 1), (256, 2), (256, 5), (128, 1), (128, 4)])
+def test_bf16_chain_backward_orders(d_in, d_out, T, b, n):
+    """The tensor-core Cayley-Neumann backward at several truncation orders,
+    both block sizes: the cluster form (a block split over row halves and
+    64-column slabs; n = 1 has no exchange step) and, where the backward runs
+    on two streams (the 2048 layer), the two-CTA ring form of the R side."""
+    case = inputs.LinearCase("chain_%d_%d_%d" % (d_in, b, n), d_in, d_out, b, b, n, T, 0.005, "bf16",
+                             610 + b + n + d_in)
+    check_layer(case, inputs.make_linear_inputs(case))
+
+
 def test_xfast_and_xmem_give_the_same_gradients():
     """POET-Xmem recomputes z with the forward's own kernels, so y and dX are
     bit-identical to POET-Xfast; the block gradients are token sums kept as
