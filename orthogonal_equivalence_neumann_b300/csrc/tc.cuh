@@ -133,11 +133,11 @@ size_t cnp_bwd_workspace_bytes(int d_in, int b_in, int d_out, int b_out);
 // kernel runs one cluster of (b/128) * (b/64) CTAs per block, and
 // with `narrow` two CTAs per block that stream K and G through a ring (for
 // running beside a kernel that holds most SMs: cnp_bwd_ctas(nb, b) = nb * b /
-// 128 is the count of SMs that kernel leaves free).  parts: 1 = the prep
-// kernel (K, K^T and the summed dQ in bf16), 2 = the chain kernel (after the
-// prep), 3 = both.
+// 128 is the count of SMs that kernel leaves free).  parts (bit flags): 1 =
+// dense bf16 K and K^T from theta (needs only theta: may run early), 2 = the
+// summed dQ as bf16 G, 4 = the chain (after both); 7 = all three.
 poetx_status cnp_bwd_side(const float* theta, const float* dQ, int splits, int nb, int b, int n,
-                          float* dtheta, void* ws, cudaStream_t s, int parts = 3,
+                          float* dtheta, void* ws, cudaStream_t s, int parts = 7,
                           bool narrow = false);
 int cnp_bwd_ctas(int nb, int b);
 // dQ_P / dQ_R come as `splits_P` / `splits_R` partial-sum slots [splits][nb, b, b].

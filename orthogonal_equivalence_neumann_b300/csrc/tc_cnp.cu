@@ -287,10 +287,13 @@ constexpr int kPrepRows = 32;
 // the packed rows above, which hold the group's columns contiguously.  All
 // loads are issued before their stores.
 constexpr int kPrepZ = 4;
+// parts of the CNP backward (cnp_bwd_side): the dense K and K^T from theta,
+// the summed dQ as bf16 G, the chain
+constexpr int kPrepK = 1, kPrepG = 2, kChain = 4;
 
 template <int B>
 __global__ void __launch_bounds__(kPrepThreads)
-    cnp_prep_kernel(Side s0, Side s1) {
+    cnp_prep_kernel(Side s0, Side s1, int what) {
   __shared__ __nv_bfloat16 tile[kPrepRows * (B + 2)];
   constexpr int LD = B + 2;
   constexpr int P = B * (B - 1) / 2;
@@ -300,7 +303,7 @@ __global__ void __launch_bounds__(kPrepThreads)
   const int c0 = blockIdx.x * kPrepRows;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // ---- dQ: rows [c0, c0 + 32), columns of quarter z -> bf16
-  {
+  if (what & kPrepG) {
     constexpr int QC = B / kPrepZ;   // columns of the quarter
     const float4* g4 = reinterpret_cast<const float4*>(sd.dQ + ((size_t)j * B + c0) * B);
     const size_t slot4 = (size_t)sd.nb * B * B / 4;
@@ -328,7 +331,7 @@ __global__ void __launch_bounds__(kPrepThreads)
                           pack_bf16x2(c.z, c.w));
     }
   }
-  if (blockIdx.z != 0) return;
+  if (blockIdx.z != 0 || !(what & kPrepK)) return;
   // ---- K and K^T rows of the group
   const float* th = sd.theta + (size_t)j * P;
   constexpr int W = kPrepThreads / 32;
@@ -797,7 +800,6 @@ __global__ void __launch_bounds__(kRingThreads, 1)
     const int quarter = warp % 4;
     const int half = (warp - 2) / 4;
     const int r = quarter * 32 + lane;
-    const int row = r0 + r;
     for (int u = wt; u < i_bytes / 16; u += kRingWorkers)
       reinterpret_cast<uint4*>(itl)[u] = make_uint4(0u, 0u, 0u, 0u);
     asm volatile("bar.sync 1, %0;" ::"n"(kRingWorkers) : "memory");
@@ -1010,16 +1012,17 @@ poetx_status cnp_bwd_ring_launch(const Side& s0, const Side& s1, int n, cudaStre
 // narrow: the two-CTA ring form (beside a kernel that holds most SMs), else
 // the cluster form (b/128 * b/64 CTAs per block).
 template <int B>
-poetx_status cnp_bwd_launch(const Side& s0, const Side& s1, int n, cudaStream_t s, int parts = 3,
+poetx_status cnp_bwd_launch(const Side& s0, const Side& s1, int n, cudaStream_t s, int parts = 7,
                             bool narrow = false) {
   const int nb = s0.nb + s1.nb;
-  if (parts & 1) {
+  if (parts & (kPrepK | kPrepG)) {
     {
       KernelScope ks_("tc_cnp_bwd_prep", s);
-      cnp_prep_kernel<B><<<dim3(B / kPrepRows, nb, kPrepZ), kPrepThreads, 0, s>>>(s0, s1);
+      const int z = (parts & kPrepG) ? kPrepZ : 1;   // K alone: one CTA per row group
+      cnp_prep_kernel<B><<<dim3(B / kPrepRows, nb, z), kPrepThreads, 0, s>>>(s0, s1, parts & (kPrepK | kPrepG));
     }
     const poetx_status st = check_launch();
-    if (st != POETX_OK || !(parts & 2)) return st;
+    if (st != POETX_OK || !(parts & kChain)) return st;
   }
   if (narrow) return cnp_bwd_ring_launch<B>(s0, s1, n, s);
   CUtensorMap tk0, tg0, tk1, tg1;
@@ -1061,7 +1064,7 @@ poetx_status cnp_bwd_sides(const Side& s0, const Side& s1, int n, cudaStream_t s
   return cnp_bwd_launch<B>(s0, s1, n, s);
 }
 
-poetx_status cnp_bwd_one(const Side& sd, int b, int n, cudaStream_t s, int parts = 3,
+poetx_status cnp_bwd_one(const Side& sd, int b, int n, cudaStream_t s, int parts = 7,
                          bool narrow = false) {
   Side none = sd;
   none.nb = 0;
@@ -1091,7 +1094,7 @@ Side carve(const float* theta, const float* dQ, int n_part, float* dtheta, int n
 
 poetx_status cnp_bwd_side(const float* theta, const float* dQ, int splits, int nb, int b, int n,
                           float* dtheta, void* ws, cudaStream_t s, int parts, bool narrow) {
-  if (!cnp_supported(b) || n < 1 || nb > 65535 || splits < 1 || parts < 1 || parts > 3)
+  if (!cnp_supported(b) || n < 1 || nb > 65535 || splits < 1 || parts < 1 || parts > 7)
     return POETX_ERR_UNSUPPORTED;
   if (nb <= 0) return POETX_OK;
   uint8_t* w = static_cast<uint8_t*>(ws);

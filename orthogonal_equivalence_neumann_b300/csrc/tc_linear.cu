@@ -295,13 +295,13 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
     if (st == POETX_OK) st = fork();
     if (st == POETX_OK)
       st = tc::cnp_bwd_side(cnp->theta_R, dqr, slots_r, nb_out, b_out, cnp->n, cnp->dtheta_R,
-                            cnp_ws_r, side->stream, 3, true);
+                            cnp_ws_r, side->stream, 7, true);
     if (st == POETX_OK) st = tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s, ctas_r);
     if (st == POETX_OK) st = p_dq(s);
     if (st == POETX_OK) st = fork();
     if (st == POETX_OK)
       st = tc::cnp_bwd_side(cnp->theta_P, dqp, slots_p, nb_in, b_in, cnp->n, cnp->dtheta_P, cnp_ws,
-                            side->stream, 3, true);
+                            side->stream, 7, true);
     if (st == POETX_OK && cudaEventRecord(side->join, side->stream) != cudaSuccess) st = check_launch();
     if (st == POETX_OK) st = p_apply(s);
     if (cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess && st == POETX_OK) st = check_launch();
@@ -309,7 +309,7 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
   }
   // Schedule (main = `s`, side = the library stream):
   //   main: g_z apply      | g_u GEMM (leaves the chain's SMs) | dX apply
-  //   side: dQ_R, R prep + chain                               | dQ_P, P prep + chain
+  //   side: dQ_R, R prep + chain, P's K                        | dQ_P, P's G + chain
   // The side stream's dQ sums take the clusters the concurrent apply leaves;
   // their partial slots are as many as their clusters.  On the P side the dQ
   // sums take the larger half: the P chain waits for them, not for dX, so
@@ -329,7 +329,12 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
             side->stream, side_r);
   if (st == POETX_OK)
     st = tc::cnp_bwd_side(cnp->theta_R, dqr, used_r, nb_out, b_out, cnp->n, cnp->dtheta_R, cnp_ws_r,
-                          side->stream, 3, true);
+                          side->stream, 7, true);
+  // the P side's dense K and K^T need only theta: made here, beside the GEMM,
+  // so that after the dQ_P sums only their sum and the chain remain
+  if (st == POETX_OK)
+    st = tc::cnp_bwd_side(cnp->theta_P, dqp, used_p, nb_in, b_in, cnp->n, cnp->dtheta_P, cnp_ws,
+                          side->stream, 1);
   if (st == POETX_OK)
     st = block_apply(dy, gz, Q_R, T, d_out, b_out, perm_out, inv_out, nullptr, true, ws, s, main_r);
   if (st == POETX_OK) st = tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s, ctas_r);
@@ -339,7 +344,7 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
             side->stream, side_p);
   if (st == POETX_OK)
     st = tc::cnp_bwd_side(cnp->theta_P, dqp, used_p, nb_in, b_in, cnp->n, cnp->dtheta_P, cnp_ws,
-                          side->stream);
+                          side->stream, 2 | 4);
   if (st == POETX_OK && cudaEventRecord(side->join, side->stream) != cudaSuccess) st = check_launch();
   if (st == POETX_OK)
     st = block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, inv_in, perm_in, true, ws, s, main_p);
