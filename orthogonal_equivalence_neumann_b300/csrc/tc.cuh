@@ -49,7 +49,8 @@ namespace tc {
 // C[M,N] (bf16) = A[M,K] . B^T with A [M,K] and B [N,K] (b_mn == false) or
 // B [K,N] (b_mn == true), all bf16 row-major, fp32 accumulation (tcgen05).
 bool gemm_supported(int N, int K);
-// reserve_sms: SMs to leave to kernels on another stream.
+// reserve_sms: SMs to leave to kernels on another stream (where that adds no
+// round of output tiles).
 poetx_status gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, bool b_mn,
                        cudaStream_t s, int reserve_sms = 0);
 

@@ -237,11 +237,15 @@ poetx_status gemm_bf16(const void* A, const void* B, void* C, int M, int N, int 
                           BK, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!okb) return POETX_ERR_CUDA;
   // as few pairs as give the fewest rounds of tiles (the SMs left over stay
-  // free for work on another stream), never more than the SMs not reserved
+  // free for work on another stream); the reserved SMs stay out of the grid
+  // unless leaving them out would add a round
   const int tiles = ((M + BM - 1) / BM) * (N / BN);
+  const int all_pairs = device_sm_count() / 2 > 0 ? device_sm_count() / 2 : 1;
+  const int min_rounds = (tiles + all_pairs - 1) / all_pairs;
   int avail = (device_sm_count() - (reserve_sms > 0 ? reserve_sms : 0)) / 2;
   if (avail < 1) avail = 1;
-  const int rounds = (tiles + avail - 1) / avail;
+  int rounds = (tiles + avail - 1) / avail;
+  if (rounds > min_rounds) rounds = min_rounds;
   const int pairs = (tiles + rounds - 1) / rounds;
   if (set_max_dynamic_smem((const void*)gemm_bf16_pair_kernel, SMEM_BYTES) != cudaSuccess)
     return check_launch();
