@@ -282,51 +282,40 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
       return check_launch();
     return POETX_OK;
   };
-  if (cl_r < 2 || cl_p < 2 || !dq_r || !dq_p) {
-    // A side outside the cluster form: the applies and the dQ sums in order on
-    // `s`, each side's Cayley-Neumann backward on the library stream as soon
-    // as its dQ sums are done, beside the GEMM (which leaves the chain's SMs
-    // free) for the R side and beside the dX apply for the P side:
-    //   main: g_z apply, dQ_R | g_u GEMM | dQ_P | dX apply | join
-    //   side:                 | R prep + chain   | P prep + chain
-    // (both chains in their narrow form: the GEMM and the dX apply beside
-    // them leave few SMs free)
-    poetx_status st = r_side(s);
-    if (st == POETX_OK) st = fork();
-    if (st == POETX_OK)
-      st = tc::cnp_bwd_side(cnp->theta_R, dqr, slots_r, nb_out, b_out, cnp->n, cnp->dtheta_R,
-                            cnp_ws_r, side->stream, 7, true);
-    if (st == POETX_OK) st = tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s, ctas_r);
-    if (st == POETX_OK) st = p_dq(s);
-    if (st == POETX_OK) st = fork();
-    if (st == POETX_OK)
-      st = tc::cnp_bwd_side(cnp->theta_P, dqp, slots_p, nb_in, b_in, cnp->n, cnp->dtheta_P, cnp_ws,
-                            side->stream, 7, true);
-    if (st == POETX_OK && cudaEventRecord(side->join, side->stream) != cudaSuccess) st = check_launch();
-    if (st == POETX_OK) st = p_apply(s);
-    if (cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess && st == POETX_OK) st = check_launch();
-    return st;
-  }
   // Schedule (main = `s`, side = the library stream):
-  //   main: g_z apply      | g_u GEMM (leaves the chain's SMs) | dX apply
-  //   side: dQ_R, R prep + chain, P's K                        | dQ_P, P's G + chain
-  // The side stream's dQ sums take the clusters the concurrent apply leaves;
-  // their partial slots are as many as their clusters.  On the P side the dQ
-  // sums take the larger half: the P chain waits for them, not for dX, so
-  // finishing them first lets the chain run beside the end of the dX apply
-  // (measured at the square 2048 layer: 15 clusters as 7 + 8 gave 0.379 ms
-  // per step, 8 + 7 0.384, 6 + 9 0.380).  The R chain runs in its narrow form
-  // (two CTAs per block: the GEMM beside it leaves 20 SMs free, where the
-  // cluster form's 8 CTAs per block would need four waves and delay dQ_P); the
-  // P chain, beside the dX apply, in the cluster form.
-  const int main_r = (cl_r + 1) / 2, main_p = cl_p / 2;
-  const int side_r = cl_r - main_r, side_p = cl_p - main_p;
-  const int used_r = tc::cluster_dq_splits(T, d_out, b_out) < side_r ? tc::cluster_dq_splits(T, d_out, b_out) : side_r;
-  const int used_p = tc::cluster_dq_splits(T, d_in, b_in) < side_p ? tc::cluster_dq_splits(T, d_in, b_in) : side_p;
-  poetx_status st = fork();
+  //   main: g_z apply                | g_u GEMM (leaves the chain's SMs) | dX apply
+  //   side: dQ_R, R prep + chain, P's K                                 | dQ_P, P's G + chain
+  // A side whose apply and dQ sums both take the cluster form runs them side
+  // by side on a split of the exchange clusters; their partial slots are as
+  // many as the dQ kernel's clusters.  On the P side the dQ sums take the
+  // larger half: the P chain waits for them, not for dX, so finishing them
+  // first lets the chain run beside the end of the dX apply (measured at the
+  // square 2048 layer: 15 clusters as 7 + 8 gave 0.379 ms per step, 8 + 7
+  // 0.384, 6 + 9 0.380).  A side without the cluster form (its blocks need
+  // more tensor memory than 8 CTAs hold) runs its apply and dQ sums as whole-
+  // GPU kernels on the two streams; when both read dy gathered by perm_out it
+  // is gathered once, before the fork.  The R chain runs in its narrow form
+  // (two CTAs per block: the GEMM beside it leaves few SMs free, where the
+  // cluster form's 8 CTAs per block would need several waves and delay dQ_P);
+  // the P chain in the cluster form where the dX apply beside it runs on
+  // half the clusters.
+  const bool split_r = cl_r >= 2 && dq_r, split_p = cl_p >= 2 && dq_p;
+  const int main_r = split_r ? (cl_r + 1) / 2 : 0, side_r = split_r ? cl_r - main_r : 0;
+  const int main_p = split_p ? cl_p / 2 : 0, side_p = split_p ? cl_p - main_p : 0;
+  auto used = [&](bool cl, int cap, int splits, int slots) {
+    if (!cl) return slots;
+    return cap > 0 && cap < splits ? cap : splits;
+  };
+  const int used_r = used(dq_r, side_r, dq_r ? tc::cluster_dq_splits(T, d_out, b_out) : 0, slots_r);
+  const int used_p = used(dq_p, side_p, dq_p ? tc::cluster_dq_splits(T, d_in, b_in) : 0, slots_p);
+  const bool share_dy = apply_staged(d_out, b_out, false) && !dq_r && dq_tc(T, d_out, b_out);
+  poetx_status st = POETX_OK;
+  if (share_dy) st = tc::permute_cols_bf16(dy, ws_dq, perm_out, T, d_out, s);   // dy[:, perm_out]
+  if (st == POETX_OK) st = fork();
   if (st == POETX_OK)
-    st = dq(dy, z, T, d_out, b_out, perm_out, inv_out, nullptr, nullptr, dqr, slots_r, ws_dq, dq_bytes,
-            side->stream, side_r);
+    st = share_dy ? tc::dq_bf16(ws_dq, z, T, d_out, b_out, slots_r, dqr, side->stream)
+                  : dq(dy, z, T, d_out, b_out, perm_out, inv_out, nullptr, nullptr, dqr, slots_r, ws_dq,
+                       dq_bytes, side->stream, side_r);
   if (st == POETX_OK)
     st = tc::cnp_bwd_side(cnp->theta_R, dqr, used_r, nb_out, b_out, cnp->n, cnp->dtheta_R, cnp_ws_r,
                           side->stream, 7, true);
@@ -336,7 +325,9 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
     st = tc::cnp_bwd_side(cnp->theta_P, dqp, used_p, nb_in, b_in, cnp->n, cnp->dtheta_P, cnp_ws,
                           side->stream, 1);
   if (st == POETX_OK)
-    st = block_apply(dy, gz, Q_R, T, d_out, b_out, perm_out, inv_out, nullptr, true, ws, s, main_r);
+    st = share_dy ? tc::plain_apply_bf16(ws_dq, gz, Q_R, T, d_out, b_out, true, s)
+                  : block_apply(dy, gz, Q_R, T, d_out, b_out, perm_out, inv_out, nullptr, true, ws, s,
+                                main_r);
   if (st == POETX_OK) st = tc::gemm_bf16(gz, W0m, gu, T, d_in, d_out, true, s, ctas_r);
   if (st == POETX_OK) st = fork();
   if (st == POETX_OK)
@@ -344,7 +335,7 @@ poetx_status tc_backward(const void* x, const void* dy, const void* W0m, const v
             side->stream, side_p);
   if (st == POETX_OK)
     st = tc::cnp_bwd_side(cnp->theta_P, dqp, used_p, nb_in, b_in, cnp->n, cnp->dtheta_P, cnp_ws,
-                          side->stream, 2 | 4);
+                          side->stream, 2 | 4, !split_p);
   if (st == POETX_OK && cudaEventRecord(side->join, side->stream) != cudaSuccess) st = check_launch();
   if (st == POETX_OK)
     st = block_apply(gu, dX, Q_P, T, d_in, b_in, nullptr, inv_in, perm_in, true, ws, s, main_p);
