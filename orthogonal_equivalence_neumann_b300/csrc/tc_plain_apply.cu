@@ -12,16 +12,18 @@
 // (the inverse permutation gathers the block outputs into place).
 //
 // One CTA per (block j, token stripe): it keeps Qop_j in tensor memory for
-// the whole launch (tc_qstage.cuh) and walks the 64-token tiles r, r + R,
+// the whole launch (tc_qstage.cuh) and walks the 128-token tiles r, r + R,
 // r + 2R, ... of its stripe r:
-//   warp 0      TMA: the tile's block columns [64 tokens x b] (128-byte swizzle,
-//               K-major: the MMA's B operand as loaded)
-//   warp 1      MMA (lane 0): M = 128 outputs (per half of the block), N = 64
-//               tokens, K = 16, A from TMEM, into one of two accumulators
-//   warps 2..    epilogue (kPaEpiWarps, two per TMEM lane quarter when 8: each
-//               drains half of the tile's tokens): TMEM -> bf16 token rows in a
-//               staging tile (the TMA store layout) -> TMA store; kPaNST
-//               staging tiles, so stores overlap the next tiles' drains
+//   warp 0      TMA: the tile's block columns [128 tokens x b] (128-byte
+//               swizzle, K-major: the MMA's B operand as loaded)
+//   warp 1      MMA (lane 0): M = 128 outputs per half of the block, N = 128
+//               tokens, K = 16, A from TMEM, each half into its own 128-column
+//               accumulator slot (b = 256: one slot per half, handed to the
+//               epilogue and back half by half; b = 128: two slots in turn)
+//   warps 2..9  epilogue, two warps per TMEM lane quarter (each drains 64 of
+//               the tile's tokens): TMEM -> bf16 token rows in the slot's
+//               staging tile (the TMA store layout) -> TMA store, so one half's
+//               store overlaps the next half's drain
 // Every wait is bounded (tc_ptx.cuh).
 #include "common.cuh"
 #include "profile.cuh"
@@ -38,50 +40,50 @@ namespace {
 constexpr int kPaEpiWarps = 8;
 constexpr int kPaEpiThreads = 32 * kPaEpiWarps;
 constexpr int kPaThreads = 64 + kPaEpiThreads;
-constexpr int kPaTT = 64;      // tokens per tile: two 32-column TMEM loads per output feature
-constexpr int kPaNA = 2;       // accumulator buffers
-constexpr int kPaNST = 2;      // output staging tiles
+constexpr int kPaTT = 128;             // tokens per tile: the MMA's N
+constexpr int kPaSlots = 2;            // 128-column accumulator slots = staging tiles
+constexpr int kPaStg = kPaTT * 128 * 2;   // one staging tile: 128 tokens x 128 features bf16
 constexpr int kPaMaxNS = 8;
 
 struct PaGeo {
   int NS;          // input stages
-  int s_bytes;     // one input tile (= one output staging tile): 64 tokens x b bf16
+  int s_bytes;     // one input tile: 128 tokens x b bf16
   int q_cols, tmem_cols;
   int smem;
 };
 
-// Shared memory: 1 KB of barriers, NS input stages, kPaNST staging tiles.  Q is
+// Shared memory: 1 KB of barriers, NS input stages, two staging tiles.  Q is
 // staged in the stages and staging tiles (contiguous) before the first tile
-// loads, which needs (NS + kPaNST) * s_bytes >= b * b * 2.
+// loads, which needs NS * s_bytes + 2 * kPaStg >= b * b * 2.
 bool pa_geometry(int b, PaGeo* g) {
   if (b != 128 && b != 256) return false;
   g->s_bytes = kPaTT * b * 2;
   g->NS = 0;
   for (int ns = kPaMaxNS; ns >= 2; --ns)
-    if (1024 + 1024 + (ns + kPaNST) * g->s_bytes <= 232448 &&
-        (ns + kPaNST) * g->s_bytes >= b * b * 2) {
+    if (1024 + 1024 + ns * g->s_bytes + kPaSlots * kPaStg <= 232448 &&
+        ns * g->s_bytes + kPaSlots * kPaStg >= b * b * 2) {
       g->NS = ns;
       break;
     }
   if (g->NS == 0) return false;
-  const int halves = b / 128;
-  g->q_cols = halves * (b / 2);
-  const int used = g->q_cols + kPaNA * halves * kPaTT;
+  g->q_cols = (b / 128) * (b / 2);
+  const int used = g->q_cols + kPaSlots * kPaTT;
   g->tmem_cols = 32;
   while (g->tmem_cols < used) g->tmem_cols *= 2;
-  g->smem = 1024 + 1024 + (g->NS + kPaNST) * g->s_bytes;
+  g->smem = 1024 + 1024 + g->NS * g->s_bytes + kPaSlots * kPaStg;
   return g->tmem_cols <= 512;
-}
-
-// the bulk store groups of this thread: at most N still reading shared memory
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void pa_epi_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(kPaEpiThreads) : "memory");
 }
+
+// Accumulator slot (= staging tile) of half h of the it-th tile, and how many
+// times the slot was used before.
+template <int B>
+__device__ __forceinline__ int pa_slot(int it, int h) { return B == 256 ? h : (it & 1); }
+template <int B>
+__device__ __forceinline__ int pa_use(int it) { return B == 256 ? it : (it >> 1); }
 
 template <int B>
 __global__ void __launch_bounds__(kPaThreads, 1)
@@ -95,9 +97,9 @@ __global__ void __launch_bounds__(kPaThreads, 1)
   constexpr int TT = kPaTT;
   uint64_t* s_full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* s_empty = s_full + kPaMaxNS;
-  uint64_t* a_full = s_empty + kPaMaxNS;
-  uint64_t* a_empty = a_full + kPaNA;
-  uint64_t* q_full = a_empty + kPaNA;
+  uint64_t* a_full = s_empty + kPaMaxNS;    // per accumulator slot
+  uint64_t* a_empty = a_full + kPaSlots;
+  uint64_t* q_full = a_empty + kPaSlots;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 1);
   uint8_t* sbuf = smem + 1024;
   uint8_t* obuf = sbuf + g.NS * g.s_bytes;
@@ -113,7 +115,7 @@ __global__ void __launch_bounds__(kPaThreads, 1)
       mbar_init(s_full + i, 1);
       mbar_init(s_empty + i, 1);
     }
-    for (int i = 0; i < kPaNA; ++i) {
+    for (int i = 0; i < kPaSlots; ++i) {
       mbar_init(a_full + i, 1);
       mbar_init(a_empty + i, kPaEpiThreads);
     }
@@ -133,9 +135,8 @@ __global__ void __launch_bounds__(kPaThreads, 1)
   }
   tc_fence_before();
   fence_proxy_async_smem();   // the staging reads are done before TMA overwrites the stages
-  __syncthreads();
-  tc_fence_after();
   ok = __syncthreads_and(ok ? 1 : 0) != 0;
+  tc_fence_after();
 
   const uint32_t acc0 = tmem_base + (uint32_t)g.q_cols;
   if (warp == 0) {
@@ -155,74 +156,74 @@ __global__ void __launch_bounds__(kPaThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(128, TT, false, false);
       for (int it = 0, tile = stripe; tile < n_tiles && ok; tile += stripes, ++it) {
-        const int s = it % g.NS, a = it % kPaNA;
+        const int s = it % g.NS;
         if (!(ok = mbar_wait(s_full + s, (it / g.NS) & 1, err))) break;
-        if (!(ok = mbar_wait(a_empty + a, ((it / kPaNA) & 1) ^ 1, err))) break;
-        tc_fence_after();
         const uint32_t sb = smem_u32(sbuf + s * g.s_bytes);
-        for (int h = 0; h < halves; ++h) {
-          const uint32_t d_tmem = acc0 + (uint32_t)((a * halves + h) * TT);
+        for (int h = 0; h < halves && ok; ++h) {
+          const int slot = pa_slot<B>(it, h);
+          if (!(ok = mbar_wait(a_empty + slot, (pa_use<B>(it) & 1) ^ 1, err))) break;
+          tc_fence_after();
+          const uint32_t d_tmem = acc0 + (uint32_t)(slot * TT);
           const uint32_t a_tmem = tmem_base + (uint32_t)(h * (B / 2));
 #pragma unroll 4
           for (int kk = 0; kk < B / 16; ++kk) {
             const uint64_t bdesc = sw128_desc(sb + (kk >> 2) * (TT * 128) + (kk & 3) * 32, 16, 1024);
             mma_bf16_ts(d_tmem, a_tmem + (uint32_t)(kk * 8), bdesc, idesc, kk != 0);
           }
+          mma_commit(a_full + slot);
         }
         mma_commit(s_empty + s);
-        mma_commit(a_full + a);
       }
     }
   } else {
     // ---------------------------------------------------------------- epilogue
     // TMEM lanes are output features, columns tokens: each thread writes its
-    // feature's 64 tokens into a token-row staging tile (128-byte swizzle, the
-    // TMA store layout); one thread then stores the tile with TMA.
+    // feature's 64 tokens into the slot's token-row staging tile (128-byte
+    // swizzle, the TMA store layout); one thread then stores it with TMA.
     const int quarter = warp % 4;
-    const int et = threadIdx.x - 64;                        // 0 .. kPaEpiThreads - 1
-    constexpr int kParts = kPaEpiWarps / 4;                 // token parts of a tile
-    constexpr int kPartTT = TT / kParts;
-    const int part = (warp - 2) / 4;
-    bool pending = false;
+    const int et = threadIdx.x - 64;   // 0 .. kPaEpiThreads - 1
+    const int part = (warp - 2) / 4;   // tokens [64 part, +64) of the tile
+    const int f = quarter * 32 + lane; // output feature within the half
+    bool any = false;
     for (int it = 0, tile = stripe; tile < n_tiles && ok; tile += stripes, ++it) {
-      const int a = it % kPaNA;
-      uint8_t* ostg = obuf + (it % kPaNST) * g.s_bytes;
-      if (!(ok = mbar_wait(a_full + a, (it / kPaNA) & 1, err))) break;
-      tc_fence_after();
-      if (pending && it >= kPaNST) {   // the store that last used this staging tile has read it
-        if (et == 0) bulk_wait_read<kPaNST - 1>();
-        pa_epi_bar();
-      }
       for (int h = 0; h < halves; ++h) {
-        const int f = h * 128 + quarter * 32 + lane;   // output feature within the block
+        const int slot = pa_slot<B>(it, h), use = pa_use<B>(it);
+        uint8_t* ostg = obuf + slot * kPaStg;
+        if (!(ok = mbar_wait(a_full + slot, use & 1, err))) break;
+        tc_fence_after();
+        if (use > 0) {   // the store that last used this staging tile has read it
+          if (et == 0)
+            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+          pa_epi_bar();
+        }
         uint8_t* col = ostg + (f >> 6) * (TT * 128) + (f & 7) * 2;
         const uint32_t fu = (uint32_t)((f & 63) >> 3);
-        const uint32_t tacc = acc0 + (uint32_t)((a * halves + h) * TT + part * kPartTT) +
-                              ((uint32_t)(quarter * 32) << 16);
-        uint32_t rr[kPartTT / 32][32];
-#pragma unroll
-        for (int q = 0; q < kPartTT / 32; ++q) tmem_ld32(tacc + 32u * q, rr[q]);
+        const uint32_t tacc = acc0 + (uint32_t)(slot * TT + part * 64) + ((uint32_t)(quarter * 32) << 16);
+        uint32_t rr[2][32];
+        tmem_ld32(tacc, rr[0]);
+        tmem_ld32(tacc + 32u, rr[1]);
         tmem_ld_wait();
+        tmem_regs_ready(rr[0]);
+        tmem_regs_ready(rr[1]);
 #pragma unroll
-        for (int q = 0; q < kPartTT / 32; ++q) tmem_regs_ready(rr[q]);
-#pragma unroll
-        for (int e = 0; e < kPartTT; ++e) {
-          const int tr = part * kPartTT + e;
+        for (int e = 0; e < 64; ++e) {
+          const int tr = part * 64 + e;
           *reinterpret_cast<__nv_bfloat16*>(col + tr * 128 + ((fu ^ (uint32_t)(tr & 7)) << 4)) =
               __float2bfloat16_rn(__uint_as_float(rr[e >> 5][e & 31]));
         }
+        tc_fence_before();
+        mbar_arrive(a_empty + slot);   // the slot may be refilled
+        fence_proxy_async_smem();
+        pa_epi_bar();
+        if (et == 0) {
+          for (int q = 0; q < 2; ++q)
+            tma_store_2d(&tmOut, ostg + q * (TT * 128), j * B + h * 128 + q * 64, tile * TT);
+          bulk_commit();
+        }
+        any = true;
       }
-      tc_fence_before();
-      mbar_arrive(a_empty + a);   // the accumulators may be refilled
-      fence_proxy_async_smem();
-      pa_epi_bar();
-      if (et == 0) {
-        for (int q = 0; q < B / 64; ++q) tma_store_2d(&tmOut, ostg + q * (TT * 128), j * B + q * 64, tile * TT);
-        bulk_commit();
-      }
-      pending = true;
     }
-    if (et == 0 && pending) bulk_wait0();
+    if (et == 0 && any) bulk_wait0();
   }
   tc_fence_before();
   __syncthreads();
