@@ -399,7 +399,6 @@ __global__ void __launch_bounds__(kCaThreads, 1)
     // 128-byte row (8 x 16 bytes in the row's swizzle order), written into the
     // exchange part of the CTA owning the feature's scattered column.
     const int quarter = warp % 4;
-    const int et = threadIdx.x - 320;
     for (int it = 0, tile = cluster_id; tile < n_tiles && ok; tile += n_clusters, ++it) {
       const int x = it % g.NX, a = it % g.NA;
       if (!(ok = mbar_wait(br.a_full + a, (it / g.NA) & 1, err))) break;

@@ -409,7 +409,8 @@ struct BwdGeo {
   static constexpr int a_bytes = 128 * B * 2;   // one A operand: 128 rows x B
   static constexpr int b_bytes = B * 128;       // one B operand: B rows x 64 columns
   static constexpr int i_bytes = 64 * 128;      // the 2I tile
-  static constexpr int half_bytes = 128 * 128;  // a row half of a B operand
+  static constexpr int half_bytes = 128 * 128;  // a row half of a B operand (MH = 2)
+  static_assert(MH == 1 || half_bytes * MH == b_bytes, "the row halves tile a B operand");
   static constexpr int off_a1 = 1024;
   static constexpr int off_a2 = off_a1 + a_bytes;
   static constexpr int off_bx = off_a2 + a_bytes;
