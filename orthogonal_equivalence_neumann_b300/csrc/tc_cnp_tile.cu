@@ -39,10 +39,13 @@
 // each), so one's unpack and conversions overlap the other's products.  One
 // thread polls each barrier and the CTA follows through a CTA barrier; every
 // wait is bounded (tc_ptx.cuh).
+#include <cstring>
+
 #include "common.cuh"
 #include "profile.cuh"
 #include "tc.cuh"
 #include "tc_ptx.cuh"
+#include "tmap.cuh"
 
 namespace poetx {
 namespace tc {
@@ -92,9 +95,8 @@ template <int B, bool F32>
 struct TileGeo {
   static constexpr int G = 128 / B;
   static constexpr int P = B * (B - 1) / 2;
-  static constexpr int NB32 = B / 32;                      // 32-wide strips of a block
-  static constexpr int NOFF = NB32 * (NB32 - 1) / 2;       // pieces above a block's diagonal
-  static constexpr int NSUB = G * (NOFF + NB32);           // 32 x 32 pieces unpacked per tile
+  static constexpr int NU = B * (B + 32) / 512;            // 8 x 32 unpack units of a block
+  static constexpr int NUNITS = G * NU;                    // ... of a tile (b = 128: 40)
   static constexpr int n_s = F32 ? 2 : 1;                  // S hi [lo]
   static constexpr int th_bytes = ((G * P * 4 + 127) / 128) * 128;
   static constexpr int used = 1024 + n_s * kOpBytes + th_bytes + 64;
@@ -104,98 +106,105 @@ struct TileGeo {
   static constexpr int smem = used > 78848 ? used : 78848;
   static constexpr int per_sm = 2;
   static constexpr int tmem_cols = 256;                    // accumulator 128, X hi 64 [, X lo 64]
+  // bf16 Q of b >= 64 leaves through shared memory (S, free after the last
+  // product) and tensor stores: 128-byte rows, as the operand layout
+  static constexpr bool staged_out = !F32 && B >= 64;
 };
 
-// Unpack piece `sb` of a tile into S = -K (K-major, 128-byte swizzle) from the
-// tile's parameters in shared memory.  Pieces are 32 x 32 parts of a block on
-// or above its diagonal, those strictly above first.  Lane l owns column
-// j = 32 J + l of the piece (I, J): it reads theta(i, j), i = 32 I .. 32 I + 31
-// (a row's parameters are consecutive, so the 32 lanes read one contiguous
-// run: no bank conflicts), writes row j of S across the piece's columns
-// (S[j][i] = K[i][j] = theta(i, j): four 16-byte stores) and then the column's
-// own entries S[i][j] = -theta(i, j) one by one.  In a piece on the diagonal
-// the row stores put zeros right of the diagonal and the column stores,
-// ordered after them, fill those.  A block the tile does not hold (last
-// tile) is written as zeros.
+// -x for each bf16 of a pair that is not zero (zeros keep their +0 pattern).
+__device__ __forceinline__ uint32_t neg_nonzero(uint32_t h) {
+  return h ^ (((h & 0x7fff7fffu) + 0x7fff7fffu) & 0x80008000u);
+}
+
+// Unpack unit `u` of a tile into S = -K (K-major, 128-byte swizzle) from the
+// tile's parameters in shared memory.  A unit is 8 rows x 32 columns of a
+// block, rows [8 I, 8 I + 8), columns [32 J, 32 J + 32), holding at least one
+// entry above the diagonal (8 I < 32 J + 32): 2 J (J + 1) units of strip J
+// come before strip J + 1, so a block of b has b (b + 32) / 512 of them
+// (b = 128: 40, five per warp).  The warp holds the unit as four 8 x 8
+// fragments M_q = theta(8 I + r, 32 J + 8 q + c) (zero on and below the
+// diagonal) and writes each twice with stmatrix: S over rows 8 I.., columns
+// 32 J + 8 q.. is -M_q, S over rows 32 J + 8 q.., columns 8 I.. is M_q^T.
+// The fragment on the diagonal (8 q = 8 I - 32 J) holds both halves of one
+// 8 x 8 part of S, -M + M^T, built in registers and written once; fragments
+// left of it lie below the diagonal (other units' transposed writes cover
+// those parts).  So every 8 x 8 part of a block is written exactly once per
+// tile; a block the tile does not hold (last tile) is written as zeros.
 template <int B, bool F32>
-__device__ __forceinline__ void unpack_sub(int sb, const float* th_tile, int nbt, uint8_t* s_hi,
-                                          uint8_t* s_lo, int lane) {
+__device__ __forceinline__ void unpack_unit(int u, const float* th_tile, int nbt, uint32_t s_hi,
+                                           uint32_t s_lo, int lane) {
   using Geo = TileGeo<B, F32>;
-  constexpr int NB32 = Geo::NB32, NOFF = Geo::NOFF, G = Geo::G;
-  int gb, I, J;
-  if (NOFF > 0 && sb < G * NOFF) {
-    constexpr int NO = NOFF > 0 ? NOFF : 1;
-    gb = sb / NO;
-    int q = sb % NO;
-    I = 0;
-    while (q >= NB32 - 1 - I) {
-      q -= NB32 - 1 - I;
-      ++I;
-    }
-    J = I + 1 + q;
-  } else {
-    const int d = sb - G * NOFF;
-    gb = d / NB32;
-    I = J = d % NB32;
-  }
+  const int gb = u / Geo::NU;
+  const int w = u % Geo::NU;
+  int J = 0;
+  while (2 * (J + 1) * (J + 2) <= w) ++J;
+  const int I = w - 2 * J * (J + 1);
   const bool live = gb < nbt;
-  const int aI = 32 * I, jj = 32 * J + lane;   // first row of the piece, this lane's column
-  const float* th = th_tile + (live ? gb : 0) * Geo::P;
-  // theta(i, j) sits at skew_row_off(i) + j - i - 1; step the row offset
-  // along i: skew_row_off(i + 1) - skew_row_off(i) = B - i - 1
-  int idx = skew_row_off(aI, B) + jj - aI - 1;
-  uint32_t h[16], l[16];   // theta(aI + r, j) as bf16 pairs (r even in the low half) [hi, lo]
+  const int a = 8 * I;                    // first row of the unit (block-relative)
+  const int qd = (a - 32 * J) >> 3;       // the fragment on the diagonal (< 0: none)
+  // this lane's fragment entries: row a + lane / 4, columns 32 J + 8 q + cp + {0, 1};
+  // theta(i, j) sits at skew_row_off(i) + j - i - 1
+  const int i = a + (lane >> 2), cp = 2 * (lane & 3);
+  const float* th = th_tile + (live ? gb : 0) * Geo::P + (skew_row_off(i, B) - i - 1 + 32 * J + cp);
+  uint32_t h[4], l[4];   // M_q as bf16 pairs [hi, lo]
 #pragma unroll
-  for (int r = 0; r < 32; r += 2) {
+  for (int q = 0; q < 4; ++q) {
     float v[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const bool in = aI + r + e < jj;
-      const float t = th[in ? idx : 0];
-      v[e] = (live && in) ? t : 0.f;
-      idx += B - aI - (r + e) - 2;
+      const bool in = live && q >= qd && (q > qd || i < 32 * J + 8 * q + cp + e);
+      v[e] = in ? th[8 * q + e] : 0.f;
     }
     if constexpr (F32) {
       uint32_t h0, l0, h1, l1;
       split_bf16(v[0], h0, l0);
       split_bf16(v[1], h1, l1);
-      h[r / 2] = h0 | (h1 << 16);
-      l[r / 2] = l0 | (l1 << 16);
+      h[q] = h0 | (h1 << 16);
+      l[q] = l0 | (l1 << 16);
     } else {
-      h[r / 2] = pack_bf16x2(v[0], v[1]);
+      h[q] = pack_bf16x2(v[0], v[1]);
     }
   }
-  const int R = gb * B + jj;        // this lane's row of the tile (the row stores)
-  const int C0 = gb * B + aI;       // first tile column of the piece
+  const int t8 = lane & 7, m = lane >> 3;   // the row this lane addresses, of fragment m
+  const int base = gb * B;
+  if (qd < 0) {
+    // every fragment above the diagonal
+    const uint32_t dir = op_off(base + a + t8, base + 32 * J + 8 * m);
+    const uint32_t tr = op_off(base + 32 * J + 8 * m + t8, base + a);
+    stmatrix_x4(s_hi + dir, neg_nonzero(h[0]), neg_nonzero(h[1]), neg_nonzero(h[2]),
+                neg_nonzero(h[3]));
+    stmatrix_x4_trans(s_hi + tr, h[0], h[1], h[2], h[3]);
+    if constexpr (F32) {
+      stmatrix_x4(s_lo + dir, neg_nonzero(l[0]), neg_nonzero(l[1]), neg_nonzero(l[2]),
+                  neg_nonzero(l[3]));
+      stmatrix_x4_trans(s_lo + tr, l[0], l[1], l[2], l[3]);
+    }
+  } else {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint32_t off = op_off(R, C0 + 8 * q);
-    *reinterpret_cast<uint4*>(s_hi + off) =
-        make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
-    if constexpr (F32)
-      *reinterpret_cast<uint4*>(s_lo + off) =
-          make_uint4(l[4 * q], l[4 * q + 1], l[4 * q + 2], l[4 * q + 3]);
-  }
-  __syncwarp();
-  // column stores: S[C0 + r][R] = -theta, the sign bit of each bf16 part
-  // flipped (both roundings are symmetric); rows C0 + r share their swizzle
-  // phase with r (C0 is a multiple of 32)
-  const uint32_t cbase = (uint32_t)((R >> 6) * (128 * 128) + (C0 >> 3) * 1024 + (R & 7) * 2);
-  const int cx = (R & 63) >> 3;
-#pragma unroll
-  for (int r = 0; r < 32; ++r) {
-    if (aI + r < jj) {
-      const uint32_t off = cbase + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((cx ^ (r & 7)) << 4));
-      *reinterpret_cast<uint16_t*>(s_hi + off) = (uint16_t)((h[r / 2] >> (16 * (r & 1))) ^ 0x8000u);
-      if constexpr (F32)
-        *reinterpret_cast<uint16_t*>(s_lo + off) = (uint16_t)((l[r / 2] >> (16 * (r & 1))) ^ 0x8000u);
+    for (int q = 0; q < 4; ++q) {
+      if (q < qd) continue;
+      const uint32_t dir = op_off(base + a + t8, base + 32 * J + 8 * q);
+      if (q == qd) {
+        // -M + M^T: where one is non-zero the other is zero
+        stmatrix_x1(s_hi + dir, movmatrix_trans(h[q]) | neg_nonzero(h[q]));
+        if constexpr (F32) stmatrix_x1(s_lo + dir, movmatrix_trans(l[q]) | neg_nonzero(l[q]));
+      } else {
+        const uint32_t tr = op_off(base + 32 * J + 8 * q + t8, base + a);
+        stmatrix_x1(s_hi + dir, neg_nonzero(h[q]));
+        stmatrix_x1_trans(s_hi + tr, h[q]);
+        if constexpr (F32) {
+          stmatrix_x1(s_lo + dir, neg_nonzero(l[q]));
+          stmatrix_x1_trans(s_lo + tr, l[q]);
+        }
+      }
     }
   }
 }
 
 template <int B, bool F32>
 __global__ void __launch_bounds__(kTileThreads, 2)
-    cnp_tile_kernel(TileSide s0, TileSide s1, int n, int* err) {
+    cnp_tile_kernel(TileSide s0, TileSide s1, const __grid_constant__ CUtensorMap tq0,
+                    const __grid_constant__ CUtensorMap tq1, int staged, int n, int* err) {
   using Geo = TileGeo<B, F32>;
   constexpr int G = Geo::G, P = Geo::P;
   extern __shared__ uint8_t smem_raw[];
@@ -229,16 +238,27 @@ __global__ void __launch_bounds__(kTileThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;                     // accumulator: columns [0, 128)
-  const uint32_t x_hi = tmem + 128, x_lo = tmem + 192;  // X_i (i >= 2): [hi, lo] bf16 pairs
+  const uint32_t x_hi = tmem + 128;                     // X_i (i >= 2): bf16 pairs [hi part]
+  const uint32_t x_lo = tmem + 192;                     // fp32 Q: X_i lo part
+  const uint32_t two_i = tmem + 192;                    // bf16 Q: 2I, the A of the 2K term
   const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
   {
-    // X starts at zero too (entries outside the blocks stay so): each thread
-    // clears its half of its row
+    // X starts at zero too (entries outside the blocks stay so); each thread
+    // writes its half of its row
     uint32_t z[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) z[e] = 0;
     tmem_st32(x_hi + lane_off + (uint32_t)(half * 32), z);
-    if constexpr (F32) tmem_st32(x_lo + lane_off + (uint32_t)(half * 32), z);
+    if constexpr (F32) {
+      tmem_st32(x_lo + lane_off + (uint32_t)(half * 32), z);
+    } else {
+      // 2I: 2.0 (bf16 0x4000) at column r of row r
+      uint32_t d2[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        d2[e] = half * 32 + e == r / 2 ? ((r & 1) ? 0x40000000u : 0x00004000u) : 0u;
+      tmem_st32(two_i + lane_off + (uint32_t)(half * 32), d2);
+    }
     tmem_st_wait();
   }
 
@@ -275,6 +295,8 @@ __global__ void __launch_bounds__(kTileThreads, 2)
     const bool live = g < nbt;   // rows of a missing block (last tile) stay zero
     bool lok = true;
     if (leader) {
+      // the last tile's output stores have read S before the unpack rewrites it
+      if (Geo::staged_out && staged) bulk_wait_read0();
       lok = mbar_poll(th_full, (uint32_t)landed & 1, err);
       if (lok) ++landed;
     }
@@ -285,8 +307,8 @@ __global__ void __launch_bounds__(kTileThreads, 2)
 
     // ---- unpack S = -K
 #pragma unroll 1
-    for (int sb = warp; sb < Geo::NSUB; sb += kTileThreads / 32)
-      unpack_sub<B, F32>(sb, th_buf, nbt, s_hi, s_lo, lane);
+    for (int u = warp; u < Geo::NUNITS; u += kTileThreads / 32)
+      unpack_unit<B, F32>(u, th_buf, nbt, smem_u32(s_hi), smem_u32(s_lo), lane);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -303,31 +325,43 @@ __global__ void __launch_bounds__(kTileThreads, 2)
       if (leader) {
         tc_fence_after();
         const uint32_t sh = smem_u32(s_hi), sl = smem_u32(s_lo);
+        // block-diagonal products: block gq's output columns (N = B) from
+        // its own K range only (the rest of X's rows there are zero)
+        const uint32_t id_kk = idesc_bf16(128, B, false, false);
+        const uint32_t id_mk = idesc_bf16(128, B, true, false);
+        // descriptors of S at an offset: the start-address field of the base
+        // descriptor plus offset / 16 (shared addresses stay below 2^18, so
+        // the 14-bit field never carries)
+        const uint64_t dk_h = sw128_desc(sh, 16, 1024), dk_l = sw128_desc(sl, 16, 1024);
+        const uint64_t dm_h = sw128_desc(sh, 128 * 128, 1024), dm_l = sw128_desc(sl, 128 * 128, 1024);
 #pragma unroll
-        for (int kq = 0; kq < 8; ++kq) {   // K = 16 steps
-          const uint32_t o = (kq >> 2) * (128 * 128) + (kq & 3) * 32;
-          if (i == 1) {
-            // A = K = S^T: S read MN-major (its rows are the K index)
-            const uint32_t idesc = idesc_bf16(128, 128, true, false);
-            const uint32_t oa = kq * (16 * 128);
-            mma_bf16(tmem, sw128_desc(sh + oa, 128 * 128, 1024), sw128_desc(sh + o, 16, 1024),
-                     idesc, kq != 0);
-            if constexpr (F32) {
-              mma_bf16(tmem, sw128_desc(sh + oa, 128 * 128, 1024), sw128_desc(sl + o, 16, 1024),
-                       idesc, 1);
-              mma_bf16(tmem, sw128_desc(sl + oa, 128 * 128, 1024), sw128_desc(sh + o, 16, 1024),
-                       idesc, 1);
+        for (int gq = 0; gq < G; ++gq)
+#pragma unroll
+          for (int kq = 0; kq < B / 16; ++kq) {   // K = 16 steps
+            const int k0 = gq * B + 16 * kq;
+            const uint32_t d = tmem + (uint32_t)(gq * B);
+            const uint32_t ob =
+                (uint32_t)((k0 >> 6) * (128 * 128) + gq * B * 128 + ((k0 & 63) >> 4) * 32);
+            const uint32_t acc0 = kq != 0;
+            if (i == 1) {
+              // A = K = S^T: S read MN-major (its rows are the K index)
+              const uint32_t oa = (uint32_t)(k0 * 128);
+              mma_bf16(d, dm_h + (oa >> 4), dk_h + (ob >> 4), id_mk, acc0);
+              if constexpr (F32) {
+                mma_bf16(d, dm_h + (oa >> 4), dk_l + (ob >> 4), id_mk, 1);
+                mma_bf16(d, dm_l + (oa >> 4), dk_h + (ob >> 4), id_mk, 1);
+              }
+            } else {
+              const uint32_t xa = (uint32_t)(k0 / 2);
+              mma_bf16_ts(d, x_hi + xa, dk_h + (ob >> 4), id_kk, acc0);
+              if constexpr (F32) {
+                mma_bf16_ts(d, x_hi + xa, dk_l + (ob >> 4), id_kk, 1);
+                mma_bf16_ts(d, x_lo + xa, dk_h + (ob >> 4), id_kk, 1);
+              }
             }
-          } else {
-            const uint32_t idesc = idesc_bf16(128, 128, false, false);
-            mma_bf16_ts(tmem, x_hi + (uint32_t)(kq * 8), sw128_desc(sh + o, 16, 1024), idesc,
-                        kq != 0);
-            if constexpr (F32) {
-              mma_bf16_ts(tmem, x_hi + (uint32_t)(kq * 8), sw128_desc(sl + o, 16, 1024), idesc, 1);
-              mma_bf16_ts(tmem, x_lo + (uint32_t)(kq * 8), sw128_desc(sh + o, 16, 1024), idesc, 1);
-            }
+            if constexpr (!F32)   // + 2I . K
+              mma_bf16_ts(d, two_i + (uint32_t)(k0 / 2), dk_h + (ob >> 4), id_kk, 1);
           }
-        }
         mma_commit(mma_done);
         lok = mbar_poll(mma_done, mma_count & 1, err);
       }
@@ -346,24 +380,30 @@ __global__ void __launch_bounds__(kTileThreads, 2)
         const uint32_t ta = tmem + (uint32_t)(g * B + c0) + lane_off;
         if constexpr (W == 32) tmem_ld32(ta, acc);
         else tmem_ld16(ta, acc);
-        // 2K from the operand's own K (S = -K): bf16, or hi + lo for fp32 Q
-        float k2[W];
+        float x[W];
+        if constexpr (F32) {
+          // 2K from the operand's own K (S = -K), hi + lo
+          float k2[W];
 #pragma unroll
-        for (int q = 0; q < W / 8; ++q) {
-          const uint32_t off = op_off(r, g * B + c0 + 8 * q);
-          widen8(s_hi + off, k2 + 8 * q);
-          if constexpr (F32) {
+          for (int q = 0; q < W / 8; ++q) {
+            const uint32_t off = op_off(r, g * B + c0 + 8 * q);
             float lo[8];
+            widen8(s_hi + off, k2 + 8 * q);
             widen8(s_lo + off, lo);
 #pragma unroll
             for (int e = 0; e < 8; ++e) k2[8 * q + e] += lo[e];
           }
-        }
-        tmem_ld_wait();
-        tmem_regs_ready(acc);
-        float x[W];
+          tmem_ld_wait();
+          tmem_regs_ready(acc);
 #pragma unroll
-        for (int e = 0; e < W; ++e) x[e] = __uint_as_float(acc[e]) - 2.f * k2[e];
+          for (int e = 0; e < W; ++e) x[e] = __uint_as_float(acc[e]) - 2.f * k2[e];
+        } else {
+          // the products already hold the 2K term
+          tmem_ld_wait();
+          tmem_regs_ready(acc);
+#pragma unroll
+          for (int e = 0; e < W; ++e) x[e] = __uint_as_float(acc[e]);
+        }
         if (i < n) {
           // X_{i+1} into tensor memory: row r, columns g*B + c0 .. (two per 32-bit column)
           uint32_t h[W / 2], l[W / 2];
@@ -388,16 +428,28 @@ __global__ void __launch_bounds__(kTileThreads, 2)
             if constexpr (F32) tmem_st8(x_lo + tx, l);
           }
         } else if (live) {
-          // Q = I + X_{n+1}: row ri of block b0 + g
+          // Q = I + X_{n+1}: row ri of block b0 + g (the diagonal lies in
+          // these columns for all or none of most warps' lanes)
+          if (__any_sync(0xffffffffu, (unsigned)(ri - c0) < (unsigned)W)) {
 #pragma unroll
-          for (int e = 0; e < W; ++e)
-            if (c0 + e == ri) x[e] += 1.f;
+            for (int e = 0; e < W; ++e)
+              if (c0 + e == ri) x[e] += 1.f;
+          }
           const size_t row = ((size_t)(b0 + g) * B + ri) * B + c0;
           if constexpr (F32) {
             float4* o = reinterpret_cast<float4*>(static_cast<float*>(sd->Q) + row);
 #pragma unroll
             for (int q = 0; q < W / 4; ++q)
               o[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+          } else if (Geo::staged_out && staged) {
+            // into S (free: the products are done and bf16 Q reads no K here)
+#pragma unroll
+            for (int q = 0; q < W / 8; ++q)
+              *reinterpret_cast<uint4*>(s_hi + op_off(r, g * B + c0 + 8 * q)) =
+                  make_uint4(pack_bf16x2(x[8 * q], x[8 * q + 1]),
+                             pack_bf16x2(x[8 * q + 2], x[8 * q + 3]),
+                             pack_bf16x2(x[8 * q + 4], x[8 * q + 5]),
+                             pack_bf16x2(x[8 * q + 6], x[8 * q + 7]));
           } else {
             uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(sd->Q) + row);
 #pragma unroll
@@ -410,11 +462,26 @@ __global__ void __launch_bounds__(kTileThreads, 2)
         }
       }
       if (i < n) tmem_st_wait();
+      else if (Geo::staged_out && staged) fence_proxy_async_smem();   // for the tensor stores
       tc_fence_before();
       __syncthreads();   // next operand written / S no longer read (the next unpack rewrites it)
+      if (Geo::staged_out && staged && i == n && leader) {
+        // the tile's blocks: 128-byte column halves of S's rows (b = 128),
+        // or block g's rows in S's column half g (b = 64)
+        const CUtensorMap* tq = sd == &s0 ? &tq0 : &tq1;
+        if constexpr (B == 128) {
+          tma_store_2d(tq, s_hi, 0, b0 * B);
+          tma_store_2d(tq, s_hi + 128 * 128, 64, b0 * B);
+        } else {
+          for (int gg = 0; gg < nbt; ++gg)
+            tma_store_2d(tq, s_hi + gg * (128 * 128 + 64 * 128), 0, (b0 + gg) * B);
+        }
+        bulk_commit();
+      }
     }
     if (!ok) break;
   }
+  if (Geo::staged_out && staged && leader) bulk_wait0();   // output stores complete
   if (!ok && leader) {
     // wind-down after an expired wait: the copies and MMAs already issued
     // finish (bounded waits) before the CTA frees its memory
@@ -438,9 +505,22 @@ poetx_status tile_launch(const TileSide& s0, const TileSide& s1, int n, cudaStre
   const int tiles = (s0.nb + Geo::G - 1) / Geo::G + (s1.nb + Geo::G - 1) / Geo::G;
   int grid = device_sm_count() * Geo::per_sm;
   if (grid > tiles) grid = tiles;
+  // output tensor maps (rows = blocks x b, b columns; 128-byte boxes); where
+  // one cannot be made (an unaligned Q) the kernel stores rows directly
+  CUtensorMap tq[2];
+  memset(tq, 0, sizeof(tq));
+  int staged = Geo::staged_out ? 1 : 0;
+  const TileSide* sides[2] = {&s0, &s1};
+  for (int k = 0; k < 2 && staged; ++k)
+    if (sides[k]->nb > 0 &&
+        !make_tmap_2d(&tq[k], sides[k]->Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                      (uint64_t)sides[k]->nb * B, (uint64_t)B, B == 128 ? 128 : 64, 64,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+      staged = 0;
   {
     KernelScope ks_(F32 ? "tc_cnp_tile_f32" : "tc_cnp_tile", s);
-    cnp_tile_kernel<B, F32><<<grid, kTileThreads, Geo::smem, s>>>(s0, s1, n, device_error_word());
+    cnp_tile_kernel<B, F32><<<grid, kTileThreads, Geo::smem, s>>>(s0, s1, tq[0], tq[1], staged, n,
+                                                                  device_error_word());
   }
   return check_launch();
 }

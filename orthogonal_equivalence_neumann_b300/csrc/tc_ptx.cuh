@@ -428,6 +428,38 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+// ---------------------------------------------------------------- 8 x 8 b16 fragments
+// Warp-collective.  Fragment layout: lane t holds row t / 4, columns
+// 2 (t % 4) and 2 (t % 4) + 1 (low half first) of an 8 x 8 matrix of 16-bit
+// elements.  stmatrix writes matrix m's row r to the 16 bytes at the address
+// lane 8 m + r gives (.trans: the matrix's transpose); movmatrix returns the
+// fragment of the transpose.
+__device__ __forceinline__ void stmatrix_x4(uint32_t saddr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                            uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, uint32_t r0, uint32_t r1,
+                                                  uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+__device__ __forceinline__ void stmatrix_x1(uint32_t saddr, uint32_t r0) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x1.shared.b16 [%0], {%1};" ::"r"(saddr), "r"(r0)
+               : "memory");
+}
+__device__ __forceinline__ void stmatrix_x1_trans(uint32_t saddr, uint32_t r0) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x1.trans.shared.b16 [%0], {%1};" ::"r"(saddr), "r"(r0)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t r) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(r));
+  return d;
+}
+
 // As tmem_st32, 16 and 8 consecutive columns.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
