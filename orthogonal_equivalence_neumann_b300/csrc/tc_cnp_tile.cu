@@ -80,9 +80,8 @@ __device__ __forceinline__ void split_bf16(float v, uint32_t& hi, uint32_t& lo) 
   lo = bf16_bits(v - __bfloat162float(h));
 }
 
-// 8 bf16 of a 16-byte shared-memory unit, widened.
-__device__ __forceinline__ void widen8(const uint8_t* p, float* v) {
-  const uint4 u = *reinterpret_cast<const uint4*>(p);
+// 8 bf16 of a 16-byte unit, widened.
+__device__ __forceinline__ void widen8(const uint4 u, float* v) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
@@ -106,9 +105,10 @@ struct TileGeo {
   static constexpr int smem = used > 78848 ? used : 78848;
   static constexpr int per_sm = 2;
   static constexpr int tmem_cols = 256;                    // accumulator 128, X hi 64 [, X lo 64]
-  // bf16 Q of b >= 64 leaves through shared memory (S, free after the last
-  // product) and tensor stores: 128-byte rows, as the operand layout
-  static constexpr bool staged_out = !F32 && B >= 64;
+  // Q leaves through shared memory (S, free after the last product) and
+  // tensor stores, in 128-byte rows: bf16 Q of b >= 64 (as the operand
+  // layout), fp32 Q of b = 128 (32-column boxes over S's rows)
+  static constexpr bool staged_out = (!F32 && B >= 64) || (F32 && B == 128);
 };
 
 // -x for each bf16 of a pair that is not zero (zeros keep their +0 pattern).
@@ -372,6 +372,17 @@ __global__ void __launch_bounds__(kTileThreads, 2)
       }
       ++mma_count;
       tc_fence_after();
+      // fp32 Q staged (b = 128): the output's first 32 columns go over this
+      // thread's row of S lo, the second over its row of S hi (no other
+      // thread reads those bytes); the lo part the second pass needs is read
+      // before the first overwrites it
+      const bool stage_f32 = F32 && Geo::staged_out && staged && i == n;
+      uint4 lo_next[4];
+      if (stage_f32) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          lo_next[q] = *reinterpret_cast<const uint4*>(s_lo + op_off(r, half * HC + 32 + 8 * q));
+      }
       // the warp's rows all lie in one block (b >= 32), so its TMEM loads
       // share their columns: [g*B + half*HC, g*B + (half+1)*HC)
 #pragma unroll 1
@@ -388,8 +399,10 @@ __global__ void __launch_bounds__(kTileThreads, 2)
           for (int q = 0; q < W / 8; ++q) {
             const uint32_t off = op_off(r, g * B + c0 + 8 * q);
             float lo[8];
-            widen8(s_hi + off, k2 + 8 * q);
-            widen8(s_lo + off, lo);
+            widen8(*reinterpret_cast<const uint4*>(s_hi + off), k2 + 8 * q);
+            widen8(stage_f32 && c0 != half * HC ? lo_next[q]
+                                                : *reinterpret_cast<const uint4*>(s_lo + off),
+                   lo);
 #pragma unroll
             for (int e = 0; e < 8; ++e) k2[8 * q + e] += lo[e];
           }
@@ -437,10 +450,20 @@ __global__ void __launch_bounds__(kTileThreads, 2)
           }
           const size_t row = ((size_t)(b0 + g) * B + ri) * B + c0;
           if constexpr (F32) {
-            float4* o = reinterpret_cast<float4*>(static_cast<float*>(sd->Q) + row);
+            if (stage_f32) {
+              // a 128-row x 32-column fp32 box, 128-byte swizzle: row r's
+              // 16-byte chunk q at r * 128 + (q ^ (r % 8)) * 16
+              uint8_t* dst = (c0 == half * HC ? s_lo : s_hi) + half * (128 * 128) + r * 128;
 #pragma unroll
-            for (int q = 0; q < W / 4; ++q)
-              o[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+              for (int q = 0; q < W / 4; ++q)
+                *reinterpret_cast<float4*>(dst + ((q ^ (r & 7)) << 4)) =
+                    make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+            } else {
+              float4* o = reinterpret_cast<float4*>(static_cast<float*>(sd->Q) + row);
+#pragma unroll
+              for (int q = 0; q < W / 4; ++q)
+                o[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+            }
           } else if (Geo::staged_out && staged) {
             // into S (free: the products are done and bf16 Q reads no K here)
 #pragma unroll
@@ -469,7 +492,12 @@ __global__ void __launch_bounds__(kTileThreads, 2)
         // the tile's blocks: 128-byte column halves of S's rows (b = 128),
         // or block g's rows in S's column half g (b = 64)
         const CUtensorMap* tq = sd == &s0 ? &tq0 : &tq1;
-        if constexpr (B == 128) {
+        if constexpr (F32) {   // boxes of 32 columns: S lo / S hi rows of column half 0, then 1
+          tma_store_2d(tq, s_lo, 0, b0 * B);
+          tma_store_2d(tq, s_hi, 32, b0 * B);
+          tma_store_2d(tq, s_lo + 128 * 128, 64, b0 * B);
+          tma_store_2d(tq, s_hi + 128 * 128, 96, b0 * B);
+        } else if constexpr (B == 128) {
           tma_store_2d(tq, s_hi, 0, b0 * B);
           tma_store_2d(tq, s_hi + 128 * 128, 64, b0 * B);
         } else {
@@ -513,9 +541,12 @@ poetx_status tile_launch(const TileSide& s0, const TileSide& s1, int n, cudaStre
   const TileSide* sides[2] = {&s0, &s1};
   for (int k = 0; k < 2 && staged; ++k)
     if (sides[k]->nb > 0 &&
-        !make_tmap_2d(&tq[k], sides[k]->Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                      (uint64_t)sides[k]->nb * B, (uint64_t)B, B == 128 ? 128 : 64, 64,
-                      CU_TENSOR_MAP_SWIZZLE_128B))
+        !(F32 ? make_tmap_2d(&tq[k], sides[k]->Q, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                             (uint64_t)sides[k]->nb * B, (uint64_t)B, 128, 32,
+                             CU_TENSOR_MAP_SWIZZLE_128B)
+              : make_tmap_2d(&tq[k], sides[k]->Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                             (uint64_t)sides[k]->nb * B, (uint64_t)B, B == 128 ? 128 : 64, 64,
+                             CU_TENSOR_MAP_SWIZZLE_128B)))
       staged = 0;
   {
     KernelScope ks_(F32 ? "tc_cnp_tile_f32" : "tc_cnp_tile", s);
