@@ -10,35 +10,43 @@
 //
 // A CTA works on tiles of 128 rows.  A tile holds G = 128 / b consecutive
 // blocks as one block-diagonal 128 x 128 matrix (b = 32: four blocks, b = 64:
-// two, b = 128: one); the off-diagonal zeros stay exactly zero through every
-// product, so each block is computed as if alone.  The chain is the Horner
-// form of Q - I = 2K + 2K^2 + ... + 2K^n + K^{n+1}:
+// two, b = 128: one); each product covers block g's own columns (N = b) from
+// its own K range, so the MMA work scales with b and the zeros between the
+// blocks are never touched.  The chain is the Horner form of
+// Q - I = 2K + 2K^2 + ... + 2K^n + K^{n+1}:
 //   X_1 = K,  X_{i+1} = X_i K + 2K  (i = 1..n),  Q = I + X_{n+1},
-// each product one tcgen05.mma chain (M = 128 rows, N = 128, K = 16; fp32
-// accumulation in TMEM); the 2K term is added in fp32, from the operand's
-// own bf16 K (bf16 Q) or its hi + lo parts (fp32 Q), when the accumulator is
-// turned into the next operand.
-//   bf16 Q:  operands rounded to bf16 (X_i and K);
+// each product one tcgen05.mma chain (M = 128 rows, K = 16 per instruction;
+// fp32 accumulation in TMEM).
+//   bf16 Q:  operands rounded to bf16 (X_i and K); for b >= 64 the 2K term
+//            is a second product, 2I . K, into the same accumulator (2I sits
+//            in TMEM; 2 * bf16 is exact), so the accumulator is X_{i+1} as
+//            it stands; at b = 32 it is added in fp32 from K when the
+//            accumulator is read;
 //   fp32 Q:  every operand split into two bf16 parts, x = hi + lo with
 //            hi = bf16(x), lo = bf16(x - hi), and each product taken as
 //            X_hi K_hi + X_hi K_lo + X_lo K_hi (the lo * lo term, 2^-16 of
-//            the product, is dropped) -- three MMA chains per step; this
-//            keeps about 16 significant bits per operand (relative error
-//            of Q below 1e-6 at the sweep's sizes, against the fp32 bar of
-//            1e-5).
+//            the product, is dropped) -- three MMA chains per step; the 2K
+//            term is added in fp32 from K's hi + lo parts when the
+//            accumulator is read.  This keeps about 16 significant bits per
+//            operand (relative error of Q below 1e-6 at the sweep's sizes,
+//            against the fp32 bar of 1e-5).
 // Operands: B[k][c] = K[k][c], stored as S = -K = K^T (row c of S is column
 // c of K), K-major with the 128-byte swizzle, in shared memory; the first
 // product reads A = X_1 = K as the same S through a transposed (MN-major)
 // descriptor; later products read A = X_i from tensor memory (lane = row,
 // two bf16 of consecutive columns per 32-bit column), where the conversion
-// of the accumulator writes it.  Thread (warp w, lane l) owns row
-// r = 32 (w % 4) + l (its TMEM lane) and half w / 4 of the row's block
-// columns.  Tiles are handed out round-robin; one parameter buffer, whose
-// next tile's copy is issued as soon as the unpack has read it, so the copy
-// runs beside the chain.  Two CTAs share an SM (tensor memory: 256 columns
-// each), so one's unpack and conversions overlap the other's products.  One
-// thread polls each barrier and the CTA follows through a CTA barrier; every
-// wait is bounded (tc_ptx.cuh).
+// of the accumulator writes it.  The unpack turns the packed parameters into
+// S with warp-wide 8 x 8 fragment stores (stmatrix, plain and transposed).
+// Thread (warp w, lane l) owns row r = 32 (w % 4) + l (its TMEM lane) and
+// half w / 4 of the row's block columns.  Q leaves through shared memory
+// and tensor stores where its rows fill 128-byte boxes (bf16 Q of b >= 64,
+// fp32 Q of b = 128), else by each thread's row stores.  Tiles are handed
+// out round-robin; one parameter buffer, whose next tile's bulk copy is
+// issued as soon as the unpack has read it, so the copy runs beside the
+// chain.  Two CTAs share an SM (tensor memory: 256 columns each), so one's
+// unpack and conversions overlap the other's products.  One thread polls
+// each barrier and the CTA follows through a CTA barrier; every wait is
+// bounded (tc_ptx.cuh).
 #include <cstring>
 
 #include "common.cuh"
@@ -109,6 +117,9 @@ struct TileGeo {
   // tensor stores, in 128-byte rows: bf16 Q of b >= 64 (as the operand
   // layout), fp32 Q of b = 128 (32-column boxes over S's rows)
   static constexpr bool staged_out = (!F32 && B >= 64) || (F32 && B == 128);
+  // bf16 Q of b >= 64 takes the 2K term as a product with 2I (at b = 32 the
+  // conversion's share of a step is small and the extra MMAs cost more)
+  static constexpr bool two_i_mma = !F32 && B >= 64;
 };
 
 // -x for each bf16 of a pair that is not zero (zeros keep their +0 pattern).
@@ -251,7 +262,7 @@ __global__ void __launch_bounds__(kTileThreads, 2)
     tmem_st32(x_hi + lane_off + (uint32_t)(half * 32), z);
     if constexpr (F32) {
       tmem_st32(x_lo + lane_off + (uint32_t)(half * 32), z);
-    } else {
+    } else if constexpr (Geo::two_i_mma) {
       // 2I: 2.0 (bf16 0x4000) at column r of row r
       uint32_t d2[32];
 #pragma unroll
@@ -359,7 +370,7 @@ __global__ void __launch_bounds__(kTileThreads, 2)
                 mma_bf16_ts(d, x_lo + xa, dk_h + (ob >> 4), id_kk, 1);
               }
             }
-            if constexpr (!F32)   // + 2I . K
+            if constexpr (Geo::two_i_mma)   // + 2I . K
               mma_bf16_ts(d, two_i + (uint32_t)(k0 / 2), dk_h + (ob >> 4), id_kk, 1);
           }
         mma_commit(mma_done);
@@ -392,19 +403,21 @@ __global__ void __launch_bounds__(kTileThreads, 2)
         if constexpr (W == 32) tmem_ld32(ta, acc);
         else tmem_ld16(ta, acc);
         float x[W];
-        if constexpr (F32) {
-          // 2K from the operand's own K (S = -K), hi + lo
+        if constexpr (!Geo::two_i_mma) {
+          // 2K from the operand's own K (S = -K): bf16, or hi + lo for fp32 Q
           float k2[W];
 #pragma unroll
           for (int q = 0; q < W / 8; ++q) {
             const uint32_t off = op_off(r, g * B + c0 + 8 * q);
-            float lo[8];
             widen8(*reinterpret_cast<const uint4*>(s_hi + off), k2 + 8 * q);
-            widen8(stage_f32 && c0 != half * HC ? lo_next[q]
-                                                : *reinterpret_cast<const uint4*>(s_lo + off),
-                   lo);
+            if constexpr (F32) {
+              float lo[8];
+              widen8(stage_f32 && c0 != half * HC ? lo_next[q]
+                                                  : *reinterpret_cast<const uint4*>(s_lo + off),
+                     lo);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) k2[8 * q + e] += lo[e];
+              for (int e = 0; e < 8; ++e) k2[8 * q + e] += lo[e];
+            }
           }
           tmem_ld_wait();
           tmem_regs_ready(acc);
