@@ -89,6 +89,8 @@ def kernel_work(case):
         "tc_cnp_tile_f32": ("tensor", 2 * cnp_f, 4 * npk + 4 * nbb),
         "tc_cnp_unpack": ("hbm", 0.0, 4 * npk + 2 * nbb),
         "tc_cnp_fwd": ("tensor", 2 * cnp_f, 2 * nbb + 2 * nbb),
+        "tc_cnp_unpack_f32": ("hbm", 0.0, 4 * npk + 4 * nbb),
+        "tc_cnp_fwd_f32": ("tensor", 2 * cnp_f, 4 * nbb + 4 * nbb),
         "tc_cnp_bwd_prep": ("hbm", 0.0, 4 * npk + 4 * nbb + 3 * 2 * nbb),
         "tc_cnp_bwd": ("tensor", 2 * cnpb_f, 3 * 2 * nbb + 4 * nbb + 4 * npk),
     }
@@ -412,9 +414,8 @@ def cnp_roofline_point(b, out_bytes, n, nblocks, seconds, peaks):
     """Roofline of one Cayley-Neumann generation call: algorithmic bytes (packed
     theta in, Q out) and flops (n products of b x b x b per block) against the
     measured HBM peak and the peak of the unit the products run on: bf16 Q on
-    the bf16 tensor cores; fp32 Q at b <= 128 on the tensor cores as three bf16
-    MMA chains per product (so a third of the bf16 peak); fp32 Q at b = 256 on
-    the CUDA cores (fp32 FMA peak from the unit counts and the clock)."""
+    the bf16 tensor cores; fp32 Q on the tensor cores as three bf16 MMA chains
+    per product (so a third of the bf16 peak)."""
     byts = nblocks * (4 * (b * (b - 1) // 2) + out_bytes * b * b)
     flops = nblocks * 2.0 * n * b ** 3
     t_hbm = byts / (peaks["hbm_gbs"] * 1e9)
@@ -422,10 +423,8 @@ def cnp_roofline_point(b, out_bytes, n, nblocks, seconds, peaks):
            "hbm_frac": round(t_hbm / seconds, 4)}
     if out_bytes == 2:
         unit, peak = "tensor", peaks["bf16_tflops"]
-    elif b <= 128:
-        unit, peak = "tensor_split3", peaks["bf16_tflops"] / 3
     else:
-        unit, peak = "alu", ALU_FP32_PEAK_TFLOPS
+        unit, peak = "tensor_split3", peaks["bf16_tflops"] / 3
     t_c = flops / (peak * 1e12)
     out["bound"] = "hbm" if t_hbm >= t_c else unit
     out["frac"] = round(max(t_hbm, t_c) / seconds, 4)

@@ -162,7 +162,8 @@ poetx_status poetx_cayley_neumann_pair(const float* theta_P, int nb_P, int b_P,
     return tc::cnp_tile_fwd(theta_P, nb_P, theta_R, nb_R, b_P, n, Q_P, Q_R,
                             out_dtype == POETX_F32, stream);
   if (b_P == b_R && tc_cnp_supported(b_P, out_dtype) && nb_P + nb_R <= 65535)
-    return tc::cnp_fwd_pair_bf16ops(theta_P, nb_P, theta_R, nb_R, b_P, n, Q_P, Q_R, false, stream);
+    return tc::cnp_fwd_pair_bf16ops(theta_P, nb_P, theta_R, nb_R, b_P, n, Q_P, Q_R,
+                                    out_dtype == POETX_F32, stream);
   POETX_TRY(poetx_cayley_neumann(theta_P, nb_P, b_P, n, Q_P, out_dtype, stream));
   return poetx_cayley_neumann(theta_R, nb_R, b_R, n, Q_R, out_dtype, stream);
 }

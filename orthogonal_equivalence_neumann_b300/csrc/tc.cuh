@@ -119,7 +119,9 @@ poetx_status cnp_tile_fwd(const float* theta0, int nb0, const float* theta1, int
                           void* Q0, void* Q1, bool out_f32, cudaStream_t s);
 
 // Cayley-Neumann forward / backward with bf16 operands and fp32 accumulation
-// (tcgen05), b in {128, 256}.  The backward overwrites dtheta.
+// (tcgen05), b in {128, 256}; the forward also gives fp32 Q at b = 256 (each
+// product as three bf16 products of split operands).  The backward
+// overwrites dtheta.
 bool cnp_supported(int b);
 poetx_status cnp_fwd_bf16ops(const float* theta, int nb, int b, int n, void* Q, bool out_f32,
                              cudaStream_t s);

@@ -262,6 +262,291 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
+// fp32 Q at b = 256 (the three-term split on the tensor cores): the unpack
+// writes Kop = -K as two bf16 parts, hi = bf16(Kop), lo = bf16(Kop - hi), into
+// the block's own fp32 Q buffer, which holds exactly both: viewed as bf16
+// [nb * 512][256], block j's hi rows are j * 512 + c and its lo rows
+// j * 512 + 256 + c.  One CTA per 32-row group of one block, the rows
+// assembled in fp32 in shared memory (row pitch 257 words: the column writes
+// fall in distinct banks); all loads are issued before their stores.
+constexpr int kSplitRows = 32;
+
+__global__ void __launch_bounds__(kUnpackThreads)
+    cnp_unpack_split_kernel(FwdSide f0, FwdSide f1) {
+  constexpr int B = 256, LD = B + 1, P = B * (B - 1) / 2;
+  __shared__ float tile[kSplitRows * LD];
+  const bool second = (int)blockIdx.y >= f0.nb;
+  const FwdSide& sd = second ? f1 : f0;
+  const int j = second ? (int)blockIdx.y - f0.nb : (int)blockIdx.y;
+  const int c0 = blockIdx.x * kSplitRows;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const float* th = sd.theta + (size_t)j * P;
+  constexpr int W = kUnpackThreads / 32;
+  // right of the diagonal (and the diagonal): warp w takes rows c0 + w, c0 + w + 8, ...
+#pragma unroll
+  for (int rr0 = 0; rr0 < kSplitRows; rr0 += W) {
+    const int rr = rr0 + warp, c = c0 + rr;
+    const float* prow = th + skew_row_start(c, B) - (c + 1);   // prow[k] = theta(c, k)
+    float v[B / 32];
+#pragma unroll
+    for (int q = 0; q < B / 32; ++q) {
+      const int k = q * 32 + lane;
+      v[q] = k > c ? __ldg(prow + k) : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < B / 32; ++q) {
+      const int k = q * 32 + lane;
+      if (k >= c) tile[rr * LD + k] = -v[q];
+    }
+  }
+  // left of the diagonal: lane = row c0 + lane, warp w takes packed rows k = w, w + 8, ...
+  {
+    const int c = c0 + lane;
+    constexpr int U = 8;
+    for (int k0 = warp; k0 < c0 + kSplitRows - 1; k0 += W * U) {
+      float v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int k = k0 + u * W;
+        v[u] = k < c ? __ldg(th + skew_row_start(k, B) + (c - k - 1)) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int k = k0 + u * W;
+        if (k < c) tile[lane * LD + k] = v[u];
+      }
+    }
+  }
+  __syncthreads();
+  __nv_bfloat16* qb = static_cast<__nv_bfloat16*>(sd.Q) + (size_t)j * 512 * B;
+  uint32_t* hi = reinterpret_cast<uint32_t*>(qb + (size_t)c0 * B);
+  uint32_t* lo = reinterpret_cast<uint32_t*>(qb + (size_t)(B + c0) * B);
+  for (int u = threadIdx.x; u < kSplitRows * B / 2; u += kUnpackThreads) {
+    const int r = u / (B / 2), c2 = (u % (B / 2)) * 2;
+    const float a = tile[r * LD + c2], b = tile[r * LD + c2 + 1];
+    const __nv_bfloat16 ha = __float2bfloat16_rn(a), hb = __float2bfloat16_rn(b);
+    hi[u] = (uint32_t)__bfloat16_as_ushort(ha) | ((uint32_t)__bfloat16_as_ushort(hb) << 16);
+    lo[u] = pack_bf16x2(a - __bfloat162float(ha), b - __bfloat162float(hb));
+  }
+}
+
+// fp32 Q at b = 256: one CTA per 128-row slab (the two slabs of a block a
+// cluster), the whole chain on the tensor cores as three bf16 products per
+// step, X_hi K_hi + X_hi K_lo + X_lo K_hi (fp32 accumulation; the dropped
+// X_lo K_lo term is below 2^-16 of the product).  Tensor memory holds the
+// slab's accumulator (128 x 256 fp32, columns [0, 256)) and X_i as the A
+// operand, hi at [256, 384) and lo at [384, 512) (two bf16 per column), so
+// one CTA owns an SM's tensor memory.  Warp 0 streams Kop's hi and lo parts
+// (the B operand: Kop[c][k] = K[k][c], K-major) through a ring of 64-column
+// chunks by TMA, every step (K does not fit in shared memory twice); warp 1
+// issues the products; warps 2..9 turn the accumulator into the next X
+// (X_{i+1} = X_i K + 2K, 2K from the slab's own Kop rows) or, after the
+// last step, into Q = I + X_{n+1}, staged in the then idle ring and written
+// by tensor stores once both slabs of the block are past their last read of
+// Kop (cluster barrier): Q overwrites the buffer Kop lives in.
+constexpr int kF32Threads = 320;
+constexpr int kF32Workers = 256;
+constexpr int kF32Stages = 3;
+constexpr int kF32Chunk = 256 * 64 * 2;            // one part of a 64-column chunk of Kop
+constexpr int kF32Stage = 2 * kF32Chunk;           // hi + lo
+constexpr int kF32Smem = 1024 + kF32Stages * kF32Stage + 256;
+
+__global__ void __launch_bounds__(kF32Threads, 1)
+    cnp_fwd_f32_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_constant__ CUtensorMap tk1,
+                       const __grid_constant__ CUtensorMap tq0, const __grid_constant__ CUtensorMap tq1,
+                       FwdSide f0, FwdSide f1, int n, int* err) {
+  constexpr int B = 256;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kF32Stages * kF32Stage);
+  uint64_t* empty = full + kF32Stages;
+  uint64_t* acc_full = empty + kF32Stages;
+  uint64_t* x_ready = acc_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(x_ready + 1);
+  int* failed = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const bool second = (int)blockIdx.y >= f0.nb;
+  const int j = second ? (int)blockIdx.y - f0.nb : (int)blockIdx.y;
+  const FwdSide& sd = second ? f1 : f0;
+  const CUtensorMap* tk = second ? &tk1 : &tk0;
+  const CUtensorMap* tq = second ? &tq1 : &tq0;
+  const int r0 = blockIdx.x * 128;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kF32Stages; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(x_ready, kF32Workers);
+    *failed = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t x_hi = tmem + 256, x_lo = tmem + 384;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ------------------------------------------------ Kop chunks by TMA
+    if (lane == 0) {
+      int it = 0, issued = 0;
+      for (int i = 1; i <= n && ok; ++i)
+        for (int c = 0; c < B / 64 && ok; ++c, ++it) {
+          const int slot = it % kF32Stages;
+          if (it >= kF32Stages &&
+              !(ok = mbar_wait(empty + slot, (uint32_t)(it / kF32Stages - 1) & 1, err)))
+            break;
+          uint8_t* dst = ring + slot * kF32Stage;
+          mbar_arrive_expect_tx(full + slot, (uint32_t)kF32Stage);
+          tma_load_2d(dst, tk, 64 * c, j * 512, full + slot);
+          tma_load_2d(dst + kF32Chunk, tk, 64 * c, j * 512 + 256, full + slot);
+          ++issued;
+        }
+      if (!ok) {
+        *failed = 1;
+        // the copies in flight land before the CTA's memory goes (bounded)
+        for (int k = (issued > kF32Stages ? issued - kF32Stages : 0); k < issued; ++k)
+          mbar_wait_bounded(full + k % kF32Stages, (uint32_t)(k / kF32Stages) & 1, 1u << 16,
+                            nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ products
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(128, B, false, false);
+      int it = 0;
+      bool pending = false;
+      for (int i = 1; i <= n && ok; ++i) {
+        if (!(ok = mbar_wait(x_ready, (uint32_t)(i - 1) & 1, err))) break;
+        tc_fence_after();
+        for (int c = 0; c < B / 64; ++c, ++it) {
+          const int slot = it % kF32Stages;
+          if (!(ok = mbar_wait(full + slot, (uint32_t)(it / kF32Stages) & 1, err))) break;
+          tc_fence_after();
+          const uint32_t bh = smem_u32(ring + slot * kF32Stage), bl = bh + kF32Chunk;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t xa = (uint32_t)(32 * c + 8 * kk);   // (64 c + 16 kk) / 2
+            mma_bf16_ts(tmem, x_hi + xa, sw128_desc(bh + kk * 32, 16, 1024), idesc, (c | kk) != 0);
+            mma_bf16_ts(tmem, x_hi + xa, sw128_desc(bl + kk * 32, 16, 1024), idesc, 1);
+            mma_bf16_ts(tmem, x_lo + xa, sw128_desc(bh + kk * 32, 16, 1024), idesc, 1);
+          }
+          mma_commit(empty + slot);
+          pending = true;
+        }
+        if (!ok) break;
+        mma_commit(acc_full);
+      }
+      if (!ok) {
+        *failed = 1;
+        // the products issued complete before tensor memory is freed (bounded)
+        if (pending && it > 0)
+          mbar_wait_bounded(empty + (it - 1) % kF32Stages, (uint32_t)((it - 1) / kF32Stages) & 1,
+                            1u << 16, nullptr);
+      }
+    }
+  } else {
+    // ------------------------------------------------ conversions
+    const int quarter = warp % 4, half = (warp - 2) / 4;
+    const int r = quarter * 32 + lane, row = r0 + r;   // TMEM lane, row of the block
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(sd.Q) + (size_t)j * 512 * B;
+    const uint4* kh = reinterpret_cast<const uint4*>(qb + (size_t)row * B);         // Kop hi row
+    const uint4* kl = reinterpret_cast<const uint4*>(qb + (size_t)(B + row) * B);   // Kop lo row
+    // X_1 = K on the slab rows: -Kop (both parts negate exactly)
+    for (int c0 = half * 128; c0 < half * 128 + 128; c0 += 32) {
+      uint32_t h[16], l[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 a = kh[c0 / 8 + q], b = kl[c0 / 8 + q];
+        h[4 * q] = a.x ^ 0x80008000u; h[4 * q + 1] = a.y ^ 0x80008000u;
+        h[4 * q + 2] = a.z ^ 0x80008000u; h[4 * q + 3] = a.w ^ 0x80008000u;
+        l[4 * q] = b.x ^ 0x80008000u; l[4 * q + 1] = b.y ^ 0x80008000u;
+        l[4 * q + 2] = b.z ^ 0x80008000u; l[4 * q + 3] = b.w ^ 0x80008000u;
+      }
+      tmem_st16(x_hi + lane_off + (uint32_t)(c0 / 2), h);
+      tmem_st16(x_lo + lane_off + (uint32_t)(c0 / 2), l);
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(x_ready);
+    for (int i = 1; i <= n && ok; ++i) {
+      if (!(ok = mbar_wait(acc_full, (uint32_t)(i - 1) & 1, err))) break;
+      tc_fence_after();
+      for (int c0 = half * 128; c0 < half * 128 + 128; c0 += 32) {
+        uint32_t acc[32];
+        tmem_ld32(tmem + lane_off + (uint32_t)c0, acc);
+        float k2[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float lo[8];
+          ld_bf16x8(reinterpret_cast<const uint8_t*>(kh + c0 / 8 + q), k2 + 8 * q);
+          ld_bf16x8(reinterpret_cast<const uint8_t*>(kl + c0 / 8 + q), lo);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) k2[8 * q + e] += lo[e];
+        }
+        tmem_ld_wait();
+        tmem_regs_ready(acc);
+        float x[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(acc[e]) - 2.f * k2[e];   // K = -Kop
+        if (i < n) {
+          uint32_t h[16], l[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const __nv_bfloat16 a = __float2bfloat16_rn(x[2 * e]), b = __float2bfloat16_rn(x[2 * e + 1]);
+            h[e] = (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+            l[e] = pack_bf16x2(x[2 * e] - __bfloat162float(a), x[2 * e + 1] - __bfloat162float(b));
+          }
+          tmem_st16(x_hi + lane_off + (uint32_t)(c0 / 2), h);
+          tmem_st16(x_lo + lane_off + (uint32_t)(c0 / 2), l);
+        } else {
+          // Q = I + X_{n+1} into the idle ring: 128 x 32 fp32 boxes (128-byte
+          // swizzle: row r's 16-byte chunk q at r * 128 + (q ^ (r % 8)) * 16)
+          if (__any_sync(0xffffffffu, (unsigned)(row - c0) < 32u)) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (row == c0 + e) x[e] += 1.f;
+          }
+          uint8_t* box = ring + (c0 / 32) * (128 * 128) + r * 128;
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(box + ((q ^ (r & 7)) << 4)) =
+                make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+        }
+      }
+      if (i < n) {
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(x_ready);
+      }
+    }
+    if (!ok) *failed = 1;
+    fence_proxy_async_smem();   // the staged Q, for the tensor stores
+  }
+  tc_fence_before();
+  __syncthreads();
+  // both slabs of the block are past their last read of Kop (the ring's
+  // copies, the 2K rows): Q may overwrite it
+  cluster_sync();
+  if (threadIdx.x == 0 && *failed == 0) {
+    for (int q = 0; q < B / 32; ++q) tma_store_2d(tq, ring + q * (128 * 128), 32 * q, j * B + r0);
+    bulk_commit();
+    bulk_wait0();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // ====================================================================== backward
 struct Side {
   const float* theta;
@@ -905,10 +1190,57 @@ __global__ void __launch_bounds__(kRingThreads, 1)
 
 bool cnp_supported(int b) { return b == 128 || b == 256; }
 
+namespace {
+
+// fp32 Q at b = 256: the split unpack, then the chain in 2-CTA clusters.
+poetx_status cnp_fwd_f32_launch(const float* theta0, int nb0, const float* theta1, int nb1, int n,
+                                void* Q0, void* Q1, cudaStream_t s) {
+  FwdSide f0{theta0, Q0, nb0}, f1{theta1, Q1, nb1};
+  const FwdSide& t1 = nb1 > 0 ? f1 : f0;
+  const FwdSide& t0 = nb0 > 0 ? f0 : f1;
+  // Kop hi / lo in the Q buffers as bf16 [nb * 512][256]; Q as fp32 [nb * 256][256]
+  CUtensorMap tk0, tk1, tq0, tq1;
+  const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  if (!make_tmap_2d(&tk0, t0.Q, bf, 2, (uint64_t)t0.nb * 512, 256, 256, 64, sw) ||
+      !make_tmap_2d(&tk1, t1.Q, bf, 2, (uint64_t)t1.nb * 512, 256, 256, 64, sw) ||
+      !make_tmap_2d(&tq0, t0.Q, f32, 4, (uint64_t)t0.nb * 256, 256, 128, 32, sw) ||
+      !make_tmap_2d(&tq1, t1.Q, f32, 4, (uint64_t)t1.nb * 256, 256, 128, 32, sw))
+    return POETX_ERR_CUDA;
+  {
+    KernelScope ks_("tc_cnp_unpack_f32", s);
+    cnp_unpack_split_kernel<<<dim3(256 / kSplitRows, nb0 + nb1), kUnpackThreads, 0, s>>>(f0, f1);
+  }
+  poetx_status st = check_launch();
+  if (st != POETX_OK) return st;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, nb0 + nb1);
+  cfg.blockDim = dim3(kF32Threads);
+  cfg.dynamicSmemBytes = kF32Smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (set_max_dynamic_smem((const void*)cnp_fwd_f32_kernel, kF32Smem) != cudaSuccess)
+    return check_launch();
+  KernelScope ks_("tc_cnp_fwd_f32", s);
+  cudaLaunchKernelEx(&cfg, cnp_fwd_f32_kernel, tk0, tk1, tq0, tq1, f0, f1, n, device_error_word());
+  return check_launch();
+}
+
+}  // namespace
+
 poetx_status cnp_fwd_pair_bf16ops(const float* theta0, int nb0, const float* theta1, int nb1,
                                   int b, int n, void* Q0, void* Q1, bool out_f32, cudaStream_t s) {
   if (nb0 + nb1 <= 0) return POETX_OK;
-  if (out_f32 || !cnp_supported(b) || n < 1 || nb0 + nb1 > 65535) return POETX_ERR_UNSUPPORTED;
+  if (!cnp_supported(b) || n < 1 || nb0 + nb1 > 65535) return POETX_ERR_UNSUPPORTED;
+  if (out_f32)
+    return b == 256 ? cnp_fwd_f32_launch(theta0, nb0, theta1, nb1, n, Q0, Q1, s)
+                    : POETX_ERR_UNSUPPORTED;
   FwdSide f0{theta0, Q0, nb0}, f1{theta1, Q1, nb1};
   const FwdSide& t1 = nb1 > 0 ? f1 : f0;
   const FwdSide& t0 = nb0 > 0 ? f0 : f1;

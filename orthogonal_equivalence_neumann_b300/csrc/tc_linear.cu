@@ -27,7 +27,8 @@ namespace poetx {
 
 // bf16 Q: tensor-core chain with bf16 operands (the fp32 path stays exact on the CUDA cores).
 bool tc_cnp_supported(int b, poetx_dtype out_dtype) {
-  return out_dtype == POETX_BF16 && tc::cnp_supported(b);
+  // bf16 Q at b in {128, 256}; fp32 Q at b = 256 (three-term split)
+  return tc::cnp_supported(b) && (out_dtype == POETX_BF16 || b == 256);
 }
 poetx_status tc_cnp_fwd(const float* theta, int nb, int b, int n, void* Q, poetx_dtype out_dtype,
                         cudaStream_t s) {

@@ -489,6 +489,37 @@ def test_wide_stack_layers_run_on_the_staged_applies(which):
     assert not any(n.startswith("tc_blockapply") or n.endswith("_simt") for n in names), sorted(names)
 
 
+@pytest.mark.parametrize("nb_P,nb_R", [(3, 0), (2, 5)])
+def test_cnp_fp32_b256_runs_on_the_tensor_cores(nb_P, nb_R):
+    """fp32 Q of 256-blocks: the split unpack and the three-term chain on the
+    tensor cores (checked by name: parity alone would not show the CUDA-core
+    kernel), one factor and both factors of a layer in one call, against the
+    oracle block by block."""
+    n = 3
+    thP = inputs.make_theta(nb_P, 256, 1e-2, 91)
+    thR = inputs.make_theta(max(nb_R, 1), 256, 1e-2, 92)[:nb_R]
+    QP = torch.empty(nb_P, 256, 256, dtype=torch.float32, device="cuda")
+    QR = torch.empty(max(nb_R, 1), 256, 256, dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    _lib.poetx_profile_report()
+    _lib.poetx_profile_enable(True)
+    try:
+        if nb_R == 0:
+            _lib.poetx_cayley_neumann(thP.cuda(), 256, n, QP)
+        else:
+            _lib.poetx_cayley_neumann_pair(thP.cuda(), 256, thR.cuda(), 256, n, QP, QR[:nb_R])
+        torch.cuda.synchronize()
+    finally:
+        _lib.poetx_profile_enable(False)
+    _lib.poetx_stream_status()
+    names = set(_lib.poetx_profile_report())
+    assert {"tc_cnp_unpack_f32", "tc_cnp_fwd_f32"} <= names, sorted(names)
+    assert not any(k.endswith("_simt") for k in names), sorted(names)
+    assert_close("Q_P", to64(QP), oracle.cnp(thP.double().numpy(), 256, n), TOL_F32)
+    if nb_R:
+        assert_close("Q_R", to64(QR[:nb_R]), oracle.cnp(thR.double().numpy(), 256, n), TOL_F32)
+
+
 @pytest.mark.parametrize("d_in,d_out,T", [(512, 768, 200), (2048, 2048, 600)])
 @pytest.mark.parametrize("b,n", [(256, 1), (256, 2), (256, 5), (128, 1), (128, 4)])
 def test_bf16_chain_backward_orders(d_in, d_out, T, b, n):
