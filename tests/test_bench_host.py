@@ -37,10 +37,10 @@ def test_cnp_roofline_point_bounds():
     f = bench.cnp_roofline_point(128, 4, 6, 4096, sec, PEAKS)
     t_split = 4096 * 2.0 * 6 * 128 ** 3 / (1.5e15 / 3)
     assert f["bound"] == "tensor_split3" and f["frac"] == pytest.approx(t_split / sec, rel=1e-3)
-    # fp32 Q at b = 256 is bound by the fp32 FMA units
+    # fp32 Q at b = 256 also runs the three-term split on the tensor cores
     a = bench.cnp_roofline_point(256, 4, 3, 4096, sec, PEAKS)
-    assert a["bound"] == "alu"
-    assert a["frac"] == pytest.approx(flops / (bench.ALU_FP32_PEAK_TFLOPS * 1e12) / sec, rel=1e-3)
+    assert a["bound"] == "tensor_split3"
+    assert a["frac"] == pytest.approx(flops / (1.5e15 / 3) / sec, rel=1e-3)
 
 
 def test_traffic_entries_follow_their_sources(tmp_path, monkeypatch):
