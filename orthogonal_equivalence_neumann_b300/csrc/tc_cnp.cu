@@ -339,9 +339,11 @@ __global__ void __launch_bounds__(kUnpackThreads)
 // one CTA owns an SM's tensor memory.  Warp 0 streams Kop's hi and lo parts
 // (the B operand: Kop[c][k] = K[k][c], K-major) through a ring of 64-column
 // chunks by TMA, every step (K does not fit in shared memory twice); warp 1
-// issues the products; warps 2..9 turn the accumulator into the next X
-// (X_{i+1} = X_i K + 2K, 2K from the slab's own Kop rows) or, after the
-// last step, into Q = I + X_{n+1}, staged in the then idle ring and written
+// issues the products, the 2K term among them as 2I . K over the slab's own
+// K range (2I, 128 x 128 bf16, sits in shared memory beside the ring; 2 * bf16
+// is exact); warps 2..9 turn the accumulator into the next X, split into its
+// bf16 parts, or, after the last step, into Q = I + X_{n+1}, staged in the
+// then idle ring and written
 // by tensor stores once both slabs of the block are past their last read of
 // Kop (cluster barrier): Q overwrites the buffer Kop lives in.
 constexpr int kF32Threads = 320;
@@ -349,7 +351,8 @@ constexpr int kF32Workers = 256;
 constexpr int kF32Stages = 3;
 constexpr int kF32Chunk = 256 * 64 * 2;            // one part of a 64-column chunk of Kop
 constexpr int kF32Stage = 2 * kF32Chunk;           // hi + lo
-constexpr int kF32Smem = 1024 + kF32Stages * kF32Stage + 256;
+constexpr int kF32TwoI = 128 * 128 * 2;            // 2I over the slab's K range, bf16
+constexpr int kF32Smem = 1024 + kF32Stages * kF32Stage + kF32TwoI + 256;
 
 __global__ void __launch_bounds__(kF32Threads, 1)
     cnp_fwd_f32_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_constant__ CUtensorMap tk1,
@@ -360,7 +363,8 @@ __global__ void __launch_bounds__(kF32Threads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kF32Stages * kF32Stage);
+  uint8_t* two_i = smem + kF32Stages * kF32Stage;    // [2 k-chunks][128 rows][64 k] bf16, K-major
+  uint64_t* full = reinterpret_cast<uint64_t*>(two_i + kF32TwoI);
   uint64_t* empty = full + kF32Stages;
   uint64_t* acc_full = empty + kF32Stages;
   uint64_t* x_ready = acc_full + 1;
@@ -386,6 +390,15 @@ __global__ void __launch_bounds__(kF32Threads, 1)
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, 512);
+  // 2I: 2.0 (bf16 0x4000) at (r, r) of the slab's K range, zero elsewhere
+  for (int o = threadIdx.x * 16; o < kF32TwoI; o += kF32Threads * 16)
+    *reinterpret_cast<uint4*>(two_i + o) = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  if (threadIdx.x < 128) {
+    const int r = threadIdx.x;
+    *reinterpret_cast<uint16_t*>(two_i + sw128_offset(r, r, 128)) = 0x4000;
+  }
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -431,12 +444,19 @@ __global__ void __launch_bounds__(kF32Threads, 1)
           if (!(ok = mbar_wait(full + slot, (uint32_t)(it / kF32Stages) & 1, err))) break;
           tc_fence_after();
           const uint32_t bh = smem_u32(ring + slot * kF32Stage), bl = bh + kF32Chunk;
+          // the chunk lies in the slab's own K range: it also carries 2I . K
+          const int ci = c - 2 * (int)blockIdx.x;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t xa = (uint32_t)(32 * c + 8 * kk);   // (64 c + 16 kk) / 2
             mma_bf16_ts(tmem, x_hi + xa, sw128_desc(bh + kk * 32, 16, 1024), idesc, (c | kk) != 0);
             mma_bf16_ts(tmem, x_hi + xa, sw128_desc(bl + kk * 32, 16, 1024), idesc, 1);
             mma_bf16_ts(tmem, x_lo + xa, sw128_desc(bh + kk * 32, 16, 1024), idesc, 1);
+            if (ci == 0 || ci == 1) {
+              const uint64_t ad = sw128_desc(smem_u32(two_i) + ci * (128 * 128) + kk * 32, 16, 1024);
+              mma_bf16(tmem, ad, sw128_desc(bh + kk * 32, 16, 1024), idesc, 1);
+              mma_bf16(tmem, ad, sw128_desc(bl + kk * 32, 16, 1024), idesc, 1);
+            }
           }
           mma_commit(empty + slot);
           pending = true;
@@ -483,20 +503,11 @@ __global__ void __launch_bounds__(kF32Threads, 1)
       for (int c0 = half * 128; c0 < half * 128 + 128; c0 += 32) {
         uint32_t acc[32];
         tmem_ld32(tmem + lane_off + (uint32_t)c0, acc);
-        float k2[32];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float lo[8];
-          ld_bf16x8(reinterpret_cast<const uint8_t*>(kh + c0 / 8 + q), k2 + 8 * q);
-          ld_bf16x8(reinterpret_cast<const uint8_t*>(kl + c0 / 8 + q), lo);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) k2[8 * q + e] += lo[e];
-        }
         tmem_ld_wait();
         tmem_regs_ready(acc);
-        float x[32];
+        float x[32];   // X_{i+1}: the products hold the 2K term
 #pragma unroll
-        for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(acc[e]) - 2.f * k2[e];   // K = -Kop
+        for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(acc[e]);
         if (i < n) {
           uint32_t h[16], l[16];
 #pragma unroll
