@@ -36,7 +36,8 @@
  * kernels run surface as POETX_ERR_CUDA from a later call or from
  * poetx_stream_status().  Kernels that wait on the tensor-core pipeline use
  * bounded waits: on expiry they set a device error word instead of hanging,
- * read back by poetx_stream_status() as POETX_ERR_TIMEOUT.
+ * read back by poetx_stream_status() as POETX_ERR_TIMEOUT; a kernel that meets
+ * a value outside the range it computes in sets POETX_ERR_RANGE there.
  */
 #ifndef POETX_H
 #define POETX_H
@@ -57,7 +58,8 @@ typedef enum {
   POETX_ERR_UNSUPPORTED = 3,     /* block size outside the supported set */
   POETX_ERR_NOT_PERMUTATION = 4, /* poetx_check_perm: an index repeats or is out of range */
   POETX_ERR_CUDA = 5,            /* a CUDA runtime call or a launch failed */
-  POETX_ERR_TIMEOUT = 6          /* a bounded device-side wait expired */
+  POETX_ERR_TIMEOUT = 6,         /* a bounded device-side wait expired */
+  POETX_ERR_RANGE = 7            /* a value left the range a kernel computes in */
 } poetx_status;
 
 typedef enum { POETX_F32 = 0, POETX_BF16 = 1 } poetx_dtype;
@@ -78,7 +80,11 @@ int poetx_version(void);
 /* Batched CNP: Q_j = (I + K_j)(I + K_j + ... + K_j^n) for j < nb.
  *   theta  [nb, b(b-1)/2] fp32, packed as above (read only)
  *   Q      [nb, b, b] in out_dtype (fp32 or bf16; written)
- *   n >= 1 is the highest Neumann power.  nb == 0 is a no-op. */
+ *   n >= 1 is the highest Neumann power.  nb == 0 is a no-op.
+ * fp32 Q at b = 256 (nb <= 65535) runs on the tensor cores with each chain
+ * value held as two fp16 parts: an intermediate power sum of magnitude
+ * 65504 or more (far outside the series' convergent range) leaves Q
+ * undefined and sets POETX_ERR_RANGE for poetx_stream_status(). */
 poetx_status poetx_cayley_neumann(const float *theta, int nb, int b, int n, void *Q,
                                   poetx_dtype out_dtype, cudaStream_t stream);
 

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libpoetx.so")
 F32, BF16 = 0, 1
 STATUS = {0: "POETX_OK", 1: "POETX_ERR_INVALID_ARG", 2: "POETX_ERR_SHAPE",
           3: "POETX_ERR_UNSUPPORTED", 4: "POETX_ERR_NOT_PERMUTATION", 5: "POETX_ERR_CUDA",
-          6: "POETX_ERR_TIMEOUT"}
+          6: "POETX_ERR_TIMEOUT", 7: "POETX_ERR_RANGE"}
 
 # every symbol include/poetx.h declares
 EXPORTS = ["poetx_status_string", "poetx_version", "poetx_cayley_neumann",

@@ -129,6 +129,7 @@ const char* poetx_status_string(poetx_status s) {
     case POETX_ERR_NOT_PERMUTATION: return "POETX_ERR_NOT_PERMUTATION";
     case POETX_ERR_CUDA: return "POETX_ERR_CUDA";
     case POETX_ERR_TIMEOUT: return "POETX_ERR_TIMEOUT";
+    case POETX_ERR_RANGE: return "POETX_ERR_RANGE";
   }
   return "POETX_ERR_UNKNOWN";
 }

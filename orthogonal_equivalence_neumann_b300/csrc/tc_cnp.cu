@@ -27,6 +27,8 @@
 // once; the chain kernel streams them in by TMA, both sides (P and R) in one
 // launch.  fp32 Q and the fp32 backward entry point use the exact CUDA-core
 // kernels.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "profile.cuh"
 #include "tc.cuh"
@@ -263,13 +265,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 }
 
 // fp32 Q at b = 256 (the three-term split on the tensor cores): the unpack
-// writes Kop = -K as two bf16 parts, hi = bf16(Kop), lo = bf16(Kop - hi), into
-// the block's own fp32 Q buffer, which holds exactly both: viewed as bf16
+// writes Kop = -K as two fp16 parts, hi = fp16(Kop), lo = fp16(Kop - hi), into
+// the block's own fp32 Q buffer, which holds exactly both: viewed as 16-bit
 // [nb * 512][256], block j's hi rows are j * 512 + c and its lo rows
-// j * 512 + 256 + c.  One CTA per 32-row group of one block, the rows
+// j * 512 + 256 + c.  (fp16 parts keep 22 significant bits where bf16 parts
+// would keep 16: at sigma = 0.05 the bf16 split left rows of Q about 1e-5 off,
+// at the fp32 bar; the lo parts of small entries fall into fp16's subnormal
+// range, about 3e-8 absolute, far below that bar relative to Q.)  One CTA per 32-row group of one block, the rows
 // assembled in fp32 in shared memory (row pitch 257 words: the column writes
 // fall in distinct banks); all loads are issued before their stores.
 constexpr int kSplitRows = 32;
+
+// Two fp32 values as fp16 hi parts and fp16 lo parts (x = hi + lo + e,
+// |e| <= 2^-22 |x| above fp16's subnormal range), each pair packed low first.
+__device__ __forceinline__ void split_f16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half ha = __float2half_rn(a), hb = __float2half_rn(b);
+  const __half la = __float2half_rn(a - __half2float(ha)), lb = __float2half_rn(b - __half2float(hb));
+  hi = (uint32_t)__half_as_ushort(ha) | ((uint32_t)__half_as_ushort(hb) << 16);
+  lo = (uint32_t)__half_as_ushort(la) | ((uint32_t)__half_as_ushort(lb) << 16);
+}
 
 __global__ void __launch_bounds__(kUnpackThreads)
     cnp_unpack_split_kernel(FwdSide f0, FwdSide f1) {
@@ -318,31 +332,28 @@ __global__ void __launch_bounds__(kUnpackThreads)
     }
   }
   __syncthreads();
-  __nv_bfloat16* qb = static_cast<__nv_bfloat16*>(sd.Q) + (size_t)j * 512 * B;
+  __half* qb = static_cast<__half*>(sd.Q) + (size_t)j * 512 * B;
   uint32_t* hi = reinterpret_cast<uint32_t*>(qb + (size_t)c0 * B);
   uint32_t* lo = reinterpret_cast<uint32_t*>(qb + (size_t)(B + c0) * B);
   for (int u = threadIdx.x; u < kSplitRows * B / 2; u += kUnpackThreads) {
     const int r = u / (B / 2), c2 = (u % (B / 2)) * 2;
-    const float a = tile[r * LD + c2], b = tile[r * LD + c2 + 1];
-    const __nv_bfloat16 ha = __float2bfloat16_rn(a), hb = __float2bfloat16_rn(b);
-    hi[u] = (uint32_t)__bfloat16_as_ushort(ha) | ((uint32_t)__bfloat16_as_ushort(hb) << 16);
-    lo[u] = pack_bf16x2(a - __bfloat162float(ha), b - __bfloat162float(hb));
+    split_f16x2(tile[r * LD + c2], tile[r * LD + c2 + 1], hi[u], lo[u]);
   }
 }
 
 // fp32 Q at b = 256: one CTA per 128-row slab (the two slabs of a block a
-// cluster), the whole chain on the tensor cores as three bf16 products per
+// cluster), the whole chain on the tensor cores as three fp16 products per
 // step, X_hi K_hi + X_hi K_lo + X_lo K_hi (fp32 accumulation; the dropped
-// X_lo K_lo term is below 2^-16 of the product).  Tensor memory holds the
+// X_lo K_lo term is below 2^-22 of the product).  Tensor memory holds the
 // slab's accumulator (128 x 256 fp32, columns [0, 256)) and X_i as the A
-// operand, hi at [256, 384) and lo at [384, 512) (two bf16 per column), so
+// operand, hi at [256, 384) and lo at [384, 512) (two fp16 per column), so
 // one CTA owns an SM's tensor memory.  Warp 0 streams Kop's hi and lo parts
 // (the B operand: Kop[c][k] = K[k][c], K-major) through a ring of 64-column
 // chunks by TMA, every step (K does not fit in shared memory twice); warp 1
 // issues the products, the 2K term among them as 2I . K over the slab's own
-// K range (2I, 128 x 128 bf16, sits in shared memory beside the ring; 2 * bf16
+// K range (2I, 128 x 128 fp16, sits in shared memory beside the ring; 2 * fp16
 // is exact); warps 2..9 turn the accumulator into the next X, split into its
-// bf16 parts, or, after the last step, into Q = I + X_{n+1}, staged in the
+// fp16 parts, or, after the last step, into Q = I + X_{n+1}, staged in the
 // then idle ring and written
 // by tensor stores once both slabs of the block are past their last read of
 // Kop (cluster barrier): Q overwrites the buffer Kop lives in.
@@ -351,7 +362,7 @@ constexpr int kF32Workers = 256;
 constexpr int kF32Stages = 3;
 constexpr int kF32Chunk = 256 * 64 * 2;            // one part of a 64-column chunk of Kop
 constexpr int kF32Stage = 2 * kF32Chunk;           // hi + lo
-constexpr int kF32TwoI = 128 * 128 * 2;            // 2I over the slab's K range, bf16
+constexpr int kF32TwoI = 128 * 128 * 2;            // 2I over the slab's K range, fp16
 constexpr int kF32Smem = 1024 + kF32Stages * kF32Stage + kF32TwoI + 256;
 
 __global__ void __launch_bounds__(kF32Threads, 1)
@@ -363,7 +374,7 @@ __global__ void __launch_bounds__(kF32Threads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* ring = smem;
-  uint8_t* two_i = smem + kF32Stages * kF32Stage;    // [2 k-chunks][128 rows][64 k] bf16, K-major
+  uint8_t* two_i = smem + kF32Stages * kF32Stage;    // [2 k-chunks][128 rows][64 k] fp16, K-major
   uint64_t* full = reinterpret_cast<uint64_t*>(two_i + kF32TwoI);
   uint64_t* empty = full + kF32Stages;
   uint64_t* acc_full = empty + kF32Stages;
@@ -390,7 +401,7 @@ __global__ void __launch_bounds__(kF32Threads, 1)
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, 512);
-  // 2I: 2.0 (bf16 0x4000) at (r, r) of the slab's K range, zero elsewhere
+  // 2I: 2.0 (fp16 0x4000) at (r, r) of the slab's K range, zero elsewhere
   for (int o = threadIdx.x * 16; o < kF32TwoI; o += kF32Threads * 16)
     *reinterpret_cast<uint4*>(two_i + o) = make_uint4(0, 0, 0, 0);
   __syncthreads();
@@ -433,7 +444,7 @@ __global__ void __launch_bounds__(kF32Threads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------ products
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(128, B, false, false);
+      const uint32_t idesc = idesc_f16(128, B, false, false);
       int it = 0;
       bool pending = false;
       for (int i = 1; i <= n && ok; ++i) {
@@ -477,7 +488,7 @@ __global__ void __launch_bounds__(kF32Threads, 1)
     const int quarter = warp % 4, half = (warp - 2) / 4;
     const int r = quarter * 32 + lane, row = r0 + r;   // TMEM lane, row of the block
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(sd.Q) + (size_t)j * 512 * B;
+    const __half* qb = static_cast<const __half*>(sd.Q) + (size_t)j * 512 * B;
     const uint4* kh = reinterpret_cast<const uint4*>(qb + (size_t)row * B);         // Kop hi row
     const uint4* kl = reinterpret_cast<const uint4*>(qb + (size_t)(B + row) * B);   // Kop lo row
     // X_1 = K on the slab rows: -Kop (both parts negate exactly)
@@ -510,12 +521,13 @@ __global__ void __launch_bounds__(kF32Threads, 1)
         for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(acc[e]);
         if (i < n) {
           uint32_t h[16], l[16];
+          float big = 0.f;
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const __nv_bfloat16 a = __float2bfloat16_rn(x[2 * e]), b = __float2bfloat16_rn(x[2 * e + 1]);
-            h[e] = (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
-            l[e] = pack_bf16x2(x[2 * e] - __bfloat162float(a), x[2 * e + 1] - __bfloat162float(b));
+            split_f16x2(x[2 * e], x[2 * e + 1], h[e], l[e]);
+            big = fmaxf(big, fmaxf(fabsf(x[2 * e]), fabsf(x[2 * e + 1])));
           }
+          if (big >= 65504.f) raise_device_error(err, POETX_ERR_RANGE);   // beyond fp16
           tmem_st16(x_hi + lane_off + (uint32_t)(c0 / 2), h);
           tmem_st16(x_lo + lane_off + (uint32_t)(c0 / 2), l);
         } else {
@@ -1209,12 +1221,12 @@ poetx_status cnp_fwd_f32_launch(const float* theta0, int nb0, const float* theta
   FwdSide f0{theta0, Q0, nb0}, f1{theta1, Q1, nb1};
   const FwdSide& t1 = nb1 > 0 ? f1 : f0;
   const FwdSide& t0 = nb0 > 0 ? f0 : f1;
-  // Kop hi / lo in the Q buffers as bf16 [nb * 512][256]; Q as fp32 [nb * 256][256]
+  // Kop hi / lo in the Q buffers as fp16 [nb * 512][256]; Q as fp32 [nb * 256][256]
   CUtensorMap tk0, tk1, tq0, tq1;
   const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
-  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-  if (!make_tmap_2d(&tk0, t0.Q, bf, 2, (uint64_t)t0.nb * 512, 256, 256, 64, sw) ||
-      !make_tmap_2d(&tk1, t1.Q, bf, 2, (uint64_t)t1.nb * 512, 256, 256, 64, sw) ||
+  const CUtensorMapDataType h16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16, f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  if (!make_tmap_2d(&tk0, t0.Q, h16, 2, (uint64_t)t0.nb * 512, 256, 256, 64, sw) ||
+      !make_tmap_2d(&tk1, t1.Q, h16, 2, (uint64_t)t1.nb * 512, 256, 256, 64, sw) ||
       !make_tmap_2d(&tq0, t0.Q, f32, 4, (uint64_t)t0.nb * 256, 256, 128, 32, sw) ||
       !make_tmap_2d(&tq1, t1.Q, f32, 4, (uint64_t)t1.nb * 256, 256, 128, 32, sw))
     return POETX_ERR_CUDA;

@@ -14,7 +14,7 @@
 //    is stored as 64-element x 8-row atoms (SBO = stride between 8-row K
 //    groups, LBO = stride between 64-element MN chunks).
 //  * instruction descriptor (32 bit): D format in [4,6) (1 = f32), A format
-//    in [7,10) and B format in [10,13) (kind::f16: 1 = bf16),
+//    in [7,10) and B format in [10,13) (kind::f16: 0 = fp16, 1 = bf16),
 //    A / B major in bits 15 / 16 (1 = MN-major), N >> 3 in [17,23),
 //    M >> 4 in [24,29).
 #pragma once
@@ -261,6 +261,12 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
   d |= (uint64_t)1 << 46;   // descriptor version
   d |= (uint64_t)2 << 61;   // 128-byte swizzle
   return d;
+}
+
+// kind::f16 with fp16 A and B, f32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // kind::f16 with bf16 A and B, f32 accumulator.

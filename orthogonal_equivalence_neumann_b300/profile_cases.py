@@ -7,8 +7,9 @@
         GEMMs and the dQ token sums once or twice; prints the library's
         per-kernel times of the last three steps (CUDA event pairs).
     python -m orthogonal_equivalence_neumann_b300.profile_cases cnp
-        three Cayley-Neumann calls at each of three sweep points (4096 blocks,
-        n = 3, sigma = 1e-2: b = 128 bf16, b = 128 fp32, b = 32 bf16).
+        three Cayley-Neumann calls at each of four sweep points (4096 blocks,
+        n = 3, sigma = 1e-2: b = 128 bf16, b = 128 fp32, b = 32 bf16,
+        b = 256 fp32).
     python -m orthogonal_equivalence_neumann_b300.profile_cases gate|down|upproj
         the same six steps as ``layer`` for one of the wide shapes: the MLP
         gate / up projection 2048 -> 5632 and the down projection 5632 -> 2048
@@ -63,7 +64,8 @@ def layer_steps(what="layer", warm=3, timed=3):
 
 
 def cnp_points(calls=3):
-    for b, dt in ((128, torch.bfloat16), (128, torch.float32), (32, torch.bfloat16)):
+    for b, dt in ((128, torch.bfloat16), (128, torch.float32), (32, torch.bfloat16),
+                  (256, torch.float32)):
         th = inputs.make_theta(4096, b, 1e-2, inputs.sweep_seed(b, 1e-2, 3)).cuda()
         Q = torch.empty(4096, b, b, dtype=dt, device="cuda")
         for _ in range(calls):
