@@ -16,9 +16,9 @@
         of the 1B-style stack (b = 256, 8192 tokens), or the up-projection
         layer 2048 -> 5632 at b = 128 with 16384 tokens.
 
-Both hold a few hundred MB on the device and run in seconds, so a profiler
-can capture one launch of a chosen kernel (e.g. ``ncu -k regex:<name> -s 2
--c 1``) without replaying a long program.  Inputs are the seeded synthetic
+Each holds a few hundred MB on the device (the b = 256 fp32 point 1.6 GB)
+and runs in seconds, so a profiler can capture one launch of a chosen kernel
+(e.g. ``ncu -k regex:<name> -s 2 -c 1``) without replaying a long program.  Inputs are the seeded synthetic
 draws of ``inputs``.
 """
 import sys
