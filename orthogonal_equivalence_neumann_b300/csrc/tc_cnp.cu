@@ -385,7 +385,6 @@ __global__ void __launch_bounds__(kF32Threads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const bool second = (int)blockIdx.y >= f0.nb;
   const int j = second ? (int)blockIdx.y - f0.nb : (int)blockIdx.y;
-  const FwdSide& sd = second ? f1 : f0;
   const CUtensorMap* tk = second ? &tk1 : &tk0;
   const CUtensorMap* tq = second ? &tq1 : &tq0;
   const int r0 = blockIdx.x * 128;
@@ -445,6 +444,9 @@ __global__ void __launch_bounds__(kF32Threads, 1)
     // ------------------------------------------------ products
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(128, B, false, false);
+      // the first step's A is X_1 = K = -Kop: the slab's own rows of each
+      // chunk of Kop, read with the instruction's negate-A bit (bit 13)
+      const uint32_t idesc_neg = idesc | (1u << 13);
       int it = 0;
       bool pending = false;
       for (int i = 1; i <= n && ok; ++i) {
@@ -460,9 +462,17 @@ __global__ void __launch_bounds__(kF32Threads, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t xa = (uint32_t)(32 * c + 8 * kk);   // (64 c + 16 kk) / 2
-            mma_bf16_ts(tmem, x_hi + xa, sw128_desc(bh + kk * 32, 16, 1024), idesc, (c | kk) != 0);
-            mma_bf16_ts(tmem, x_hi + xa, sw128_desc(bl + kk * 32, 16, 1024), idesc, 1);
-            mma_bf16_ts(tmem, x_lo + xa, sw128_desc(bh + kk * 32, 16, 1024), idesc, 1);
+            if (i == 1) {
+              const uint64_t ah = sw128_desc(bh + r0 * 128 + kk * 32, 16, 1024);
+              const uint64_t al = sw128_desc(bl + r0 * 128 + kk * 32, 16, 1024);
+              mma_bf16(tmem, ah, sw128_desc(bh + kk * 32, 16, 1024), idesc_neg, (c | kk) != 0);
+              mma_bf16(tmem, ah, sw128_desc(bl + kk * 32, 16, 1024), idesc_neg, 1);
+              mma_bf16(tmem, al, sw128_desc(bh + kk * 32, 16, 1024), idesc_neg, 1);
+            } else {
+              mma_bf16_ts(tmem, x_hi + xa, sw128_desc(bh + kk * 32, 16, 1024), idesc, (c | kk) != 0);
+              mma_bf16_ts(tmem, x_hi + xa, sw128_desc(bl + kk * 32, 16, 1024), idesc, 1);
+              mma_bf16_ts(tmem, x_lo + xa, sw128_desc(bh + kk * 32, 16, 1024), idesc, 1);
+            }
             if (ci == 0 || ci == 1) {
               const uint64_t ad = sw128_desc(smem_u32(two_i) + ci * (128 * 128) + kk * 32, 16, 1024);
               mma_bf16(tmem, ad, sw128_desc(bh + kk * 32, 16, 1024), idesc, 1);
@@ -488,25 +498,7 @@ __global__ void __launch_bounds__(kF32Threads, 1)
     const int quarter = warp % 4, half = (warp - 2) / 4;
     const int r = quarter * 32 + lane, row = r0 + r;   // TMEM lane, row of the block
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const __half* qb = static_cast<const __half*>(sd.Q) + (size_t)j * 512 * B;
-    const uint4* kh = reinterpret_cast<const uint4*>(qb + (size_t)row * B);         // Kop hi row
-    const uint4* kl = reinterpret_cast<const uint4*>(qb + (size_t)(B + row) * B);   // Kop lo row
-    // X_1 = K on the slab rows: -Kop (both parts negate exactly)
-    for (int c0 = half * 128; c0 < half * 128 + 128; c0 += 32) {
-      uint32_t h[16], l[16];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 a = kh[c0 / 8 + q], b = kl[c0 / 8 + q];
-        h[4 * q] = a.x ^ 0x80008000u; h[4 * q + 1] = a.y ^ 0x80008000u;
-        h[4 * q + 2] = a.z ^ 0x80008000u; h[4 * q + 3] = a.w ^ 0x80008000u;
-        l[4 * q] = b.x ^ 0x80008000u; l[4 * q + 1] = b.y ^ 0x80008000u;
-        l[4 * q + 2] = b.z ^ 0x80008000u; l[4 * q + 3] = b.w ^ 0x80008000u;
-      }
-      tmem_st16(x_hi + lane_off + (uint32_t)(c0 / 2), h);
-      tmem_st16(x_lo + lane_off + (uint32_t)(c0 / 2), l);
-    }
-    tmem_st_wait();
-    tc_fence_before();
+    // X_1 needs no conversion (the first products read it from the ring)
     mbar_arrive(x_ready);
     for (int i = 1; i <= n && ok; ++i) {
       if (!(ok = mbar_wait(acc_full, (uint32_t)(i - 1) & 1, err))) break;
