@@ -414,8 +414,8 @@ def cnp_roofline_point(b, out_bytes, n, nblocks, seconds, peaks):
     """Roofline of one Cayley-Neumann generation call: algorithmic bytes (packed
     theta in, Q out) and flops (n products of b x b x b per block) against the
     measured HBM peak and the peak of the unit the products run on: bf16 Q on
-    the bf16 tensor cores; fp32 Q on the tensor cores as three bf16 MMA chains
-    per product (so a third of the bf16 peak)."""
+    the bf16 tensor cores; fp32 Q on the tensor cores as three MMA chains of
+    fp16 parts per product (so a third of the 16-bit peak)."""
     byts = nblocks * (4 * (b * (b - 1) // 2) + out_bytes * b * b)
     flops = nblocks * 2.0 * n * b ** 3
     t_hbm = byts / (peaks["hbm_gbs"] * 1e9)

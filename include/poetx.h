@@ -81,10 +81,11 @@ int poetx_version(void);
  *   theta  [nb, b(b-1)/2] fp32, packed as above (read only)
  *   Q      [nb, b, b] in out_dtype (fp32 or bf16; written)
  *   n >= 1 is the highest Neumann power.  nb == 0 is a no-op.
- * fp32 Q at b = 256 (nb <= 65535) runs on the tensor cores with each chain
- * value held as two fp16 parts: an intermediate power sum of magnitude
- * 65504 or more (far outside the series' convergent range) leaves Q
- * undefined and sets POETX_ERR_RANGE for poetx_stream_status(). */
+ * fp32 Q at b in {32, 64, 128, 256} (at b = 256: nb <= 65535) runs on the
+ * tensor cores with each chain value held as two fp16 parts: an intermediate
+ * power sum of magnitude 65504 or more (far outside the series' convergent
+ * range) leaves Q undefined and sets POETX_ERR_RANGE for
+ * poetx_stream_status(). */
 poetx_status poetx_cayley_neumann(const float *theta, int nb, int b, int n, void *Q,
                                   poetx_dtype out_dtype, cudaStream_t stream);
 

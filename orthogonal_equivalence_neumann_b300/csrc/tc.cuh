@@ -111,16 +111,16 @@ poetx_status permute_cols_bf16(const void* in, void* out, const int32_t* perm, i
 
 // Cayley-Neumann forward for b in {32, 64, 128}: the parameters unpacked in
 // shared memory, 128 / b blocks per 128-row tile (block-diagonal), bf16 Q
-// from bf16 operands or fp32 Q from a three-term bf16 split of every
-// operand; both factors of a layer in one launch (nb0 or nb1 may be 0).  Any
-// block count.
+// from bf16 operands or fp32 Q from a three-term split of every operand
+// into fp16 parts; both factors of a layer in one launch (nb0 or nb1 may be
+// 0).  Any block count.
 bool cnp_tile_supported(int b);
 poetx_status cnp_tile_fwd(const float* theta0, int nb0, const float* theta1, int nb1, int b, int n,
                           void* Q0, void* Q1, bool out_f32, cudaStream_t s);
 
 // Cayley-Neumann forward / backward with bf16 operands and fp32 accumulation
 // (tcgen05), b in {128, 256}; the forward also gives fp32 Q at b = 256 (each
-// product as three bf16 products of split operands).  The backward
+// product as three products of the operands' fp16 parts).  The backward
 // overwrites dtheta.
 bool cnp_supported(int b);
 poetx_status cnp_fwd_bf16ops(const float* theta, int nb, int b, int n, void* Q, bool out_f32,

@@ -22,14 +22,16 @@
 //            in TMEM; 2 * bf16 is exact), so the accumulator is X_{i+1} as
 //            it stands; at b = 32 it is added in fp32 from K when the
 //            accumulator is read;
-//   fp32 Q:  every operand split into two bf16 parts, x = hi + lo with
-//            hi = bf16(x), lo = bf16(x - hi), and each product taken as
-//            X_hi K_hi + X_hi K_lo + X_lo K_hi (the lo * lo term, 2^-16 of
+//   fp32 Q:  every operand split into two fp16 parts, x = hi + lo with
+//            hi = fp16(x), lo = fp16(x - hi), and each product taken as
+//            X_hi K_hi + X_hi K_lo + X_lo K_hi (the lo * lo term, 2^-22 of
 //            the product, is dropped) -- three MMA chains per step; the 2K
 //            term is added in fp32 from K's hi + lo parts when the
-//            accumulator is read.  This keeps about 16 significant bits per
-//            operand (relative error of Q below 1e-6 at the sweep's sizes,
-//            against the fp32 bar of 1e-5).
+//            accumulator is read.  This keeps about 22 significant bits per
+//            operand (the lo parts of small entries fall into fp16's
+//            subnormal range, about 3e-8 absolute: far below the fp32 bar
+//            of 1e-5 relative to Q; bf16 parts, 16 bits, would leave rows
+//            of Q some 6e-6 off at sigma = 0.05).
 // Operands: B[k][c] = K[k][c], stored as S = -K = K^T (row c of S is column
 // c of K), K-major with the 128-byte swizzle, in shared memory; the first
 // product reads A = X_1 = K as the same S through a transposed (MN-major)
@@ -48,6 +50,8 @@
 // each barrier and the CTA follows through a CTA barrier; every wait is
 // bounded (tc_ptx.cuh).
 #include <cstring>
+
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "profile.cuh"
@@ -77,15 +81,12 @@ __device__ __forceinline__ uint32_t op_off(int r, int k) {
                     ((((k & 63) >> 3) ^ (r & 7)) << 4) + (k & 7) * 2);
 }
 
-__device__ __forceinline__ uint32_t bf16_bits(float v) {
-  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v));
-}
-
-// hi = bf16(v), lo = bf16(v - hi) as 16-bit patterns.
-__device__ __forceinline__ void split_bf16(float v, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(v);
-  hi = (uint32_t)__bfloat16_as_ushort(h);
-  lo = bf16_bits(v - __bfloat162float(h));
+// hi = fp16(v), lo = fp16(v - hi) as 16-bit patterns (v = hi + lo + e,
+// |e| <= 2^-22 |v| above fp16's subnormal range).
+__device__ __forceinline__ void split_f16(float v, uint32_t& hi, uint32_t& lo) {
+  const __half h = __float2half_rn(v);
+  hi = (uint32_t)__half_as_ushort(h);
+  lo = (uint32_t)__half_as_ushort(__float2half_rn(v - __half2float(h)));
 }
 
 // 8 bf16 of a 16-byte unit, widened.
@@ -95,6 +96,17 @@ __device__ __forceinline__ void widen8(const uint4 u, float* v) {
   for (int e = 0; e < 4; ++e) {
     v[2 * e] = __uint_as_float(w[e] << 16);
     v[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+  }
+}
+
+// 8 fp16 of a 16-byte unit, widened.
+__device__ __forceinline__ void widen8_f16(const uint4 u, float* v) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+    v[2 * e] = f.x;
+    v[2 * e + 1] = f.y;
   }
 }
 
@@ -122,7 +134,8 @@ struct TileGeo {
   static constexpr bool two_i_mma = !F32 && B >= 64;
 };
 
-// -x for each bf16 of a pair that is not zero (zeros keep their +0 pattern).
+// -x for each 16-bit float of a pair that is not zero (bf16 or fp16: the sign
+// is bit 15; zeros keep their +0 pattern).
 __device__ __forceinline__ uint32_t neg_nonzero(uint32_t h) {
   return h ^ (((h & 0x7fff7fffu) + 0x7fff7fffu) & 0x80008000u);
 }
@@ -157,7 +170,7 @@ __device__ __forceinline__ void unpack_unit(int u, const float* th_tile, int nbt
   // theta(i, j) sits at skew_row_off(i) + j - i - 1
   const int i = a + (lane >> 2), cp = 2 * (lane & 3);
   const float* th = th_tile + (live ? gb : 0) * Geo::P + (skew_row_off(i, B) - i - 1 + 32 * J + cp);
-  uint32_t h[4], l[4];   // M_q as bf16 pairs [hi, lo]
+  uint32_t h[4], l[4];   // M_q as 16-bit pairs: bf16, or fp16 [hi, lo] parts for fp32 Q
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     float v[2];
@@ -168,8 +181,8 @@ __device__ __forceinline__ void unpack_unit(int u, const float* th_tile, int nbt
     }
     if constexpr (F32) {
       uint32_t h0, l0, h1, l1;
-      split_bf16(v[0], h0, l0);
-      split_bf16(v[1], h1, l1);
+      split_f16(v[0], h0, l0);
+      split_f16(v[1], h1, l1);
       h[q] = h0 | (h1 << 16);
       l[q] = l0 | (l1 << 16);
     } else {
@@ -338,8 +351,9 @@ __global__ void __launch_bounds__(kTileThreads, 2)
         const uint32_t sh = smem_u32(s_hi), sl = smem_u32(s_lo);
         // block-diagonal products: block gq's output columns (N = B) from
         // its own K range only (the rest of X's rows there are zero)
-        const uint32_t id_kk = idesc_bf16(128, B, false, false);
-        const uint32_t id_mk = idesc_bf16(128, B, true, false);
+        // fp32 Q: the operands' parts are fp16
+        const uint32_t id_kk = F32 ? idesc_f16(128, B, false, false) : idesc_bf16(128, B, false, false);
+        const uint32_t id_mk = F32 ? idesc_f16(128, B, true, false) : idesc_bf16(128, B, true, false);
         // descriptors of S at an offset: the start-address field of the base
         // descriptor plus offset / 16 (shared addresses stay below 2^18, so
         // the 14-bit field never carries)
@@ -409,14 +423,16 @@ __global__ void __launch_bounds__(kTileThreads, 2)
 #pragma unroll
           for (int q = 0; q < W / 8; ++q) {
             const uint32_t off = op_off(r, g * B + c0 + 8 * q);
-            widen8(*reinterpret_cast<const uint4*>(s_hi + off), k2 + 8 * q);
             if constexpr (F32) {
               float lo[8];
-              widen8(stage_f32 && c0 != half * HC ? lo_next[q]
-                                                  : *reinterpret_cast<const uint4*>(s_lo + off),
-                     lo);
+              widen8_f16(*reinterpret_cast<const uint4*>(s_hi + off), k2 + 8 * q);
+              widen8_f16(stage_f32 && c0 != half * HC ? lo_next[q]
+                                                      : *reinterpret_cast<const uint4*>(s_lo + off),
+                         lo);
 #pragma unroll
               for (int e = 0; e < 8; ++e) k2[8 * q + e] += lo[e];
+            } else {
+              widen8(*reinterpret_cast<const uint4*>(s_hi + off), k2 + 8 * q);
             }
           }
           tmem_ld_wait();
@@ -433,18 +449,21 @@ __global__ void __launch_bounds__(kTileThreads, 2)
         if (i < n) {
           // X_{i+1} into tensor memory: row r, columns g*B + c0 .. (two per 32-bit column)
           uint32_t h[W / 2], l[W / 2];
+          float big = 0.f;
 #pragma unroll
           for (int e = 0; e < W / 2; ++e) {
             if constexpr (F32) {
               uint32_t h0, l0, h1, l1;
-              split_bf16(x[2 * e], h0, l0);
-              split_bf16(x[2 * e + 1], h1, l1);
+              split_f16(x[2 * e], h0, l0);
+              split_f16(x[2 * e + 1], h1, l1);
               h[e] = h0 | (h1 << 16);
               l[e] = l0 | (l1 << 16);
+              big = fmaxf(big, fmaxf(fabsf(x[2 * e]), fabsf(x[2 * e + 1])));
             } else {
               h[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
             }
           }
+          if (F32 && big >= 65504.f) raise_device_error(err, POETX_ERR_RANGE);   // beyond fp16
           const uint32_t tx = lane_off + (uint32_t)((g * B + c0) / 2);
           if constexpr (W == 32) {
             tmem_st16(x_hi + tx, h);
