@@ -489,6 +489,26 @@ def test_wide_stack_layers_run_on_the_staged_applies(which):
     assert not any(n.startswith("tc_blockapply") or n.endswith("_simt") for n in names), sorted(names)
 
 
+@pytest.mark.parametrize("b", [32, 256])
+def test_cnp_fp32_chain_beyond_fp16_range_reports_a_status(b):
+    """fp32 Q on the tensor cores holds chain values as two fp16 parts: a
+    chain far outside the series' convergent range (sigma = 10, values past
+    65504) is reported as POETX_ERR_RANGE by the next status read, and the
+    context stays usable (the next call in range is checked against the
+    oracle)."""
+    Q = torch.empty(4, b, b, dtype=torch.float32, device="cuda")
+    _lib.poetx_stream_status()
+    _lib.poetx_cayley_neumann(inputs.make_theta(4, b, 10.0, 93).cuda(), b, 3, Q)
+    torch.cuda.synchronize()
+    with pytest.raises(_lib.PoetxError) as e:
+        _lib.poetx_stream_status()
+    assert e.value.code == 7
+    th = inputs.make_theta(4, b, 1e-2, 94)
+    _lib.poetx_cayley_neumann(th.cuda(), b, 3, Q)
+    _lib.poetx_stream_status()
+    assert_close("Q", to64(Q), oracle.cnp(th.double().numpy(), b, 3), TOL_F32)
+
+
 @pytest.mark.parametrize("nb_P,nb_R", [(3, 0), (2, 5)])
 def test_cnp_fp32_b256_runs_on_the_tensor_cores(nb_P, nb_R):
     """fp32 Q of 256-blocks: the split unpack and the three-term chain on the
