@@ -152,7 +152,8 @@ __global__ void __launch_bounds__(kUnpackThreads)
 // where the unpack kernel left it; once every slab of the block holds it
 // (cluster barrier) the buffer may be overwritten with Q.  The steps
 //   X_1 = K,  X_{i+1} = X_i K + 2K,  Q = I + X_n K + 2K
-// add 2K from the same bf16 operand (the output is bf16).
+// add 2K from the same bf16 operand (the output is bf16); the first step's A
+// is the slab's rows of Kop itself, negated by the instruction.
 template <int B>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     cnp_fwd_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_constant__ CUtensorMap tk1,
@@ -198,29 +199,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int i = 1; i <= n; ++i) {
         if (!mbar_wait(afull, (i - 1) & 1, err)) break;
         tc_fence_after();
+        // step 1: A = X_1 = K = -Kop on the slab rows, read from Kop itself
+        // with the instruction's negate-A bit (bit 13)
+        const uint32_t a0 = i == 1 ? bb + (uint32_t)r0 * 128 : ab;
+        const uint32_t a_chunk = i == 1 ? B * 128 : 128 * 128;
+        const uint32_t id = i == 1 ? (idesc | (1u << 13)) : idesc;
 #pragma unroll
         for (int kc = 0; kc < B / 64; ++kc)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tmem_base, sw128_desc(ab + kc * 128 * 128 + kk * 32, 16, 1024),
-                     sw128_desc(bb + kc * B * 128 + kk * 32, 16, 1024), idesc, (kc | kk) != 0);
+            mma_bf16(tmem_base, sw128_desc(a0 + kc * a_chunk + kk * 32, 16, 1024),
+                     sw128_desc(bb + kc * B * 128 + kk * 32, 16, 1024), id, (kc | kk) != 0);
         mma_commit(stepdone);
       }
     }
   } else if (ok) {
-    const int wt = threadIdx.x - 32;
     const int quarter = warp % 4;
     const int half = (warp - 1) / 4;
     const int r = quarter * 32 + lane;
     const int row = r0 + r;
-    // ---- X_1 = K on the slab rows: A[r][k] = K[r0+r][k] = -Kop[r0+r][k]
-    for (int u = wt; u < 128 * (B / 8); u += kFwdWorkers) {
-      const int rr = u / (B / 8), k8 = (u % (B / 8)) * 8;
-      uint4 w = *reinterpret_cast<const uint4*>(kop + sw128_offset(r0 + rr, k8, B));
-      w.x ^= 0x80008000u; w.y ^= 0x80008000u; w.z ^= 0x80008000u; w.w ^= 0x80008000u;
-      *reinterpret_cast<uint4*>(amat + sw128_offset(rr, k8, 128)) = w;
-    }
-    fence_proxy_async_smem();
+    // X_1 = K needs no copy: the first products read it from Kop (negated)
     mbar_arrive(afull);
     // ---- X_{i+1} = X_i K + 2K (as the next A operand), and finally Q = I + X_n K + 2K
     for (int i = 2; i <= n + 1 && ok; ++i) {
